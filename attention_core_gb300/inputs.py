@@ -1,0 +1,104 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the smoke check.
+
+This module holds no arithmetic of the attention core: it only draws random
+numbers and lays out fixed probe patterns.  Both the CUDA path and the CPU
+oracle receive exactly the tensors built here.
+
+Recipe for the random inputs: a CPU ``torch.Generator`` seeded with the given
+seed draws Q, K, V and dO, in that order, as fp32 N(0, 1) and rounds each to
+bf16 (round to nearest even).  The same bf16 bits go to the GPU and, widened
+exactly to fp64, to the oracle.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+# Named workloads: the GPT-3-style layers of the paper (one tensor-parallel
+# rank of eight, so local heads = heads / 8) and a Llama-3-70B-shaped layer.
+# Fields: b, h_q, h_kv, s, d, p_drop.
+WORKLOADS = {
+    "tiny": dict(b=1, h_q=2, h_kv=2, s=128, d=64, p_drop=0.1),
+    "gpt22b": dict(b=4, h_q=8, h_kv=8, s=2048, d=96, p_drop=0.1),
+    "gpt175b": dict(b=2, h_q=12, h_kv=12, s=2048, d=128, p_drop=0.1),
+    "gpt530b": dict(b=1, h_q=16, h_kv=16, s=2048, d=160, p_drop=0.1),
+    "llama70b_p0": dict(b=1, h_q=64, h_kv=8, s=8192, d=128, p_drop=0.0),
+    "llama70b_p01": dict(b=1, h_q=64, h_kv=8, s=8192, d=128, p_drop=0.1),
+}
+
+
+@dataclass
+class Tensors:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    dout: torch.Tensor
+
+
+def random_inputs(b: int, h_q: int, h_kv: int, s: int, d: int, seed: int) -> Tensors:
+    """bf16 Q [b,h_q,s,d], K/V [b,h_kv,s,d], dO [b,h_q,s,d], all N(0,1), on the CPU."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((b, h_q, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((b, h_kv, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((b, h_kv, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dout = torch.randn((b, h_q, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return Tensors(q, k, v, dout)
+
+
+def fwd_mask_probe(b: int, h_q: int, h_kv: int, s: int, d: int, w0: int) -> Tensors:
+    """Inputs that expose the forward dropout mask on a window of keys.
+
+    Q = K = 0 makes every visible score equal, and V row j is the unit vector
+    e_(j - w0) for keys j in [w0, w0 + d) (zero elsewhere), so output column c
+    of query row i is non-zero exactly when key w0 + c is visible to row i
+    and kept by dropout.
+    """
+    q = torch.zeros((b, h_q, s, d), dtype=torch.bfloat16)
+    k = torch.zeros((b, h_kv, s, d), dtype=torch.bfloat16)
+    v = torch.zeros((b, h_kv, s, d), dtype=torch.bfloat16)
+    for c in range(d):
+        j = w0 + c
+        if j < s:
+            v[:, :, j, c] = 1.0
+    dout = torch.zeros((b, h_q, s, d), dtype=torch.bfloat16)
+    return Tensors(q, k, v, dout)
+
+
+def dv_mask_probe(b: int, h_q: int, h_kv: int, s: int, d: int, w0: int) -> Tensors:
+    """Inputs that expose the backward dropout mask through dV.
+
+    Q = K = 0 (equal scores), V = 0, and dO row i is e_(i - w0) for query
+    rows i in [w0, w0 + d): column c of dV row j then collects only the
+    probability of (query w0 + c, key j), non-zero exactly when that pair is
+    visible and kept.  Use with one query head per KV head (h_q == h_kv).
+    """
+    q = torch.zeros((b, h_q, s, d), dtype=torch.bfloat16)
+    k = torch.zeros((b, h_kv, s, d), dtype=torch.bfloat16)
+    v = torch.zeros((b, h_kv, s, d), dtype=torch.bfloat16)
+    dout = torch.zeros((b, h_q, s, d), dtype=torch.bfloat16)
+    for c in range(d):
+        i = w0 + c
+        if i < s:
+            dout[:, :, i, c] = 1.0
+    return Tensors(q, k, v, dout)
+
+
+def dq_mask_probe(b: int, h_q: int, h_kv: int, s: int, d: int, w0: int) -> Tensors:
+    """Inputs that make dQ depend on the dropout mask of a window of keys.
+
+    Q = 0 (equal scores), V rows and dO rows all e_0, and K row j is
+    e_(j - w0) for keys in [w0, w0 + d): dQ column c of row i then takes one
+    of two well-separated values depending on whether key w0 + c was kept.
+    """
+    q = torch.zeros((b, h_q, s, d), dtype=torch.bfloat16)
+    k = torch.zeros((b, h_kv, s, d), dtype=torch.bfloat16)
+    v = torch.zeros((b, h_kv, s, d), dtype=torch.bfloat16)
+    dout = torch.zeros((b, h_q, s, d), dtype=torch.bfloat16)
+    v[..., 0] = 1.0
+    dout[..., 0] = 1.0
+    for c in range(d):
+        j = w0 + c
+        if j < s:
+            k[:, :, j, c] = 1.0
+    return Tensors(q, k, v, dout)

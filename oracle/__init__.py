@@ -1,0 +1,231 @@
+"""CPU oracle for the attention core (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package.  The product library never does: it shares
+no code with this package, and this package imports nothing from the product.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows or
+heads).  This module compiles it with gcc and exposes it through ctypes with
+numpy float64 arrays.  See the header of ``attn_oracle.c`` for what each
+function computes and which passage of the pages it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
+                ("s", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("p_drop", ctypes.c_float), ("scale", ctypes.c_float),
+                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
+class _Bytes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in
+                ("layer_none", "layer_selective", "layer_full", "core_scores_avoided",
+                 "core_kept", "core_recompute_state")]
+
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
+_U32 = ctypes.POINTER(ctypes.c_uint32)
+_PP = ctypes.POINTER(_Params)
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_philox4x32_10.argtypes = [_U32, _U32, _U32]
+        lib.oracle_drop_threshold.argtypes = [ctypes.c_float]
+        lib.oracle_drop_threshold.restype = ctypes.c_uint32
+        lib.oracle_draw16.argtypes = [_PP, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_draw16.restype = ctypes.c_uint32
+        lib.oracle_keep.argtypes = [_PP, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_keep.restype = ctypes.c_int
+        lib.oracle_resolved_scale.argtypes = [_PP]
+        lib.oracle_resolved_scale.restype = ctypes.c_double
+        lib.oracle_fwd.argtypes = [_PP, _D, _D, _D, _D, _D]
+        lib.oracle_fwd_rows.argtypes = [_PP, _D, _D, _D, ctypes.c_int64, _I64, _I64, _D, _D]
+        lib.oracle_head_matrices.argtypes = [_PP, _D, _D, ctypes.c_int64, _D, _D, _U8]
+        lib.oracle_mask_rows.argtypes = [_PP, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _U8]
+        lib.oracle_bwd.argtypes = [_PP, _D, _D, _D, _D, _D, _D, _D]
+        lib.oracle_dq_rows.argtypes = [_PP, _D, _D, _D, _D, ctypes.c_int64, _I64, _I64, _D]
+        lib.oracle_dkdv_rows.argtypes = [_PP, _D, _D, _D, _D, ctypes.c_int64, _I64, _I64, _D, _D]
+        lib.oracle_stored_bytes.argtypes = [_PP, ctypes.POINTER(_Bytes)]
+        _lib = lib
+    return _lib
+
+
+@dataclass
+class Problem:
+    """Shape and method parameters of one attention-core call."""
+    b: int
+    h_q: int
+    h_kv: int
+    s: int
+    d: int
+    causal: bool = True
+    p_drop: float = 0.0
+    scale: float = 0.0      # <= 0: 1/sqrt(d) rounded to fp32
+    seed: int = 0
+    offset: int = 0
+
+    def _c(self) -> _Params:
+        return _Params(self.b, self.h_q, self.h_kv, self.s, self.d, int(bool(self.causal)),
+                       float(self.p_drop), float(self.scale), int(self.seed) & (2**64 - 1),
+                       int(self.offset) & (2**64 - 1))
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening of a tensor or array (bf16 widens exactly) to contiguous fp64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _dp(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def _ip(a: np.ndarray):
+    return a.ctypes.data_as(_I64)
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox-4x32-10 of a 4-word counter and 2-word key (SC'11 definition)."""
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(c.ctypes.data_as(_U32), k.ctypes.data_as(_U32), out.ctypes.data_as(_U32))
+    return out
+
+
+def drop_threshold(p_drop: float) -> int:
+    return int(_load().oracle_drop_threshold(ctypes.c_float(p_drop)))
+
+
+def draw16(pr: Problem, bh: int, i: int, j: int) -> int:
+    return int(_load().oracle_draw16(ctypes.byref(pr._c()), bh, i, j))
+
+
+def keep(pr: Problem, bh: int, i: int, j: int) -> int:
+    return int(_load().oracle_keep(ctypes.byref(pr._c()), bh, i, j))
+
+
+def resolved_scale(pr: Problem) -> float:
+    return float(_load().oracle_resolved_scale(ctypes.byref(pr._c())))
+
+
+def fwd(pr: Problem, q, k, v):
+    """Full forward: returns (O [b,h_q,s,d] fp64, LSE [b,h_q,s] fp64)."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    o = np.zeros((pr.b, pr.h_q, pr.s, pr.d))
+    lse = np.zeros((pr.b, pr.h_q, pr.s))
+    lib.oracle_fwd(ctypes.byref(pr._c()), _dp(q), _dp(k), _dp(v), _dp(o), _dp(lse))
+    return o, lse
+
+
+def fwd_rows(pr: Problem, q, k, v, bh, rows):
+    """Forward for sampled (flattened query head, row) pairs: (O [n,d], LSE [n])."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bh = np.ascontiguousarray(np.asarray(bh, dtype=np.int64))
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = len(rows)
+    o = np.zeros((n, pr.d))
+    lse = np.zeros(n)
+    lib.oracle_fwd_rows(ctypes.byref(pr._c()), _dp(q), _dp(k), _dp(v), n, _ip(bh), _ip(rows),
+                        _dp(o), _dp(lse))
+    return o, lse
+
+
+def head_matrices(pr: Problem, q, k, bh: int):
+    """Dense S, P (fp64, s x s) and keep mask M (uint8) of one query head."""
+    lib = _load()
+    q, k = _f64(q), _f64(k)
+    S = np.zeros((pr.s, pr.s))
+    P = np.zeros((pr.s, pr.s))
+    M = np.zeros((pr.s, pr.s), dtype=np.uint8)
+    lib.oracle_head_matrices(ctypes.byref(pr._c()), _dp(q), _dp(k), bh, _dp(S), _dp(P),
+                             M.ctypes.data_as(_U8))
+    return S, P, M
+
+
+def mask_rows(pr: Problem, bh: int, i0: int, i1: int) -> np.ndarray:
+    """Keep mask (uint8, rows [i0,i1) x s keys) of one query head; hidden keys are 0."""
+    M = np.zeros((i1 - i0, pr.s), dtype=np.uint8)
+    _load().oracle_mask_rows(ctypes.byref(pr._c()), bh, i0, i1, M.ctypes.data_as(_U8))
+    return M
+
+
+def bwd(pr: Problem, q, k, v, dout):
+    """Full backward: (dQ [b,h_q,s,d], dK [b,h_kv,s,d], dV [b,h_kv,s,d]), fp64."""
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    dq = np.zeros((pr.b, pr.h_q, pr.s, pr.d))
+    dk = np.zeros((pr.b, pr.h_kv, pr.s, pr.d))
+    dv = np.zeros((pr.b, pr.h_kv, pr.s, pr.d))
+    lib.oracle_bwd(ctypes.byref(pr._c()), _dp(q), _dp(k), _dp(v), _dp(dout), _dp(dq), _dp(dk),
+                   _dp(dv))
+    return dq, dk, dv
+
+
+def dq_rows(pr: Problem, q, k, v, dout, bh, rows) -> np.ndarray:
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    bh = np.ascontiguousarray(np.asarray(bh, dtype=np.int64))
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((len(rows), pr.d))
+    lib.oracle_dq_rows(ctypes.byref(pr._c()), _dp(q), _dp(k), _dp(v), _dp(dout), len(rows),
+                       _ip(bh), _ip(rows), _dp(out))
+    return out
+
+
+def dkdv_rows(pr: Problem, q, k, v, dout, bkv, rows):
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    bkv = np.ascontiguousarray(np.asarray(bkv, dtype=np.int64))
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dk = np.zeros((len(rows), pr.d))
+    dv = np.zeros((len(rows), pr.d))
+    lib.oracle_dkdv_rows(ctypes.byref(pr._c()), _dp(q), _dp(k), _dp(v), _dp(dout), len(rows),
+                         _ip(bkv), _ip(rows), _dp(dk), _dp(dv))
+    return dk, dv
+
+
+def stored_bytes(pr: Problem) -> dict:
+    out = _Bytes()
+    _load().oracle_stored_bytes(ctypes.byref(pr._c()), ctypes.byref(out))
+    return {n: int(getattr(out, n)) for n, _ in _Bytes._fields_}
