@@ -1,0 +1,227 @@
+"""GB300 (sm_103a) attention core under selective activation recomputation.
+
+Thin Python binding of the C ABI in ``include/attn_core.h``: the functions
+below marshal torch tensors into device pointers and the current CUDA stream
+and call the library; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if ``libattn_core.so`` is missing or
+cannot be loaded, the first call raises.
+
+The attention core (QK^T, softmax, softmax dropout, attention over V) is the
+part of a transformer layer that selective activation recomputation drops
+after the forward pass and recomputes in the backward pass ("Reducing
+Activation Recomputation in Large Transformer Models", Key takeaways, fourth
+bullet).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+__all__ = [
+    "AttnCoreError", "Params", "load_library", "attn_core_fwd", "attn_core_bwd_recompute",
+    "attn_core_bwd_workspace_bytes", "attn_core_stored_bytes", "attn_core_strerror",
+    "fwd", "bwd_recompute", "stored_bytes", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED",
+    "ERR_MISALIGNED", "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
+    "FLAG_TEST_WAIT_TIMEOUT", "SUPPORTED_HEAD_DIMS",
+]
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_MISALIGNED = 3
+ERR_WORKSPACE_TOO_SMALL = 4
+ERR_CUDA = 5
+ERR_DEVICE_TIMEOUT = 6
+FLAG_TEST_WAIT_TIMEOUT = 0x100
+SUPPORTED_HEAD_DIMS = (64, 96, 128, 160)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libattn_core.so")
+
+
+class AttnCoreError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {attn_core_strerror(code)} (code {code})")
+
+
+class _CParams(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
+                ("s", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("p_drop", ctypes.c_float), ("scale", ctypes.c_float),
+                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+                ("dev_status", ctypes.c_void_p), ("flags", ctypes.c_int32),
+                ("wait_timeout_ms", ctypes.c_uint32), ("timing_events", ctypes.c_void_p)]
+
+
+class _CBytes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in
+                ("layer_none", "layer_selective", "layer_full", "core_scores_avoided",
+                 "core_kept", "core_recompute_state")]
+
+
+@dataclass
+class Params:
+    """Mirror of ``attn_core_params`` (see include/attn_core.h)."""
+    b: int
+    h_q: int
+    h_kv: int
+    s: int
+    d: int
+    causal: bool = True
+    p_drop: float = 0.0
+    scale: float = 0.0
+    seed: int = 0
+    offset: int = 0
+    dev_status: int = 0          # device address of an int32, or 0
+    flags: int = 0
+    wait_timeout_ms: int = 0
+    timing_events: int = 0       # address of a void*[2 * n_kernels] array, or 0
+
+    def to_c(self) -> _CParams:
+        return _CParams(self.b, self.h_q, self.h_kv, self.s, self.d, int(self.causal),
+                        float(self.p_drop), float(self.scale), int(self.seed) & (2**64 - 1),
+                        int(self.offset) & (2**64 - 1), self.dev_status or None, int(self.flags),
+                        int(self.wait_timeout_ms), self.timing_events or None)
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libattn_core.so (raises if it is absent: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"attention-core library not built ({path} missing); run "
+            "`python -m attention_core_gb300.build` or __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    P = ctypes.POINTER(_CParams)
+    lib.attn_core_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp]
+    lib.attn_core_fwd.restype = ctypes.c_int
+    lib.attn_core_bwd_workspace_bytes.argtypes = [P]
+    lib.attn_core_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_core_bwd_recompute.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.attn_core_bwd_recompute.restype = ctypes.c_int
+    lib.attn_core_stored_bytes.argtypes = [P, ctypes.POINTER(_CBytes)]
+    lib.attn_core_stored_bytes.restype = ctypes.c_int
+    lib.attn_core_strerror.argtypes = [ctypes.c_int]
+    lib.attn_core_strerror.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------ raw C ABI ---
+# Same names and arguments as the C functions; pointers are plain integers.
+
+def attn_core_strerror(code: int) -> str:
+    return load_library().attn_core_strerror(int(code)).decode()
+
+
+def attn_core_fwd(p: Params, q: int, k: int, v: int, o: int, lse: int, stream: int) -> int:
+    cp = p.to_c()
+    return load_library().attn_core_fwd(ctypes.byref(cp), q, k, v, o, lse, stream or None)
+
+
+def attn_core_bwd_workspace_bytes(p: Params) -> int:
+    cp = p.to_c()
+    return int(load_library().attn_core_bwd_workspace_bytes(ctypes.byref(cp)))
+
+
+def attn_core_bwd_recompute(p: Params, q: int, k: int, v: int, o: int, lse: int, dout: int,
+                            dq: int, dk: int, dv: int, workspace: int, workspace_bytes: int,
+                            stream: int) -> int:
+    cp = p.to_c()
+    return load_library().attn_core_bwd_recompute(ctypes.byref(cp), q, k, v, o, lse, dout, dq, dk,
+                                                  dv, workspace, workspace_bytes, stream or None)
+
+
+def attn_core_stored_bytes(p: Params) -> tuple[int, dict]:
+    cp = p.to_c()
+    out = _CBytes()
+    rc = load_library().attn_core_stored_bytes(ctypes.byref(cp), ctypes.byref(out))
+    return rc, {n: int(getattr(out, n)) for n, _ in _CBytes._fields_}
+
+
+# --------------------------------------------------- torch conveniences ---
+
+def _check(t, name, dtype, shape):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream() -> int:
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _params_from(q, k, causal, p_drop, seed, offset, scale, **kw) -> Params:
+    b, h_q, s, d = q.shape
+    return Params(b=b, h_q=h_q, h_kv=k.shape[1], s=s, d=d, causal=causal, p_drop=p_drop,
+                  scale=scale, seed=seed, offset=offset, **kw)
+
+
+def fwd(q, k, v, *, causal: bool = True, p_drop: float = 0.0, seed: int = 0, offset: int = 0,
+        scale: float = 0.0, out=None, lse=None, **kw):
+    """Forward of the attention core.  Returns (O bf16 [b,h_q,s,d], LSE fp32 [b,h_q,s])."""
+    import torch
+    p = _params_from(q, k, causal, p_drop, seed, offset, scale, **kw)
+    _check(q, "q", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
+    _check(k, "k", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
+    _check(v, "v", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((p.b, p.h_q, p.s), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
+    _check(lse, "lse", torch.float32, (p.b, p.h_q, p.s))
+    rc = attn_core_fwd(p, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_fwd")
+    return out, lse
+
+
+def bwd_recompute(q, k, v, o, lse, dout, *, causal: bool = True, p_drop: float = 0.0, seed: int = 0,
+                  offset: int = 0, scale: float = 0.0, dq=None, dk=None, dv=None, workspace=None,
+                  **kw):
+    """Recompute-backward.  Returns (dQ, dK, dV), bf16, shaped like Q, K, V."""
+    import torch
+    p = _params_from(q, k, causal, p_drop, seed, offset, scale, **kw)
+    _check(q, "q", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
+    _check(k, "k", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
+    _check(v, "v", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
+    _check(o, "o", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
+    _check(dout, "dout", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
+    _check(lse, "lse", torch.float32, (p.b, p.h_q, p.s))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = attn_core_bwd_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    rc = attn_core_bwd_recompute(p, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_bwd_recompute")
+    return dq, dk, dv
+
+
+def stored_bytes(b: int, h_q: int, h_kv: int, s: int, d: int) -> dict:
+    """Activation-byte accounting of one layer shard (see attn_core_bytes)."""
+    rc, out = attn_core_stored_bytes(Params(b=b, h_q=h_q, h_kv=h_kv, s=s, d=d))
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_stored_bytes")
+    return out

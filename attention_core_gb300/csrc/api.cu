@@ -1,0 +1,236 @@
+// api.cu -- the C ABI declared in include/attn_core.h: argument checks,
+// TMA tensor-map encoding and kernel launches.  No device memory is
+// allocated here; the caller owns every buffer.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include "../../include/attn_core.h"
+#include "kernels.h"
+#include "tile.cuh"
+
+namespace {
+
+using ac::kBlockRows;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder()
+{
+    if (g_encode) return ATTN_CORE_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return ATTN_CORE_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return ATTN_CORE_OK;
+}
+
+// 0: not checked yet, 1: sm_103, -1: other.
+int g_dev_ok[128];
+
+int check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_CORE_ERR_CUDA;
+    if (dev < 0 || dev >= 128) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (g_dev_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return ATTN_CORE_ERR_CUDA;
+        g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_dev_ok[dev] == 1 ? ATTN_CORE_OK : ATTN_CORE_ERR_UNSUPPORTED;
+}
+
+bool supported_d(int d) { return d == 64 || d == 96 || d == 128 || d == 160; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_params(const attn_core_params* p)
+{
+    if (p == nullptr) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->b <= 0 || p->h_q <= 0 || p->h_kv <= 0 || p->s <= 0 || p->d <= 0) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->h_q % p->h_kv != 0) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->causal != 0 && p->causal != 1) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!(p->p_drop >= 0.0f && p->p_drop < 1.0f)) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->offset >> 32) return ATTN_CORE_ERR_INVALID_ARG;
+    if (isnan(p->scale) || isinf(p->scale)) return ATTN_CORE_ERR_INVALID_ARG;
+    // Counter words and grid sizes are 32-bit.
+    const int64_t n_bh = (int64_t)p->b * p->h_q;
+    const int64_t n_blk = ((int64_t)p->s + kBlockRows - 1) / kBlockRows;
+    if (n_bh * n_blk >= (int64_t)INT32_MAX || (int64_t)p->s * n_bh >= ((int64_t)1 << 40)) return ATTN_CORE_ERR_INVALID_ARG;
+    return ATTN_CORE_OK;
+}
+
+uint32_t drop_threshold(float p)
+{
+    if (!(p > 0.0f)) return 0u;
+    long long t = llround((double)p * 65536.0);
+    if (t > 65535) t = 65535;
+    if (t < 0) t = 0;
+    return (uint32_t)t;
+}
+
+ac::CommonArgs common_args(const attn_core_params* p)
+{
+    ac::CommonArgs c{};
+    c.s = p->s;
+    c.h_q = p->h_q;
+    c.h_kv = p->h_kv;
+    c.n_blk = (p->s + kBlockRows - 1) / kBlockRows;
+    c.n_bh = p->b * p->h_q;
+    c.causal = p->causal;
+    const float scale = (p->scale > 0.0f) ? p->scale : 1.0f / sqrtf((float)p->d);
+    c.scale = scale;
+    c.scale_log2 = scale * 1.44269504088896340736f;
+    c.thr = drop_threshold(p->p_drop);
+    c.keep_scale = 1.0f / (1.0f - (float)c.thr / 65536.0f);
+    c.seed_lo = (uint32_t)(p->seed & 0xffffffffu);
+    c.seed_hi = (uint32_t)(p->seed >> 32);
+    c.offset = (uint32_t)p->offset;
+    c.status = p->dev_status;
+    c.timeout_ns = (uint64_t)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
+    c.inject_timeout = (p->flags & ATTN_CORE_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
+    return c;
+}
+
+// 3-D map over a [heads, s, d] bf16 tensor: box = one column chunk of
+// `rows` rows of one head, swizzled to match the shared-memory tile layout.
+int encode_map(CUtensorMap* m, const void* ptr, int d, int s, int64_t heads, int rows)
+{
+    const int cw = (d % 64 == 0) ? 64 : 32;
+    const CUtensorMapSwizzle sw = (cw == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)s, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)s * (cuuint64_t)d * 2};
+    cuuint32_t box[3] = {(cuuint32_t)cw, (cuuint32_t)rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_CORE_OK : ATTN_CORE_ERR_CUDA;
+}
+
+size_t padded_rows(const attn_core_params* p)
+{
+    const size_t n_blk = ((size_t)p->s + kBlockRows - 1) / kBlockRows;
+    return (size_t)p->b * p->h_q * n_blk * kBlockRows;
+}
+
+int record(void** ev, int idx, cudaStream_t st)
+{
+    if (!ev) return ATTN_CORE_OK;
+    return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[idx]), st) == cudaSuccess ? ATTN_CORE_OK
+                                                                                       : ATTN_CORE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_core_strerror(int code)
+{
+    switch (code & 0xff) {
+        case ATTN_CORE_OK: return "ok";
+        case ATTN_CORE_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_CORE_ERR_UNSUPPORTED: return "unsupported head dimension or device";
+        case ATTN_CORE_ERR_MISALIGNED: return "pointer not aligned (16 bytes; workspace 256 bytes)";
+        case ATTN_CORE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case ATTN_CORE_ERR_CUDA: return "CUDA error";
+        case ATTN_CORE_ERR_DEVICE_TIMEOUT: return "a kernel wait ran past its time limit";
+        default: return "unknown error";
+    }
+}
+
+int attn_core_stored_bytes(const attn_core_params* p, attn_core_bytes* out)
+{
+    int rc = check_params(p);
+    if (rc) return rc;
+    if (!out) return ATTN_CORE_ERR_INVALID_ARG;
+    const int64_t s = p->s, b = p->b, a = p->h_q, akv = p->h_kv, d = p->d;
+    const int64_t h = a * d;
+    out->layer_selective = 34 * s * b * h;
+    out->core_scores_avoided = 5 * a * s * s * b;
+    out->layer_none = out->layer_selective + out->core_scores_avoided;
+    out->layer_full = 2 * s * b * h;
+    out->core_kept = 2 * s * d * b * (2 * a + 2 * akv);
+    out->core_recompute_state = 4 * b * a * s + 16;
+    return ATTN_CORE_OK;
+}
+
+size_t attn_core_bwd_workspace_bytes(const attn_core_params* p)
+{
+    if (check_params(p)) return 0;
+    return 2 * sizeof(float) * padded_rows(p);
+}
+
+int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                  void* stream)
+{
+    int rc = check_params(p);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!supported_d(p->d)) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_CORE_ERR_MISALIGNED;
+    if ((rc = check_device())) return rc;
+    if ((rc = get_encoder())) return rc;
+    const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
+    CUtensorMap tq, tk, tv, to;
+    if ((rc = encode_map(&tq, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tk, k, p->d, p->s, nkv, 128)) ||
+        (rc = encode_map(&tv, v, p->d, p->s, nkv, 128)) || (rc = encode_map(&to, o, p->d, p->s, nq, 128)))
+        return rc;
+    ac::FwdArgs a{};
+    a.c = common_args(p);
+    a.lse = lse;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((rc = record(p->timing_events, 0, st))) return rc;
+    if (ac::launch_fwd(p->d, a.c.thr != 0, tq, tk, tv, to, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    return record(p->timing_events, 1, st);
+}
+
+int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, void* stream)
+{
+    int rc = check_params(p);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!supported_d(p->d)) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return ATTN_CORE_ERR_MISALIGNED;
+    if (workspace_bytes < attn_core_bwd_workspace_bytes(p)) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    if ((rc = check_device())) return rc;
+    if ((rc = get_encoder())) return rc;
+    const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
+    const int bq = ac::dkdv_query_tile(p->d);
+    CUtensorMap tq128, tdo128, tqb, tdob, tk, tv, tdq, tdk, tdv;
+    if ((rc = encode_map(&tq128, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tdo128, dout, p->d, p->s, nq, 128)) ||
+        (rc = encode_map(&tqb, q, p->d, p->s, nq, bq)) || (rc = encode_map(&tdob, dout, p->d, p->s, nq, bq)) ||
+        (rc = encode_map(&tk, k, p->d, p->s, nkv, 128)) || (rc = encode_map(&tv, v, p->d, p->s, nkv, 128)) ||
+        (rc = encode_map(&tdq, dq, p->d, p->s, nq, 128)) || (rc = encode_map(&tdk, dk, p->d, p->s, nkv, 128)) ||
+        (rc = encode_map(&tdv, dv, p->d, p->s, nkv, 128)))
+        return rc;
+    ac::BwdArgs a{};
+    a.c = common_args(p);
+    a.s_pad = a.c.n_blk * kBlockRows;
+    a.o = static_cast<const uint16_t*>(o);
+    a.dout = static_cast<const uint16_t*>(dout);
+    a.lse = lse;
+    a.lse2_ws = static_cast<float*>(workspace);
+    a.delta_ws = static_cast<float*>(workspace) + padded_rows(p);
+    a.d = p->d;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool drop = a.c.thr != 0;
+    if ((rc = record(p->timing_events, 0, st))) return rc;
+    if (ac::launch_bwd_pre(a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
+    if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    if ((rc = record(p->timing_events, 3, st)) || (rc = record(p->timing_events, 4, st))) return rc;
+    if (ac::launch_bwd_dq(p->d, drop, tq128, tk, tv, tdo128, tdq, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    return record(p->timing_events, 5, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,740 @@
+// bwd.cu -- recompute-backward of the attention core on sm_103a.
+//
+// Selective activation recomputation keeps only Q, K, V, O, the per-row LSE
+// and the dropout seed/offset; the backward pass recomputes the scores,
+// probabilities and dropout mask on chip ("Reducing Activation Recomputation
+// in Large Transformer Models", Key takeaways, fourth bullet; "Recomputing
+// Activations": the scores are "recomputed during the backward pass").
+// With Z = M / (1 - p) the gradients are
+//     dP_d = dO V^T,  dP = dP_d * Z,  dS = P * (dP - D),  D_i = rowsum(dO_i * O_i)
+//     dV = (P * Z)^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K
+// (D_i equals sum_j P_ij dP_ij because O_i = sum_j P_ij Z_ij V_j).
+//
+// Three kernels:
+//   bwd_pre   D_i and LSE_i * log2(e) per query row into a padded workspace
+//   bwd_dkdv  one (KV head, 128-key block) per CTA; keys on TMEM lanes; loops
+//             over the query heads of the GQA group and their query tiles;
+//             recomputes S^T and dP^T, accumulates dV and dK in TMEM
+//   bwd_dq    one (query head, 128-query block) per CTA; queries on TMEM
+//             lanes; recomputes S and dP per key block, accumulates dQ in TMEM
+// Neither gradient kernel writes a partial sum to global memory: each output
+// tile is finished in TMEM and stored once.
+#include "kernels.h"
+#include "philox.cuh"
+#include "ptx.cuh"
+#include "tile.cuh"
+
+namespace ac {
+
+namespace {
+
+enum : int32_t {
+    kSiteInject = 1, kSiteKvFull, kSiteQEmpty, kSiteQFull, kSitePFull, kSiteDsFull, kSiteSFull,
+    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSiteSRead
+};
+__device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
+
+}  // namespace
+
+// ======================================================= preprocess ======
+// One warp per padded query row: D_i = sum_c dO_ic O_ic in fp32 and
+// LSE_i * log2(e); rows past s get D = 0 and +inf (their probabilities
+// recompute to exactly 0).
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdArgs a)
+{
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int64_t n_rows = (int64_t)a.c.n_bh * a.s_pad;
+    if (row >= n_rows) return;
+    const int64_t bh = row / a.s_pad;
+    const int64_t i = row % a.s_pad;
+    if (i >= a.c.s) {
+        if (lane == 0) {
+            a.delta_ws[row] = 0.f;
+            a.lse2_ws[row] = INFINITY;
+        }
+        return;
+    }
+    const int64_t base = (bh * a.c.s + i) * a.d;
+    float acc = 0.f;
+    for (int c8 = lane; c8 < a.d / 8; c8 += 32) {
+        const uint4 o4 = *reinterpret_cast<const uint4*>(a.o + base + c8 * 8);
+        const uint4 g4 = *reinterpret_cast<const uint4*>(a.dout + base + c8 * 8);
+        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
+            acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(gw[e] & 0xFFFF0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+        a.delta_ws[row] = acc;
+        a.lse2_ws[row] = a.lse[bh * a.c.s + i] * 1.44269504088896340736f;
+    }
+}
+
+// ============================================================ dK / dV ====
+namespace {
+
+template <int D>
+struct DkdvCfg {
+    using G = TileGeom<D>;
+    static constexpr int BQ = dkdv_query_tile(D);
+    static constexpr uint32_t KV_TILE = G::template tile_bytes<128>();
+    static constexpr uint32_t KV_CHUNK = G::template chunk_bytes<128>();
+    static constexpr uint32_t Q_TILE = G::template tile_bytes<BQ>();
+    static constexpr uint32_t Q_CHUNK = G::template chunk_bytes<BQ>();
+    static constexpr int ST = 2;
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = KV_TILE;
+    static constexpr uint32_t OFF_Q = 2 * KV_TILE;
+    static constexpr uint32_t OFF_DO = OFF_Q + ST * Q_TILE;
+    static constexpr uint32_t OFF_LSE = OFF_DO + ST * Q_TILE;
+    static constexpr uint32_t OFF_DEL = OFF_LSE + ST * BQ * 4;
+    static constexpr uint32_t OFF_BAR = OFF_DEL + ST * BQ * 4;
+    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    // TMEM columns
+    static constexpr uint32_t T_DV = 0, T_DK = D, T_S = 2 * D, T_DP = 2 * D + BQ;
+    static_assert(T_DP + BQ <= 512, "TMEM budget");
+};
+
+struct DkdvBars {
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full, dp_full, p_full, ds_full, acc_done;
+    uint64_t never;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+}  // namespace
+
+template <int D, bool DROP>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                     const BwdArgs args)
+{
+    using G = TileGeom<D>;
+    using C = DkdvCfg<D>;
+    constexpr int BQ = C::BQ;
+    constexpr int ST = C::ST;
+    const CommonArgs& a = args.c;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sb = raw + pad;
+    uint8_t* smem = smem_raw + pad;
+    DkdvBars* bars = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
+    auto bar = [](uint64_t& b) { return smem_u32(&b); };
+
+    const int n_bkv = a.n_bh / a.h_q * a.h_kv;
+    const int kb = (int)(blockIdx.x / n_bkv);          // small key blocks carry the most work
+    const int bkv = (int)(blockIdx.x % n_bkv);
+    const int group = a.h_q / a.h_kv;
+    const int bh0 = (bkv / a.h_kv) * a.h_q + (bkv % a.h_kv) * group;
+    const int n_qt = args.s_pad / BQ;
+    const int qt0 = a.causal ? (kb * 128) / BQ : 0;
+    const int per_head = n_qt - qt0;
+    const int n_it = group * per_head;
+    const uint32_t warp = warp_id(), lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(bars->kv_full), 1);
+        for (int st = 0; st < ST; ++st) {
+            mbar_init(bar(bars->q_full[st]), 1);
+            mbar_init(bar(bars->q_empty[st]), 1);
+        }
+        mbar_init(bar(bars->s_full), 1);
+        mbar_init(bar(bars->dp_full), 1);
+        mbar_init(bar(bars->p_full), 128);
+        mbar_init(bar(bars->ds_full), 128);
+        mbar_init(bar(bars->acc_done), 1);
+        mbar_init(bar(bars->never), 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
+
+    bool alive = true;
+    if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
+
+    if (alive && warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer: K and V once, then (Q, dO, LSE2, D) per query tile
+            mbar_arrive_expect_tx(bar(bars->kv_full), 2 * C::KV_TILE);
+            for (int ch = 0; ch < G::NCH; ++ch) {
+                tma_load_3d(sb + C::OFF_K + ch * C::KV_CHUNK, &tm_k, ch * G::CW, kb * 128, bkv, bar(bars->kv_full));
+                tma_load_3d(sb + C::OFF_V + ch * C::KV_CHUNK, &tm_v, ch * G::CW, kb * 128, bkv, bar(bars->kv_full));
+            }
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % ST;
+                const int bh = bh0 + it / per_head;
+                const int qt = qt0 + it % per_head;
+                if (!wait_bounded(wc, bar(bars->q_empty[st]), ((it / ST) & 1) ^ 1, timeout_code(kSiteQEmpty)))
+                    break;
+                const uint32_t fb = bar(bars->q_full[st]);
+                mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 2 * BQ * 4);
+                for (int ch = 0; ch < G::NCH; ++ch) {
+                    tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, qt * BQ, bh, fb);
+                    tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, qt * BQ, bh,
+                                fb);
+                }
+                const size_t srow = (size_t)bh * args.s_pad + (size_t)qt * BQ;
+                bulk_load_1d(sb + C::OFF_LSE + st * BQ * 4, args.lse2_ws + srow, BQ * 4, fb);
+                bulk_load_1d(sb + C::OFF_DEL + st * BQ * 4, args.delta_ws + srow, BQ * 4, fb);
+            }
+        }
+    } else if (alive && warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer.  Order: S0 dP0 | dV0 S1 dK0 dP1 | dV1 S2 dK1 dP2 | ...
+            constexpr uint32_t IDS = idesc_bf16(128, BQ, false, false);  // S^T = K Q^T, dP^T = V dO^T
+            constexpr uint32_t IDG = idesc_bf16(128, D, false, true);    // dV += P^T dO, dK += dS^T Q
+            auto issue_s = [&](int it) {
+                const uint32_t qbase = sb + C::OFF_Q + (it % ST) * C::Q_TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::T_S, G::template desc_k<128>(sb + C::OFF_K, kk),
+                           G::template desc_k<BQ>(qbase, kk), IDS, kk > 0 ? 1u : 0u);
+                mma_commit(bar(bars->s_full));
+            };
+            auto issue_dp = [&](int it) {
+                const uint32_t dobase = sb + C::OFF_DO + (it % ST) * C::Q_TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::T_DP, G::template desc_k<128>(sb + C::OFF_V, kk),
+                           G::template desc_k<BQ>(dobase, kk), IDS, kk > 0 ? 1u : 0u);
+                mma_commit(bar(bars->dp_full));
+            };
+            bool ok = wait_bounded(wc, bar(bars->kv_full), 0, timeout_code(kSiteKvFull));
+            if (ok) ok = wait_bounded(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull));
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_dp(0);
+            }
+            for (int it = 0; it < n_it && ok; ++it) {
+                const int st = it % ST;
+                const uint32_t qbase = sb + C::OFF_Q + st * C::Q_TILE;
+                const uint32_t dobase = sb + C::OFF_DO + st * C::Q_TILE;
+                ok = wait_bounded(wc, bar(bars->p_full), it & 1, timeout_code(kSitePFull));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, G::template desc_mn<BQ>(dobase, kk), IDG,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                if (it + 1 < n_it) {
+                    const int st1 = (it + 1) % ST;
+                    ok = wait_bounded(wc, bar(bars->q_full[st1]), ((it + 1) / ST) & 1, timeout_code(kSiteQFull));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
+                ok = wait_bounded(wc, bar(bars->ds_full), it & 1, timeout_code(kSiteDsFull));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + C::T_DK, tmem + C::T_DP + kk * 8, G::template desc_mn<BQ>(qbase, kk), IDG,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(bars->q_empty[st]));
+                if (it + 1 < n_it) issue_dp(it + 1);
+            }
+            if (ok) mma_commit(bar(bars->acc_done));
+        }
+    } else if (alive && warp >= 4) {
+        // ---- row threads: one key per thread (= TMEM lane)
+        const int r = (int)threadIdx.x - 128;
+        const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+        const int key = kb * 128 + r;
+        const uint32_t warp_key0 = (uint32_t)(kb * 128 + (int)(warp & 3u) * 32);
+        const float* lse2_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
+        const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DEL);
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int st = it % ST;
+            const int bh = bh0 + it / per_head;
+            const int q0 = (qt0 + it % per_head) * BQ;
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded(wc, bar(bars->q_full[st]), (it / ST) & 1, timeout_code(kSiteQFull)));
+            if (ok)
+                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), it & 1, timeout_code(kSiteSFull)));
+            if (!ok) break;
+            tc_fence_after();
+            const float* l2 = lse2_s + st * BQ;
+            const float* dl = del_s + st * BQ;
+            float p[BQ];
+#pragma unroll
+            for (int c32 = 0; c32 < BQ / 32; ++c32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + C::T_S + lane_off + c32 * 32, rr);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    p[c32 * 32 + e] = ex2_approx(fmaf(__uint_as_float(rr[e]), a.scale_log2, -l2[c32 * 32 + e]));
+            }
+            if (a.causal && q0 < kb * 128 + 128) {
+#pragma unroll
+                for (int c = 0; c < BQ; ++c)
+                    if (q0 + c < key) p[c] = 0.f;
+            }
+            uint32_t kw[BQ / 32];
+            if (DROP) {
+                const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+#pragma unroll
+                for (int v = 0; v < BQ / 32; ++v) kw[v] = keep_word_col(pk, warp_key0, (uint32_t)(q0 + 32 * v));
+            } else {
+#pragma unroll
+                for (int v = 0; v < BQ / 32; ++v) kw[v] = 0xffffffffu;
+            }
+            // P_d^T (without the 1/(1-p) factor, applied to dV at the end) -> TMEM over S^T
+#pragma unroll
+            for (int h = 0; h < BQ / 64; ++h) {
+                uint32_t pw[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int c = h * 64 + 2 * e;
+                    const float p0 = ((kw[c >> 5] >> (c & 31)) & 1u) ? p[c] : 0.f;
+                    const float p1 = ((kw[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? p[c + 1] : 0.f;
+                    pw[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tmem + C::T_S + lane_off + h * 32, pw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(bars->p_full));
+
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), it & 1, timeout_code(kSiteDpFull)));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c32 = 0; c32 < BQ / 32; ++c32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + C::T_DP + lane_off + c32 * 32, rr);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float ds[2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int c = c32 * 32 + 2 * e + t;
+                        const float dpd = __uint_as_float(rr[2 * e + t]);
+                        const float dpv = ((kw[c32] >> (2 * e + t)) & 1u) ? dpd * a.keep_scale : 0.f;
+                        ds[t] = p[c] * (dpv - dl[c]);
+                    }
+                    w[e] = pack_bf16x2(ds[0], ds[1]);
+                }
+                tmem_st16(tmem + C::T_DP + lane_off + c32 * 16, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(bars->ds_full));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c32 = 0; c32 < D / 32; ++c32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
+                stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, a.keep_scale);
+                tmem_ld32(tmem + C::T_DK + lane_off + c32 * 32, rr);
+                stage_row32<D, 128>(sb + C::OFF_K, r, c32 * 32, rr, a.scale);
+            }
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (r == 0 && !bars->abort_flag) {
+            for (int ch = 0; ch < G::NCH; ++ch) {
+                tma_store_3d(&tm_dv, sb + C::OFF_V + ch * C::KV_CHUNK, ch * G::CW, kb * 128, bkv);
+                tma_store_3d(&tm_dk, sb + C::OFF_K + ch * C::KV_CHUNK, ch * G::CW, kb * 128, bkv);
+            }
+            bulk_commit();
+            bulk_wait_read0();
+        }
+    }
+
+    __syncthreads();
+    if (bars->abort_flag) {
+        for (int k = 0; k < 20; ++k) __nanosleep(50000);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// =============================================================== dQ ======
+namespace {
+
+template <int D>
+struct DqCfg {
+    using G = TileGeom<D>;
+    static constexpr uint32_t TILE = G::template tile_bytes<128>();
+    static constexpr uint32_t CHUNK = G::template chunk_bytes<128>();
+    static constexpr int KST = 2;                    // K is read by S and by dQ: two stages
+    static constexpr int VST = (D <= 128) ? 2 : 1;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_DO = TILE;
+    static constexpr uint32_t OFF_K = 2 * TILE;
+    static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
+    static constexpr uint32_t OFF_BAR = OFF_V + VST * TILE;
+    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+    static_assert(T_DQ + D <= 512, "TMEM budget");
+};
+
+struct DqBars {
+    uint64_t qdo_full;
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full, s_read, dp_full, ds_full, acc_done;
+    uint64_t never;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+}  // namespace
+
+template <int D, bool DROP>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args)
+{
+    using G = TileGeom<D>;
+    using C = DqCfg<D>;
+    constexpr int KST = C::KST, VST = C::VST;
+    const CommonArgs& a = args.c;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sb = raw + pad;
+    DqBars* bars = reinterpret_cast<DqBars*>(smem_raw + pad + C::OFF_BAR);
+    auto bar = [](uint64_t& b) { return smem_u32(&b); };
+
+    const int n_bh = a.n_bh;
+    const int qb = a.n_blk - 1 - (int)(blockIdx.x / n_bh);
+    const int bh = (int)(blockIdx.x % n_bh);
+    const int group = a.h_q / a.h_kv;
+    const int bkv = (bh / a.h_q) * a.h_kv + (bh % a.h_q) / group;
+    const int nk = a.causal ? (qb + 1) : a.n_blk;
+    const uint32_t warp = warp_id(), lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(bars->qdo_full), 1);
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(bar(bars->k_full[st]), 1);
+            mbar_init(bar(bars->k_empty[st]), 1);
+            mbar_init(bar(bars->v_full[st]), 1);
+            mbar_init(bar(bars->v_empty[st]), 1);
+        }
+        mbar_init(bar(bars->s_full), 1);
+        mbar_init(bar(bars->s_read), 128);
+        mbar_init(bar(bars->dp_full), 1);
+        mbar_init(bar(bars->ds_full), 128);
+        mbar_init(bar(bars->acc_done), 1);
+        mbar_init(bar(bars->never), 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
+
+    bool alive = true;
+    if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
+
+    if (alive && warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer: Q and dO once, then the K ring
+            mbar_arrive_expect_tx(bar(bars->qdo_full), 2 * C::TILE);
+            for (int ch = 0; ch < G::NCH; ++ch) {
+                tma_load_3d(sb + C::OFF_Q + ch * C::CHUNK, &tm_q, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
+                tma_load_3d(sb + C::OFF_DO + ch * C::CHUNK, &tm_do, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
+            }
+            for (int j = 0; j < nk; ++j) {
+                const int st = j % KST;
+                if (!wait_bounded(wc, bar(bars->k_empty[st]), ((j / KST) & 1) ^ 1, timeout_code(kSiteKEmpty)))
+                    break;
+                mbar_arrive_expect_tx(bar(bars->k_full[st]), C::TILE);
+                for (int ch = 0; ch < G::NCH; ++ch)
+                    tma_load_3d(sb + C::OFF_K + st * C::TILE + ch * C::CHUNK, &tm_k, ch * G::CW, j * 128, bkv,
+                                bar(bars->k_full[st]));
+            }
+        }
+    } else if (alive && warp == 2) {
+        if (lane == 0) {
+            // ---- TMA producer: the V ring
+            for (int j = 0; j < nk; ++j) {
+                const int st = j % VST;
+                if (!wait_bounded(wc, bar(bars->v_empty[st]), ((j / VST) & 1) ^ 1, timeout_code(kSiteVEmpty)))
+                    break;
+                mbar_arrive_expect_tx(bar(bars->v_full[st]), C::TILE);
+                for (int ch = 0; ch < G::NCH; ++ch)
+                    tma_load_3d(sb + C::OFF_V + st * C::TILE + ch * C::CHUNK, &tm_v, ch * G::CW, j * 128, bkv,
+                                bar(bars->v_full[st]));
+            }
+        }
+    } else if (alive && warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer.  Order: S0 dP0 | S1 dQ0 dP1 | S2 dQ1 dP2 | ...
+            constexpr uint32_t IDS = idesc_bf16(128, 128, false, false);  // S = Q K^T, dP = dO V^T
+            constexpr uint32_t IDQ = idesc_bf16(128, D, false, true);     // dQ += dS K
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % KST;
+                if (!wait_bounded(wc, bar(bars->k_full[st]), (j / KST) & 1, timeout_code(kSiteKFull))) return false;
+                tc_fence_after();
+                const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::T_S, G::template desc_k<128>(sb + C::OFF_Q, kk), G::template desc_k<128>(kbase, kk),
+                           IDS, kk > 0 ? 1u : 0u);
+                mma_commit(bar(bars->s_full));
+                return true;
+            };
+            auto issue_dp = [&](int j) -> bool {
+                const int st = j % VST;
+                if (!wait_bounded(wc, bar(bars->v_full[st]), (j / VST) & 1, timeout_code(kSiteVFull))) return false;
+                tc_fence_after();
+                const uint32_t vbase = sb + C::OFF_V + st * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::T_DP, G::template desc_k<128>(sb + C::OFF_DO, kk),
+                           G::template desc_k<128>(vbase, kk), IDS, kk > 0 ? 1u : 0u);
+                mma_commit(bar(bars->v_empty[st]));
+                mma_commit(bar(bars->dp_full));
+                return true;
+            };
+            bool ok = wait_bounded(wc, bar(bars->qdo_full), 0, timeout_code(kSiteQFull));
+            if (ok) ok = issue_s(0);
+            if (ok) ok = issue_dp(0);
+            for (int j = 0; j < nk && ok; ++j) {
+                if (j + 1 < nk) {
+                    ok = wait_bounded(wc, bar(bars->s_read), j & 1, timeout_code(kSiteSRead));
+                    if (ok) ok = issue_s(j + 1);
+                    if (!ok) break;
+                }
+                ok = wait_bounded(wc, bar(bars->ds_full), j & 1, timeout_code(kSiteDsFull));
+                if (!ok) break;
+                tc_fence_after();
+                const int st = j % KST;
+                const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + C::T_DQ, tmem + C::T_DP + kk * 8, G::template desc_mn<128>(kbase, kk), IDQ,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(bars->k_empty[st]));
+                if (j + 1 < nk) ok = issue_dp(j + 1);
+            }
+            if (ok) mma_commit(bar(bars->acc_done));
+        }
+    } else if (alive && warp >= 4) {
+        // ---- row threads: one query row per thread (= TMEM lane)
+        const int r = (int)threadIdx.x - 128;
+        const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+        const int i = qb * 128 + r;
+        const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
+        const float lse2 = args.lse2_ws[srow];
+        const float delta = args.delta_ws[srow];
+        const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+        bool ok = true;
+        for (int j = 0; j < nk; ++j) {
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
+            if (!ok) break;
+            tc_fence_after();
+            float p[128];
+#pragma unroll
+            for (int c32 = 0; c32 < 4; ++c32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + C::T_S + lane_off + c32 * 32, rr);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) p[c32 * 32 + e] = __uint_as_float(rr[e]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(bars->s_read));
+            const int key0 = j * 128;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
+            if (a.causal && j == qb) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > r) p[c] = 0.f;
+            }
+            if (!a.causal && key0 + 128 > a.s) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (key0 + c >= a.s) p[c] = 0.f;
+            }
+            uint32_t kw[4];
+            if (DROP) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) kw[v] = keep_word_row(pk, (uint32_t)(key0 >> 5) + v, (uint32_t)i);
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) kw[v] = 0xffffffffu;
+            }
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c32 = 0; c32 < 4; ++c32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + C::T_DP + lane_off + c32 * 32, rr);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float ds[2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int c = c32 * 32 + 2 * e + t;
+                        const float dpd = __uint_as_float(rr[2 * e + t]);
+                        const float dpv = ((kw[c32] >> (2 * e + t)) & 1u) ? dpd * a.keep_scale : 0.f;
+                        ds[t] = p[c] * (dpv - delta);
+                    }
+                    w[e] = pack_bf16x2(ds[0], ds[1]);
+                }
+                tmem_st16(tmem + C::T_DP + lane_off + c32 * 16, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(bars->ds_full));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c32 = 0; c32 < D / 32; ++c32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + C::T_DQ + lane_off + c32 * 32, rr);
+                stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rr, a.scale);
+            }
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (r == 0 && !bars->abort_flag) {
+            for (int ch = 0; ch < G::NCH; ++ch)
+                tma_store_3d(&tm_dq, sb + C::OFF_Q + ch * C::CHUNK, ch * G::CW, qb * 128, bh);
+            bulk_commit();
+            bulk_wait_read0();
+        }
+    }
+
+    __syncthreads();
+    if (bars->abort_flag) {
+        for (int k = 0; k < 20; ++k) __nanosleep(50000);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ========================================================== launchers ====
+int launch_bwd_pre(const BwdArgs& a, cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)a.c.n_bh * a.s_pad;
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    attn_bwd_pre_kernel<<<grid, 256, 0, stream>>>(a);
+    return (int)cudaGetLastError();
+}
+
+template <int D, bool DROP>
+static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
+                         cudaStream_t stream)
+{
+    constexpr uint32_t smem = DkdvCfg<D>::SMEM;
+    auto kern = attn_bwd_dkdv_kernel<D, DROP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
+    const unsigned grid = (unsigned)a.c.n_blk * n_bkv;
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
+    return (int)cudaGetLastError();
+}
+
+template <int D, bool DROP>
+static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
+{
+    constexpr uint32_t smem = DqCfg<D>::SMEM;
+    auto kern = attn_bwd_dq_kernel<D, DROP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    const unsigned grid = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+    return (int)cudaGetLastError();
+}
+
+int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                    const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
+                    cudaStream_t stream)
+{
+#define AC_DKDV_CASE(DD)                                                                            \
+    case DD:                                                                                        \
+        return dropout ? launch_dkdv_t<DD, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)              \
+                       : launch_dkdv_t<DD, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+    switch (d) {
+        AC_DKDV_CASE(64)
+        AC_DKDV_CASE(96)
+        AC_DKDV_CASE(128)
+        AC_DKDV_CASE(160)
+        default: return (int)cudaErrorInvalidValue;
+    }
+#undef AC_DKDV_CASE
+}
+
+int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
+{
+#define AC_DQ_CASE(DD)                                                                              \
+    case DD:                                                                                        \
+        return dropout ? launch_dq_t<DD, true>(tq, tk, tv, tdo, tdq, a, stream)                     \
+                       : launch_dq_t<DD, false>(tq, tk, tv, tdo, tdq, a, stream);
+    switch (d) {
+        AC_DQ_CASE(64)
+        AC_DQ_CASE(96)
+        AC_DQ_CASE(128)
+        AC_DQ_CASE(160)
+        default: return (int)cudaErrorInvalidValue;
+    }
+#undef AC_DQ_CASE
+}
+
+}  // namespace ac

@@ -1,0 +1,61 @@
+// kernels.h -- internal interface between the C-ABI layer and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ac {
+
+// Query / key tile height of every kernel (TMEM has 128 lanes).
+constexpr int kBlockRows = 128;
+// Threads per CTA of the tensor-core kernels: warp 0 loads Q/K (or K/V),
+// warp 1 issues MMAs and owns TMEM, warp 2 loads V (or the per-row
+// statistics), warp 3 idles, warps 4..7 are the 128 row threads.
+constexpr int kThreads = 256;
+
+struct CommonArgs {
+    int32_t s;            // sequence length (queries == keys)
+    int32_t h_q, h_kv;    // query / key-value heads
+    int32_t n_blk;        // ceil(s / 128)
+    int32_t n_bh;         // b * h_q
+    int32_t causal;
+    float scale_log2;     // score scale * log2(e)
+    float scale;          // score scale
+    float keep_scale;     // 1 / (1 - thr / 65536)
+    uint32_t thr;         // dropout threshold on a 16-bit draw (0: no dropout)
+    uint32_t seed_lo, seed_hi, offset;
+    int32_t* status;      // caller-owned device status word (may be null)
+    uint64_t timeout_ns;  // limit of every in-kernel wait
+    int32_t inject_timeout;  // test hook: every thread waits on a barrier nothing completes
+};
+
+struct FwdArgs {
+    CommonArgs c;
+    float* lse;           // [b*h_q*s]
+};
+
+struct BwdArgs {
+    CommonArgs c;
+    int32_t s_pad;        // n_blk * 128
+    const uint16_t* o;    // bf16 [b*h_q*s*d]
+    const uint16_t* dout; // bf16 [b*h_q*s*d]
+    const float* lse;     // [b*h_q*s]
+    float* lse2_ws;       // [b*h_q*s_pad]  LSE * log2(e); +inf past s
+    float* delta_ws;      // [b*h_q*s_pad]  rowsum(dO * O); 0 past s
+    int32_t d;
+};
+
+// Host launchers; return a cudaError_t value.
+int launch_fwd(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& to, const FwdArgs& a, cudaStream_t stream);
+int launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk,
+                    const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                    const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);
+int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream);
+
+// Query-tile height of the dK/dV kernel for head dimension d (TMEM budget).
+constexpr int dkdv_query_tile(int d) { return (2 * d + 2 * 128 <= 512) ? 128 : 64; }
+
+}  // namespace ac

@@ -1,0 +1,136 @@
+/*
+ * attn_core.h -- C ABI of the GB300 (sm_103a) attention-core library.
+ *
+ * The attention core is QK^T, softmax, softmax dropout and attention over V:
+ * the part of a transformer layer that selective activation recomputation
+ * does not store, because its activations are large and its FLOPs few, and
+ * recomputes in the backward pass instead ("Reducing Activation
+ * Recomputation in Large Transformer Models", dmarx anthology LIT-736, Key
+ * takeaways, fourth bullet; "Recomputing Activations", curionode Plate 2,
+ * second paragraph and "Memory for compute, selectively").
+ *
+ * attn_core_fwd stores only O and one fp32 log-sum-exp per query row; with
+ * Q, K, V and the Philox seed/offset that is everything the backward pass
+ * needs.  attn_core_bwd_recompute rebuilds the scores, probabilities and
+ * dropout mask on chip and never writes them to global memory, so the
+ * 5 a s^2 b byte term of the per-layer activation formula sbh(34 + 5as/h)
+ * is never held in device memory.  attn_core_stored_bytes reports that
+ * accounting exactly.
+ *
+ * Tensors (all device pointers, 16-byte aligned, contiguous, row-major):
+ *   Q, O, dO, dQ : bf16 [b, h_q,  s, d]
+ *   K, V, dK, dV : bf16 [b, h_kv, s, d]
+ *   LSE          : fp32 [b, h_q, s]   natural-log log-sum-exp of each row
+ * Query head h uses KV head h / (h_q / h_kv) (grouped-query attention).
+ * Causal masking is top-left aligned: query i sees keys 0..i.
+ *
+ * Readings the pages leave open (the CPU oracle in the tests follows the
+ * same ones):
+ *   - scale: scale <= 0 selects 1/sqrtf(d), computed in fp32.
+ *   - LSE is in natural-log units.
+ *   - dropout acts on the normalised probabilities, before the product with V.
+ *   - dropout mask: Philox-4x32-10 (Salmon et al., SC'11) with key
+ *     (seed & 0xffffffff, seed >> 32) and counter (j / 8, i, b*h_q + h,
+ *     offset) for query i, key j of query head h in batch b; the call's four
+ *     output words give eight 16-bit draws, key j taking the low half (j even)
+ *     or high half (j odd) of word (j % 8) / 2.  With thr = round(p * 65536)
+ *     (at most 65535) an element is dropped iff its draw < thr, and kept
+ *     elements are scaled by 1 / (1 - thr / 65536).  p == 0 draws nothing.
+ *
+ * Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  The library allocates no device memory: the caller owns
+ * every buffer, including the backward workspace.
+ */
+#ifndef ATTN_CORE_H
+#define ATTN_CORE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  On any non-zero code no kernel has been launched and no
+ * output has been written, except ATTN_CORE_ERR_CUDA from a launch, which
+ * reports the CUDA error of that launch. */
+#define ATTN_CORE_OK 0
+#define ATTN_CORE_ERR_INVALID_ARG 1         /* null pointer, bad shape, p outside [0,1), offset >= 2^32 */
+#define ATTN_CORE_ERR_UNSUPPORTED 2         /* head dimension or device not supported */
+#define ATTN_CORE_ERR_MISALIGNED 3          /* a pointer is not 16-byte aligned (workspace: 256) */
+#define ATTN_CORE_ERR_WORKSPACE_TOO_SMALL 4 /* bwd workspace smaller than attn_core_bwd_workspace_bytes */
+#define ATTN_CORE_ERR_CUDA 5                /* a CUDA runtime or driver call failed */
+#define ATTN_CORE_ERR_DEVICE_TIMEOUT 6      /* a kernel wait ran past its limit (reported via dev_status) */
+
+/* flags */
+#define ATTN_CORE_FLAG_TEST_WAIT_TIMEOUT 0x100 /* test hook: every kernel waits on a barrier that nothing
+                                                  completes; it gives up after wait_timeout_ms, writes
+                                                  ATTN_CORE_ERR_DEVICE_TIMEOUT to dev_status and exits */
+
+typedef struct {
+    int32_t b, h_q, h_kv, s, d; /* s queries == s keys; h_q % h_kv == 0; d in {64, 96, 128, 160} */
+    int32_t causal;             /* 0 or 1 */
+    float p_drop;               /* softmax-dropout probability in [0, 1) */
+    float scale;                /* score scale; <= 0 selects 1/sqrtf(d) */
+    uint64_t seed;              /* Philox key */
+    uint64_t offset;            /* Philox counter word 3; must be < 2^32 */
+    /* Optional caller-owned device int32, zero before the call.  A kernel
+     * whose wait runs out writes (ATTN_CORE_ERR_DEVICE_TIMEOUT | site << 8)
+     * there (first error wins); read it after synchronising.  May be NULL. */
+    int32_t* dev_status;
+    int32_t flags;              /* ATTN_CORE_FLAG_* */
+    uint32_t wait_timeout_ms;   /* limit of each in-kernel wait; 0 selects 2000 ms */
+    /* Optional profiling hook: an array of cudaEvent_t handles, two per
+     * kernel the call launches (fwd: 1 kernel; bwd: 3 kernels, in order
+     * preprocess, dK/dV, dQ), recorded on `stream` immediately before and
+     * after each launch.  May be NULL. */
+    void** timing_events;
+} attn_core_params;
+
+typedef struct {
+    /* Per-layer activation bytes of one rank's shard, hidden h = h_q * d:
+     * the activation-checkpointing page's per-token forms 34d + 5HT,
+     * 34d and 2d ("Recomputing Activations", Workshop) times s * b. */
+    int64_t layer_none;           /* 34 s b h + 5 h_q s^2 b : nothing recomputed */
+    int64_t layer_selective;      /* 34 s b h               : attention core recomputed */
+    int64_t layer_full;           /* 2 s b h                : only the layer input kept */
+    int64_t core_scores_avoided;  /* 5 h_q s^2 b            : what this library never stores */
+    int64_t core_kept;            /* 2 s d b (2 h_q + 2 h_kv): Q, K, V, O in bf16 */
+    int64_t core_recompute_state; /* 4 b h_q s + 16         : LSE and seed/offset */
+} attn_core_bytes;
+
+/* Forward: O and LSE from Q, K, V (the core's forward in the takeaways'
+ * order: QK^T, softmax, softmax dropout, attention over V).  Launches one
+ * kernel.  Writes O and LSE only. */
+int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const void* v, void* o,
+                  float* lse, void* stream);
+
+/* Bytes of device workspace attn_core_bwd_recompute needs:
+ * 8 * b * h_q * ceil(s / 128) * 128 (two fp32 row statistics per padded
+ * query row), 0 if p is invalid. */
+size_t attn_core_bwd_workspace_bytes(const attn_core_params* p);
+
+/* Backward with recomputation: dQ, dK, dV from Q, K, V, O, LSE and dO.  The
+ * scores, probabilities and dropout mask are rebuilt on chip from Q, K, LSE
+ * and (seed, offset); the mask is bit-identical to the forward's.  Launches
+ * three kernels (row statistics, dK/dV, dQ).  `workspace` is caller-owned
+ * device memory of at least attn_core_bwd_workspace_bytes(p) bytes, 256-byte
+ * aligned; its contents on entry do not matter.  dQ, dK, dV are written
+ * whole (no accumulation into existing contents). */
+int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Activation-byte accounting (pure host, integer, exact).  Worked example of
+ * the activation-checkpointing page: Llama 3 70B, s = 8192, b = 1, h_q = 64,
+ * d = 128, 80 layers -> 1.9 TB none, 182.5 GB selective, 10.7 GB full. */
+int attn_core_stored_bytes(const attn_core_params* p, attn_core_bytes* out);
+
+/* Static description of a return code. */
+const char* attn_core_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_CORE_H */

@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol the public header declares, validates its arguments before touching
+the device, and reports the activation-byte accounting exactly."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_core_gb300 as ac
+import oracle
+from attention_core_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return ac.load_library()
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            src = open(os.path.join(inc, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(attn_core_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("attn_core_fwd", "attn_core_bwd_recompute", "attn_core_stored_bytes",
+              "attn_core_bwd_workspace_bytes", "attn_core_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(ac.LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(raw, n), n
+
+
+def test_strerror(lib):
+    assert ac.attn_core_strerror(ac.OK) == "ok"
+    assert "workspace" in ac.attn_core_strerror(ac.ERR_WORKSPACE_TOO_SMALL)
+    assert "time limit" in ac.attn_core_strerror(ac.ERR_DEVICE_TIMEOUT | (3 << 8))
+
+
+def _p(**kw):
+    base = dict(b=1, h_q=2, h_kv=2, s=128, d=64, causal=True, p_drop=0.1, seed=1, offset=0)
+    base.update(kw)
+    return ac.Params(**base)
+
+
+FAKE = 0x7f0000000000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(b=0), ac.ERR_INVALID_ARG),
+    (dict(s=-1), ac.ERR_INVALID_ARG),
+    (dict(h_q=3, h_kv=2), ac.ERR_INVALID_ARG),
+    (dict(p_drop=1.0), ac.ERR_INVALID_ARG),
+    (dict(p_drop=-0.1), ac.ERR_INVALID_ARG),
+    (dict(p_drop=float("nan")), ac.ERR_INVALID_ARG),
+    (dict(offset=2**32), ac.ERR_INVALID_ARG),
+    (dict(causal=2), ac.ERR_INVALID_ARG),
+    (dict(d=80), ac.ERR_UNSUPPORTED),
+    (dict(d=256), ac.ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_params(lib, kw, code):
+    assert ac.attn_core_fwd(_p(**kw), FAKE, FAKE, FAKE, FAKE, FAKE, 0) == code
+
+
+def test_fwd_rejects_null_and_misaligned(lib):
+    assert ac.attn_core_fwd(_p(), 0, FAKE, FAKE, FAKE, FAKE, 0) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_fwd(_p(), FAKE + 8, FAKE, FAKE, FAKE, FAKE, 0) == ac.ERR_MISALIGNED
+    assert ac.attn_core_fwd(_p(), FAKE, FAKE, FAKE, FAKE, FAKE + 4, 0) == ac.ERR_MISALIGNED
+
+
+def test_bwd_workspace_and_validation(lib):
+    p = _p(s=200)
+    ws = ac.attn_core_bwd_workspace_bytes(p)
+    assert ws == 2 * 4 * 1 * 2 * 256   # two fp32 statistics per padded query row
+    assert ac.attn_core_bwd_workspace_bytes(_p(b=0)) == 0
+    args = [FAKE] * 10
+    assert ac.attn_core_bwd_recompute(p, *args, ws - 1, 0) == ac.ERR_WORKSPACE_TOO_SMALL
+    a2 = list(args)
+    a2[9] = FAKE + 16                  # workspace needs 256-byte alignment
+    assert ac.attn_core_bwd_recompute(p, *a2, ws, 0) == ac.ERR_MISALIGNED
+    a3 = list(args)
+    a3[5] = 0                          # dout
+    assert ac.attn_core_bwd_recompute(p, *a3, ws, 0) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_bwd_recompute(_p(d=48), *args, ws, 0) == ac.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape", [(1, 64, 64, 8192, 128), (2, 12, 12, 2048, 128),
+                                   (4, 8, 8, 2048, 96), (1, 16, 16, 2048, 160),
+                                   (1, 64, 8, 8192, 128), (3, 6, 2, 333, 64)])
+def test_stored_bytes_match_oracle(lib, shape):
+    b, hq, hkv, s, d = shape
+    got = ac.stored_bytes(b, hq, hkv, s, d)
+    ref = oracle.stored_bytes(oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d))
+    assert got == ref
+
+
+def test_stored_bytes_llama_worked_example(lib):
+    sb = ac.stored_bytes(1, 64, 8, 8192, 128)
+    assert sb["layer_none"] * 80 == 1_900_523_028_480
+    assert sb["layer_selective"] * 80 == 182_536_110_080
+    assert sb["layer_full"] * 80 == 10_737_418_240
+    # what the core actually keeps under GQA: Q and O at 64 heads, K and V at 8
+    assert sb["core_kept"] == 2 * 8192 * 128 * (2 * 64 + 2 * 8)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    saved = ac._lib
+    try:
+        ac._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            ac.load_library(str(tmp_path / "missing.so"))
+    finally:
+        ac._lib = saved

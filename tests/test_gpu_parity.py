@@ -1,0 +1,158 @@
+"""GPU parity against the CPU oracle, element by element, on sizes the oracle
+finishes in seconds: several 128-row tiles, ragged tails, every supported head
+dimension, causal and not, GQA, p = 0 and p > 0, and the degenerate s = 1.
+Also: bit-exact dropout masks read out through probe inputs, determinism,
+and the bounded-wait error path."""
+import numpy as np
+import pytest
+import torch
+
+import attention_core_gb300 as ac
+import oracle
+from attention_core_gb300.inputs import (dq_mask_probe, dv_mask_probe, fwd_mask_probe,
+                                         random_inputs)
+from tests.gpu_util import LSE_TOL, TOL, row_rel_err, run_gpu, to_np
+
+pytestmark = pytest.mark.gpu
+
+# (b, h_q, h_kv, s, d, causal, p_drop)
+CASES = [
+    (1, 2, 2, 128, 64, True, 0.1),     # the tiny configuration
+    (1, 2, 2, 300, 64, True, 0.1),
+    (1, 2, 2, 300, 96, True, 0.1),
+    (1, 2, 2, 300, 128, True, 0.1),
+    (1, 2, 2, 300, 160, True, 0.1),
+    (2, 4, 2, 256, 128, True, 0.0),    # GQA 2:1, p = 0
+    (1, 4, 1, 200, 64, True, 0.1),     # GQA 4:1, ragged
+    (1, 8, 1, 384, 96, True, 0.1),     # GQA 8:1 like the Llama layer
+    (1, 2, 2, 300, 128, False, 0.1),   # not causal, ragged
+    (1, 2, 2, 256, 96, False, 0.0),
+    (1, 2, 1, 330, 160, False, 0.25),
+    (1, 1, 1, 1, 64, True, 0.1),       # s = 1
+    (1, 1, 1, 17, 160, False, 0.3),
+    (3, 2, 2, 130, 128, True, 0.5),
+]
+
+
+def _ids(c):
+    b, hq, hkv, s, d, causal, p = c
+    return f"b{b}_h{hq}x{hkv}_s{s}_d{d}_{'c' if causal else 'nc'}_p{p}"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_fwd_bwd_match_oracle(case):
+    b, hq, hkv, s, d, causal, p = case
+    seed = 1234 if s == 128 else 987654321 + s
+    t = random_inputs(b, hq, hkv, s, d, seed=0 if s == 128 else s + d)
+    out = run_gpu(t, causal, p, seed)
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=causal, p_drop=p, seed=seed)
+    ro, rlse = oracle.fwd(pr, t.q, t.k, t.v)
+    rdq, rdk, rdv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    errs = {"o": row_rel_err(to_np(out["o"]), ro), "dq": row_rel_err(to_np(out["dq"]), rdq),
+            "dk": row_rel_err(to_np(out["dk"]), rdk), "dv": row_rel_err(to_np(out["dv"]), rdv)}
+    lse_err = float(np.abs(to_np(out["lse"]) - rlse).max())
+    assert lse_err <= LSE_TOL, lse_err
+    assert all(e <= TOL for e in errs.values()), errs
+
+
+def test_custom_scale_and_offset():
+    b, hq, hkv, s, d = 1, 2, 2, 200, 128
+    t = random_inputs(b, hq, hkv, s, d, seed=11)
+    out = run_gpu(t, True, 0.2, seed=2**40 + 5, offset=123456, scale=0.05)
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=True, p_drop=0.2,
+                        seed=2**40 + 5, offset=123456, scale=0.05)
+    ro, rlse = oracle.fwd(pr, t.q, t.k, t.v)
+    rdq, rdk, rdv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    assert row_rel_err(to_np(out["o"]), ro) <= TOL
+    assert float(np.abs(to_np(out["lse"]) - rlse).max()) <= LSE_TOL
+    for name, ref in (("dq", rdq), ("dk", rdk), ("dv", rdv)):
+        assert row_rel_err(to_np(out[name]), ref) <= TOL, name
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 128, 64), (1, 2, 300, 128), (2, 1, 260, 96),
+                                   (1, 2, 200, 160)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_forward_mask_bit_exact(shape, causal):
+    """O column c of row i is non-zero exactly when key w0 + c is kept."""
+    b, h, s, d = shape
+    seed = 1234
+    pr = oracle.Problem(b=b, h_q=h, h_kv=h, s=s, d=d, causal=causal, p_drop=0.1, seed=seed)
+    masks = [oracle.mask_rows(pr, bh, 0, s) for bh in range(b * h)]
+    for w0 in range(0, s, d):
+        t = fwd_mask_probe(b, h, h, s, d, w0)
+        o = to_np(run_gpu(t, causal, 0.1, seed, bwd=False)["o"]).reshape(b * h, s, d)
+        width = min(d, s - w0)
+        for bh in range(b * h):
+            got = (o[bh, :, :width] != 0).astype(np.uint8)
+            assert np.array_equal(got, masks[bh][:, w0:w0 + width]), (bh, w0)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 128, 64), (1, 2, 300, 128), (1, 1, 260, 160)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_mask_bit_exact_through_dv(shape, causal):
+    """dV column c of key row j is non-zero exactly when (query w0 + c, key j) is kept:
+    the dK/dV kernel's recomputed (transposed) mask equals the forward's."""
+    b, h, s, d = shape
+    seed = 77
+    pr = oracle.Problem(b=b, h_q=h, h_kv=h, s=s, d=d, causal=causal, p_drop=0.1, seed=seed)
+    masks = [oracle.mask_rows(pr, bh, 0, s) for bh in range(b * h)]
+    for w0 in range(0, s, d):
+        t = dv_mask_probe(b, h, h, s, d, w0)
+        dv = to_np(run_gpu(t, causal, 0.1, seed)["dv"]).reshape(b * h, s, d)
+        width = min(d, s - w0)
+        for bh in range(b * h):
+            got = (dv[bh, :, :width] != 0).astype(np.uint8)           # [key j, query w0+c]
+            assert np.array_equal(got, masks[bh][w0:w0 + width, :].T), (bh, w0)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_mask_through_dq(causal):
+    """dQ on probe inputs takes one of two separated values per element
+    depending on the mask: element-wise parity with the oracle is exact up to
+    bf16 rounding and fails on any flipped mask bit."""
+    b, h, s, d = 1, 2, 256, 128
+    seed = 4242
+    pr = oracle.Problem(b=b, h_q=h, h_kv=h, s=s, d=d, causal=causal, p_drop=0.1, seed=seed)
+    for w0 in (0, 128):
+        t = dq_mask_probe(b, h, h, s, d, w0)
+        dq = to_np(run_gpu(t, causal, 0.1, seed)["dq"])
+        rdq, _, _ = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+        assert row_rel_err(dq, rdq) <= TOL
+
+
+def test_deterministic():
+    """No atomics anywhere: two runs give identical bits."""
+    t = random_inputs(1, 4, 2, 384, 128, seed=3)
+    a = run_gpu(t, True, 0.1, seed=9)
+    b_ = run_gpu(t, True, 0.1, seed=9)
+    for k in a:
+        assert torch.equal(a[k], b_[k]), k
+
+
+def test_wait_timeout_reports_status_and_context_survives():
+    """Test hook: every kernel waits on a barrier nothing completes; each wait
+    gives up after 50 ms, the status word reads DEVICE_TIMEOUT, and the next
+    normal call on the same context is correct."""
+    dev = torch.device("cuda:0")
+    t = random_inputs(1, 2, 2, 128, 64, seed=0)
+    q, k, v, g = (x.to(dev) for x in (t.q, t.k, t.v, t.dout))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kw = dict(causal=True, p_drop=0.1, seed=1234, dev_status=status.data_ptr(),
+              flags=ac.FLAG_TEST_WAIT_TIMEOUT, wait_timeout_ms=50)
+    o, lse = ac.fwd(q, k, v, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0xFF == ac.ERR_DEVICE_TIMEOUT
+    status.zero_()
+    ac.bwd_recompute(q, k, v, o, lse, g, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0xFF == ac.ERR_DEVICE_TIMEOUT
+    out = run_gpu(t, True, 0.1, 1234)
+    pr = oracle.Problem(b=1, h_q=2, h_kv=2, s=128, d=64, causal=True, p_drop=0.1, seed=1234)
+    ro, _ = oracle.fwd(pr, t.q, t.k, t.v)
+    assert row_rel_err(to_np(out["o"]), ro) <= TOL
