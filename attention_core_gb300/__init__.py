@@ -213,7 +213,8 @@ def bwd_recompute(q, k, v, o, lse, dout, *, causal: bool = True, p_drop: float =
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     rc = attn_core_bwd_recompute(p, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                  lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                 dv.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
+                                 dv.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream())
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_bwd_recompute")
     return dq, dk, dv

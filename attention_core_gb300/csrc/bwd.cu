@@ -10,13 +10,17 @@
 //     dV = (P * Z)^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K
 // (D_i equals sum_j P_ij dP_ij because O_i = sum_j P_ij Z_ij V_j).
 //
-// Three kernels:
-//   bwd_pre   D_i and LSE_i * log2(e) per query row into a padded workspace
+// Three kernels, launched in this order:
+//   bwd_pre   per query row, LSE_i * log2(e) and a first estimate
+//             D~_i = rowsum(dO_i * O_i) from the bf16 output, into a padded
+//             workspace
+//   bwd_dq    one (query head, 128-query block) per CTA; queries on TMEM
+//             lanes; recomputes S and dP per key block, accumulates dQ in TMEM
+//             with the exact statistic D_i = sum_j P_ij dP_ij (see below) and
+//             writes that D_i back to the workspace
 //   bwd_dkdv  one (KV head, 128-key block) per CTA; keys on TMEM lanes; loops
 //             over the query heads of the GQA group and their query tiles;
 //             recomputes S^T and dP^T, accumulates dV and dK in TMEM
-//   bwd_dq    one (query head, 128-query block) per CTA; queries on TMEM
-//             lanes; recomputes S and dP per key block, accumulates dQ in TMEM
 // Neither gradient kernel writes a partial sum to global memory: each output
 // tile is finished in TMEM and stored once.
 #include "kernels.h"
@@ -37,8 +41,8 @@ __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site
 }  // namespace
 
 // ======================================================= preprocess ======
-// One warp per padded query row: D_i = sum_c dO_ic O_ic in fp32 and
-// LSE_i * log2(e); rows past s get D = 0 and +inf (their probabilities
+// One warp per padded query row: D~_i = sum_c dO_ic O_ic in fp32 and
+// LSE_i * log2(e); rows past s get 0 and +inf (their probabilities
 // recompute to exactly 0).
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdArgs a)
 {
@@ -386,24 +390,37 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 }
 
 // =============================================================== dQ ======
+// One (query head, 128-query block) per CTA; queries on TMEM lanes.  Per
+// key block j: S = Q K_j^T and dP_d = dO V_j^T into TMEM; the row threads
+// form P, the mask, dP = dP_d * Z and
+//     dS~ = P (dP - D~),        D~ = rowsum(dO * O) from the bf16 output,
+// and accumulate the exact row statistic D = sum_j P_ij dP_ij in fp32.  The
+// tensor core accumulates dQ~ += dS~ K_j and PK += P K_j.  At the end
+//     dQ = scale (dQ~ - (D - D~) PK),
+// which equals scale * sum_j P_ij (dP_ij - D_i) K_j: the gradient with the
+// exact statistic, not the one rounded through the stored bf16 output.  The
+// exact D is written back to the workspace for the dK/dV kernel.
 namespace {
 
 template <int D>
 struct DqCfg {
     using G = TileGeom<D>;
-    static constexpr uint32_t TILE = G::template tile_bytes<128>();
-    static constexpr uint32_t CHUNK = G::template chunk_bytes<128>();
-    static constexpr int KST = 2;                    // K is read by S and by dQ: two stages
-    static constexpr int VST = (D <= 128) ? 2 : 1;
+    static constexpr int BN = dq_key_tile(D);
+    static constexpr uint32_t QT = G::template tile_bytes<128>();
+    static constexpr uint32_t QCH = G::template chunk_bytes<128>();
+    static constexpr uint32_t KT = G::template tile_bytes<BN>();
+    static constexpr uint32_t KCH = G::template chunk_bytes<BN>();
+    static constexpr int KST = 2, VST = 2;
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_DO = TILE;
-    static constexpr uint32_t OFF_K = 2 * TILE;
-    static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
-    static constexpr uint32_t OFF_BAR = OFF_V + VST * TILE;
+    static constexpr uint32_t OFF_DO = QT;
+    static constexpr uint32_t OFF_K = 2 * QT;
+    static constexpr uint32_t OFF_V = OFF_K + KST * KT;
+    static constexpr uint32_t OFF_BAR = OFF_V + VST * KT;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
-    static_assert(T_DQ + D <= 512, "TMEM budget");
+    // TMEM: S | dP (later dS~ in its first half, P in its second) | dQ~ | PK
+    static constexpr uint32_t T_S = 0, T_DP = BN, T_DQ = 2 * BN, T_PK = 2 * BN + D;
+    static_assert(T_PK + D <= 512, "TMEM budget");
 };
 
 struct DqBars {
@@ -425,6 +442,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 {
     using G = TileGeom<D>;
     using C = DqCfg<D>;
+    constexpr int BN = C::BN;
     constexpr int KST = C::KST, VST = C::VST;
     const CommonArgs& a = args.c;
 
@@ -440,7 +458,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int bh = (int)(blockIdx.x % n_bh);
     const int group = a.h_q / a.h_kv;
     const int bkv = (bh / a.h_q) * a.h_kv + (bh % a.h_q) / group;
-    const int nk = a.causal ? (qb + 1) : a.n_blk;
+    const int n_kblk = (a.s + BN - 1) / BN;
+    const int nk = a.causal ? min((qb + 1) * (128 / BN), n_kblk) : n_kblk;
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
@@ -482,18 +501,18 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (alive && warp == 0) {
         if (lane == 0) {
             // ---- TMA producer: Q and dO once, then the K ring
-            mbar_arrive_expect_tx(bar(bars->qdo_full), 2 * C::TILE);
+            mbar_arrive_expect_tx(bar(bars->qdo_full), 2 * C::QT);
             for (int ch = 0; ch < G::NCH; ++ch) {
-                tma_load_3d(sb + C::OFF_Q + ch * C::CHUNK, &tm_q, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
-                tma_load_3d(sb + C::OFF_DO + ch * C::CHUNK, &tm_do, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
+                tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
+                tma_load_3d(sb + C::OFF_DO + ch * C::QCH, &tm_do, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
             }
             for (int j = 0; j < nk; ++j) {
                 const int st = j % KST;
                 if (!wait_bounded(wc, bar(bars->k_empty[st]), ((j / KST) & 1) ^ 1, timeout_code(kSiteKEmpty)))
                     break;
-                mbar_arrive_expect_tx(bar(bars->k_full[st]), C::TILE);
+                mbar_arrive_expect_tx(bar(bars->k_full[st]), C::KT);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_K + st * C::TILE + ch * C::CHUNK, &tm_k, ch * G::CW, j * 128, bkv,
+                    tma_load_3d(sb + C::OFF_K + st * C::KT + ch * C::KCH, &tm_k, ch * G::CW, j * BN, bkv,
                                 bar(bars->k_full[st]));
             }
         }
@@ -504,25 +523,25 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int st = j % VST;
                 if (!wait_bounded(wc, bar(bars->v_empty[st]), ((j / VST) & 1) ^ 1, timeout_code(kSiteVEmpty)))
                     break;
-                mbar_arrive_expect_tx(bar(bars->v_full[st]), C::TILE);
+                mbar_arrive_expect_tx(bar(bars->v_full[st]), C::KT);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_V + st * C::TILE + ch * C::CHUNK, &tm_v, ch * G::CW, j * 128, bkv,
+                    tma_load_3d(sb + C::OFF_V + st * C::KT + ch * C::KCH, &tm_v, ch * G::CW, j * BN, bkv,
                                 bar(bars->v_full[st]));
             }
         }
     } else if (alive && warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer.  Order: S0 dP0 | S1 dQ0 dP1 | S2 dQ1 dP2 | ...
-            constexpr uint32_t IDS = idesc_bf16(128, 128, false, false);  // S = Q K^T, dP = dO V^T
-            constexpr uint32_t IDQ = idesc_bf16(128, D, false, true);     // dQ += dS K
+            // ---- MMA issuer.  Order: S0 dP0 | S1 dQ0 PK0 dP1 | S2 dQ1 PK1 dP2 | ...
+            constexpr uint32_t IDS = idesc_bf16(128, BN, false, false);  // S = Q K^T, dP_d = dO V^T
+            constexpr uint32_t IDQ = idesc_bf16(128, D, false, true);    // dQ~ += dS~ K, PK += P K
             auto issue_s = [&](int j) -> bool {
                 const int st = j % KST;
                 if (!wait_bounded(wc, bar(bars->k_full[st]), (j / KST) & 1, timeout_code(kSiteKFull))) return false;
                 tc_fence_after();
-                const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
+                const uint32_t kbase = sb + C::OFF_K + st * C::KT;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::T_S, G::template desc_k<128>(sb + C::OFF_Q, kk), G::template desc_k<128>(kbase, kk),
+                    mma_ss(tmem + C::T_S, G::template desc_k<128>(sb + C::OFF_Q, kk), G::template desc_k<BN>(kbase, kk),
                            IDS, kk > 0 ? 1u : 0u);
                 mma_commit(bar(bars->s_full));
                 return true;
@@ -531,11 +550,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int st = j % VST;
                 if (!wait_bounded(wc, bar(bars->v_full[st]), (j / VST) & 1, timeout_code(kSiteVFull))) return false;
                 tc_fence_after();
-                const uint32_t vbase = sb + C::OFF_V + st * C::TILE;
+                const uint32_t vbase = sb + C::OFF_V + st * C::KT;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + C::T_DP, G::template desc_k<128>(sb + C::OFF_DO, kk),
-                           G::template desc_k<128>(vbase, kk), IDS, kk > 0 ? 1u : 0u);
+                           G::template desc_k<BN>(vbase, kk), IDS, kk > 0 ? 1u : 0u);
                 mma_commit(bar(bars->v_empty[st]));
                 mma_commit(bar(bars->dp_full));
                 return true;
@@ -553,11 +572,14 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 const int st = j % KST;
-                const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
+                const uint32_t kbase = sb + C::OFF_K + st * C::KT;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + C::T_DQ, tmem + C::T_DP + kk * 8, G::template desc_mn<128>(kbase, kk), IDQ,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t bdesc = G::template desc_mn<BN>(kbase, kk);
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tmem + C::T_DQ, tmem + C::T_DP + kk * 8, bdesc, IDQ, acc);
+                    mma_ts(tmem + C::T_PK, tmem + C::T_DP + BN / 2 + kk * 8, bdesc, IDQ, acc);
+                }
                 mma_commit(bar(bars->k_empty[st]));
                 if (j + 1 < nk) ok = issue_dp(j + 1);
             }
@@ -570,16 +592,17 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int i = qb * 128 + r;
         const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
         const float lse2 = args.lse2_ws[srow];
-        const float delta = args.delta_ws[srow];
+        const float d_tilde = args.delta_ws[srow];
         const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+        float d_exact = 0.f;
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
-            float p[128];
+            float p[BN];
 #pragma unroll
-            for (int c32 = 0; c32 < 4; ++c32) {
+            for (int c32 = 0; c32 < BN / 32; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_S + lane_off + c32 * 32, rr);
 #pragma unroll
@@ -587,32 +610,32 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             tc_fence_before();
             mbar_arrive(bar(bars->s_read));
-            const int key0 = j * 128;
+            const int key0 = j * BN;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
-            if (a.causal && j == qb) {
+            for (int c = 0; c < BN; ++c) p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
+            if (a.causal && key0 + BN > qb * 128) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > r) p[c] = 0.f;
+                for (int c = 0; c < BN; ++c)
+                    if (key0 + c > i) p[c] = 0.f;
             }
-            if (!a.causal && key0 + 128 > a.s) {
+            if (!a.causal && key0 + BN > a.s) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
+                for (int c = 0; c < BN; ++c)
                     if (key0 + c >= a.s) p[c] = 0.f;
             }
-            uint32_t kw[4];
+            uint32_t kw[BN / 32];
             if (DROP) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) kw[v] = keep_word_row(pk, (uint32_t)(key0 >> 5) + v, (uint32_t)i);
+                for (int v = 0; v < BN / 32; ++v) kw[v] = keep_word_row(pk, (uint32_t)(key0 >> 5) + v, (uint32_t)i);
             } else {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) kw[v] = 0xffffffffu;
+                for (int v = 0; v < BN / 32; ++v) kw[v] = 0xffffffffu;
             }
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c32 = 0; c32 < 4; ++c32) {
+            for (int c32 = 0; c32 < BN / 32; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DP + lane_off + c32 * 32, rr);
                 uint32_t w[16];
@@ -624,11 +647,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         const int c = c32 * 32 + 2 * e + t;
                         const float dpd = __uint_as_float(rr[2 * e + t]);
                         const float dpv = ((kw[c32] >> (2 * e + t)) & 1u) ? dpd * a.keep_scale : 0.f;
-                        ds[t] = p[c] * (dpv - delta);
+                        d_exact = fmaf(p[c], dpv, d_exact);
+                        ds[t] = p[c] * (dpv - d_tilde);
                     }
                     w[e] = pack_bf16x2(ds[0], ds[1]);
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + c32 * 16, w);
+            }
+            // P (before dropout) into the second half of the dP columns, all read by now
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h) {
+                uint32_t pw[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(p[h * 64 + 2 * e], p[h * 64 + 2 * e + 1]);
+                tmem_st32(tmem + C::T_DP + BN / 2 + lane_off + h * 32, pw);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -637,18 +669,24 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
         if (ok) {
             tc_fence_after();
+            const float eps = d_exact - d_tilde;
 #pragma unroll 1
             for (int c32 = 0; c32 < D / 32; ++c32) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + C::T_DQ + lane_off + c32 * 32, rr);
-                stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rr, a.scale);
+                uint32_t rq[32], rp[32];
+                tmem_ld32(tmem + C::T_DQ + lane_off + c32 * 32, rq);
+                tmem_ld32(tmem + C::T_PK + lane_off + c32 * 32, rp);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    rq[e] = __float_as_uint(fmaf(-eps, __uint_as_float(rp[e]), __uint_as_float(rq[e])));
+                stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rq, a.scale);
             }
+            args.delta_ws[srow] = d_exact;
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, 128);
         if (r == 0 && !bars->abort_flag) {
             for (int ch = 0; ch < G::NCH; ++ch)
-                tma_store_3d(&tm_dq, sb + C::OFF_Q + ch * C::CHUNK, ch * G::CW, qb * 128, bh);
+                tma_store_3d(&tm_dq, sb + C::OFF_Q + ch * C::QCH, ch * G::CW, qb * 128, bh);
             bulk_commit();
             bulk_wait_read0();
         }

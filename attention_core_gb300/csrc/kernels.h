@@ -41,7 +41,8 @@ struct BwdArgs {
     const uint16_t* dout; // bf16 [b*h_q*s*d]
     const float* lse;     // [b*h_q*s]
     float* lse2_ws;       // [b*h_q*s_pad]  LSE * log2(e); +inf past s
-    float* delta_ws;      // [b*h_q*s_pad]  rowsum(dO * O); 0 past s
+    float* delta_ws;      // [b*h_q*s_pad]  row statistic D: rowsum(dO * O) from the
+                          // preprocess, replaced by sum_j P_ij dP_ij by the dQ kernel
     int32_t d;
 };
 
@@ -57,5 +58,8 @@ int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap&
 
 // Query-tile height of the dK/dV kernel for head dimension d (TMEM budget).
 constexpr int dkdv_query_tile(int d) { return (2 * d + 2 * 128 <= 512) ? 128 : 64; }
+// Key-block width of the dQ kernel for head dimension d (TMEM budget:
+// S, dP, and two d-wide accumulators).
+constexpr int dq_key_tile(int d) { return (2 * 128 + 2 * d <= 512) ? 128 : 64; }
 
 }  // namespace ac

@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the attention core under selective activation recomputation.
+
+One step = forward (S = QK^T with causal mask and scale, softmax, softmax
+dropout, O = P_d V, LSE) plus the recompute-backward (row statistics, dK/dV,
+dQ) over one batch of synthetic bf16 inputs of the named workload, through the
+library's C ABI.  Default workload: the GPT-3-style 175B layer, one
+tensor-parallel rank's shard (b=2, 12 local heads, s=2048, d_head=128,
+causal, p=0.1).
+
+Prints one JSON line (rank 0).  Metric: combined fwd + recompute-bwd
+TFLOP/s with algorithmic FLOPs 14 d b h s(s+1)/2 (fwd 4, bwd 10: the
+recomputed QK^T plus dV, dP, dQ, dK), and its share of the measured dense
+BF16 tensor peak.
+
+--impl reference runs the CPU oracle on the host cores instead (rank 0 only),
+each step a bounded sample (query and key rows) of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+core shards by independent heads; no collective on the data path), so work
+per GPU is fixed ("scaling": "weak") and value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _flops(w) -> dict:
+    pairs = w["s"] * (w["s"] + 1) // 2
+    u = w["d"] * pairs * w["b"] * w["h_q"]
+    return {"fwd": 4 * u, "bwd": 10 * u, "total": 14 * u, "model": 12 * u,
+            # algorithmic FLOPs of each kernel's launch
+            "k_fwd": 4 * u, "k_dkdv": 8 * u, "k_dq": 2 * u}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": float(pk["bf16_tflops"]), "hbm_gbs": float(pk["hbm_gbs"]),
+                "source": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _csrc_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_core_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/traffic.txt, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = _csrc_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[3] == cur:
+                return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the GPU is busy."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.dev = dev_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _workload(name):
+    from attention_core_gb300.inputs import WORKLOADS
+    w = dict(WORKLOADS[name])
+    w["name"] = name
+    return w
+
+
+def _config(w, extra=None):
+    c = {"workload": w["name"], "b": w["b"], "h_q": w["h_q"], "h_kv": w["h_kv"], "s": w["s"],
+         "d_head": w["d"], "causal": True, "p_drop": w["p_drop"]}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def _oracle_sample(w, budget_s: float, seed: int):
+    """Time the oracle on a bounded sample of the workload: forward and dQ for a
+    set R of query rows, dK/dV for a set C of key rows, all of one KV group.
+    The 14 d FLOPs of each causal pair (i, j) are credited as 10 d to query row
+    i (QK^T and P.V forward; QK^T, dP and dQ backward) and 4 d to key row j (dV,
+    dK), so whole rows of both sets add up to the workload's count.
+    Returns (seconds, credited flops, threads, description)."""
+    import numpy as np
+
+    import oracle
+    from attention_core_gb300.inputs import random_inputs
+    s, d, g = w["s"], w["d"], w["h_q"] // w["h_kv"]
+    t = random_inputs(1, g, 1, s, d, seed=seed)
+    q, k, v, dout = (x.double().numpy() for x in (t.q, t.k, t.v, t.dout))
+    pr = oracle.Problem(b=1, h_q=g, h_kv=1, s=s, d=d, causal=True, p_drop=w["p_drop"], seed=seed)
+    oracle.build()
+
+    def run(n):
+        rows = np.arange(n, dtype=np.int64) * 7919 % s            # spread over the sequence
+        heads = np.arange(n, dtype=np.int64) % g
+        krows = np.linspace(s - max(1, s // 16), s - 1, max(1, n // 4)).astype(np.int64)
+        kheads = np.zeros(len(krows), dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.fwd_rows(pr, q, k, v, heads, rows)
+        oracle.dq_rows(pr, q, k, v, dout, heads, rows)
+        oracle.dkdv_rows(pr, q, k, v, dout, kheads, krows)
+        dt = time.perf_counter() - t0
+        flops = 10 * d * int((rows + 1).sum()) + 4 * d * g * int((s - krows).sum())
+        return dt, flops, f"{n} query rows and {len(krows)} key rows of one KV group"
+
+    n = 32
+    dt, flops, desc = run(n)
+    while dt < budget_s / 2 and n < 64 * s * g:
+        n = int(n * min(16.0, max(2.0, budget_s / max(dt, 1e-3))))
+        dt, flops, desc = run(n)
+    return dt, flops, len(os.sched_getaffinity(0)), desc
+
+
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        _oracle_sample(w, per_step, seed=1 + i)
+    tot_t, tot_f, threads, desc = 0.0, 0, 1, ""
+    for i in range(args.steps):
+        dt, fl, threads, desc = _oracle_sample(w, per_step, seed=100 + i)
+        tot_t += dt
+        tot_f += fl
+    val = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": "attn-core fwd+recompute-bwd TFLOP/s", "value": val,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, {"sample_per_step": desc}),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc + " per step", "cpu": _cpu_model()},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU ----
+
+def run_ours(args, w):
+    import secrets
+
+    import torch
+
+    import attention_core_gb300 as ac
+    from attention_core_gb300 import build as lib_build
+    from attention_core_gb300.inputs import random_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        lib_build.build()
+    if dist is not None:
+        dist.barrier()
+    ac.load_library()
+
+    b, hq, hkv, s, d, p = w["b"], w["h_q"], w["h_kv"], w["s"], w["d"], w["p_drop"]
+    fl = _flops(w)
+    seed = secrets.randbits(63)
+    base = random_inputs(b, hq, hkv, s, d, seed=rank)
+    per_set = 2 * (4 * b * hq * s * d + 4 * b * hkv * s * d) + 4 * b * hq * s
+    pr = ac.Params(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=True, p_drop=p, seed=seed)
+    ws_bytes = ac.attn_core_bwd_workspace_bytes(pr)
+    per_set += ws_bytes
+    n_sets = max(1, math.ceil(3 * L2_BYTES / per_set))
+    sets = []
+    for i in range(n_sets):
+        q, k, v, g = (x.to(dev) for x in (base.q, base.k, base.v, base.dout))
+        sets.append({
+            "q": q, "k": k, "v": v, "dout": g, "o": torch.empty_like(q),
+            "lse": torch.empty((b, hq, s), dtype=torch.float32, device=dev),
+            "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+            "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev)})
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(ts, ev_ptr=0):
+        pr.dev_status = status.data_ptr()
+        pr.timing_events = ev_ptr
+        rc = ac.attn_core_fwd(pr, ts["q"].data_ptr(), ts["k"].data_ptr(), ts["v"].data_ptr(),
+                              ts["o"].data_ptr(), ts["lse"].data_ptr(), sh)
+        if rc:
+            raise ac.AttnCoreError(rc, "attn_core_fwd")
+        pr.timing_events = ev_ptr + 2 * ctypes.sizeof(ctypes.c_void_p) if ev_ptr else 0
+        rc = ac.attn_core_bwd_recompute(
+            pr, ts["q"].data_ptr(), ts["k"].data_ptr(), ts["v"].data_ptr(), ts["o"].data_ptr(),
+            ts["lse"].data_ptr(), ts["dout"].data_ptr(), ts["dq"].data_ptr(),
+            ts["dk"].data_ptr(), ts["dv"].data_ptr(), ts["ws"].data_ptr(), ws_bytes, sh)
+        if rc:
+            raise ac.AttnCoreError(rc, "attn_core_bwd_recompute")
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize(dev)
+
+    # per-kernel events: fwd, pre, dq, dkdv -> 8 events per step
+    K = args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(8 * K)]
+    for e in evs:              # torch creates the CUDA event at its first record
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    ev_arr = (ctypes.c_void_p * (8 * K))(*[e.cuda_event for e in evs])
+    ev_base = ctypes.addressof(ev_arr)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for i in range(K):
+        step(sets[i % n_sets], ev_base + 8 * i * ctypes.sizeof(ctypes.c_void_p))
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} during the timed region")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    names = ["fwd", "pre", "dq", "dkdv"]
+    kt = {n: [] for n in names}
+    for i in range(K):
+        for j, n in enumerate(names):
+            kt[n].append(evs[8 * i + 2 * j].elapsed_time(evs[8 * i + 2 * j + 1]))
+    kavg = {n: sum(v) / len(v) for n, v in kt.items()}
+    fwd_ms = kavg["fwd"]
+    bwd_ms = kavg["pre"] + kavg["dkdv"] + kavg["dq"]
+
+    pk = _peaks()
+    total_units = fl["total"] * K * world
+    value = total_units / (elapsed_ms / 1e3) / 1e12
+    dom = max(("fwd", "dkdv", "dq"), key=lambda n: kavg[n])
+    dom_flops = fl["k_" + dom]
+    achieved = dom_flops / (kavg[dom] / 1e3) / 1e12
+    kname = {"fwd": "attn_fwd_kernel", "dkdv": "attn_bwd_dkdv_kernel", "dq": "attn_bwd_dq_kernel"}[dom]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, w, pr, base, dev, stream, ws_bytes, fl, world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, cflops, threads, desc = _oracle_sample(w, args.cpu_seconds, seed=7)
+        cpu = {"value": cflops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{desc} ({dt:.1f} s)", "cpu": _cpu_model()}
+
+    if rank == 0:
+        line = {
+            "metric": "attn-core fwd+recompute-bwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": elapsed_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": _config(w, {"philox_seed": seed, "l2": f"{n_sets} rotating input sets of "
+                                  f"{per_set / 2**20:.0f} MiB (> L2)", "parallelism":
+                                  f"replicas x{world}" if world > 1 else "single GPU"}),
+            "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
+            "fwd_tflops": fl["fwd"] / (fwd_ms / 1e3) / 1e12,
+            "bwd_tflops": fl["bwd"] / (bwd_ms / 1e3) / 1e12,
+            "model_flops_tflops": fl["model"] * K * world / (elapsed_ms / 1e3) / 1e12,
+            "kernel_ms": {n: round(v, 4) for n, v in kavg.items()},
+            "wall_ms_per_step": wall / K * 1e3,
+            "roofline": {"bound": "tensor", "kernel": kname, "achieved": achieved,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / pk["bf16_tflops"],
+                         "peak_source": pk["source"] + " (burst)",
+                         "traffic": _traffic(kname, w["name"])},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e(args, w, pr, base, dev, stream, ws_bytes, fl, world, dist):
+    """Same metric through the public API with host buffers: each step copies
+    Q, K, V, dO from pinned host memory, runs fwd + bwd, and reads O, LSE, dQ,
+    dK, dV back into pinned host memory."""
+    import torch
+
+    import attention_core_gb300 as ac
+    hq_in = {n: getattr(base, n).pin_memory() for n in ("q", "k", "v", "dout")}
+    dv_in = {n: torch.empty_like(x, device=dev) for n, x in hq_in.items()}
+    outs = {"o": torch.empty_like(dv_in["q"]), "dq": torch.empty_like(dv_in["q"]),
+            "dk": torch.empty_like(dv_in["k"]), "dv": torch.empty_like(dv_in["v"]),
+            "lse": torch.empty((w["b"], w["h_q"], w["s"]), dtype=torch.float32, device=dev)}
+    host_out = {n: torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for n, x in outs.items()}
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    h2d = sum(x.numel() * x.element_size() for x in hq_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in outs.values())
+    pr.timing_events = 0
+    sh = stream.cuda_stream
+
+    def step():
+        for n in hq_in:
+            dv_in[n].copy_(hq_in[n], non_blocking=True)
+        rc = ac.attn_core_fwd(pr, dv_in["q"].data_ptr(), dv_in["k"].data_ptr(), dv_in["v"].data_ptr(),
+                              outs["o"].data_ptr(), outs["lse"].data_ptr(), sh)
+        if rc:
+            raise ac.AttnCoreError(rc, "attn_core_fwd")
+        rc = ac.attn_core_bwd_recompute(
+            pr, dv_in["q"].data_ptr(), dv_in["k"].data_ptr(), dv_in["v"].data_ptr(),
+            outs["o"].data_ptr(), outs["lse"].data_ptr(), dv_in["dout"].data_ptr(),
+            outs["dq"].data_ptr(), outs["dk"].data_ptr(), outs["dv"].data_ptr(), ws.data_ptr(),
+            ws_bytes, sh)
+        if rc:
+            raise ac.AttnCoreError(rc, "attn_core_bwd_recompute")
+        for n in outs:
+            host_out[n].copy_(outs[n], non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        step()
+    torch.cuda.synchronize(dev)
+    k2 = max(5, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(k2):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": fl["total"] * k2 * world / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k2,
+            "ms_per_step": ms / k2}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt175b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="time budget of the CPU-oracle baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = _workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -43,7 +43,8 @@ class _Params(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
                 ("s", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("p_drop", ctypes.c_float), ("scale", ctypes.c_float),
-                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+                ("stored_o_bf16", ctypes.c_int32)]
 
 
 class _Bytes(ctypes.Structure):
@@ -97,11 +98,15 @@ class Problem:
     scale: float = 0.0      # <= 0: 1/sqrt(d) rounded to fp32
     seed: int = 0
     offset: int = 0
+    # Backward row statistic sum_j P_ij dP_ij taken as dO_i . bf16(O_i), the
+    # way a method that stores only the bf16 output must form it.  False: the
+    # exact definition.
+    stored_o_bf16: bool = False
 
     def _c(self) -> _Params:
         return _Params(self.b, self.h_q, self.h_kv, self.s, self.d, int(bool(self.causal)),
                        float(self.p_drop), float(self.scale), int(self.seed) & (2**64 - 1),
-                       int(self.offset) & (2**64 - 1))
+                       int(self.offset) & (2**64 - 1), int(bool(self.stored_o_bf16)))
 
 
 def _f64(x) -> np.ndarray:

@@ -24,10 +24,18 @@
  * caller widens bf16 exactly).  Work is split over rows or heads with OpenMP;
  * there is no blocking, fusion or reordering beyond that.
  *
+ * Stored-output model (flag stored_o_bf16): the method keeps only the bf16
+ * output O from the forward pass, so its backward must form the softmax row
+ * statistic sum_j P_ij dP_ij as dO_i . O_i from that stored O.  With the flag
+ * set the oracle does the same with its own O rounded to bf16; without it the
+ * exact row sum is used.  The two differ by (D_exact - D_stored) P_ij in every
+ * dS_ij, an error set by bf16 storage, not by the kernels.
+ *
  * Parity status: every function here is pinned by a CPU test (known-answer
  * vectors for Philox, textbook attention for p = 0, finite differences for
- * the gradients, the worked example for the byte counts).  No function is
- * "parity unpinned".
+ * the gradients, the worked example for the byte counts, and the exact
+ * first-order relation between the stored-output model and the exact
+ * backward).  No function is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -41,6 +49,7 @@ typedef struct {
     float scale;        /* score scale; <= 0 means 1/sqrt(d) in fp32 */
     uint64_t seed;      /* Philox key */
     uint64_t offset;    /* Philox stream offset, < 2^32 */
+    int32_t stored_o_bf16; /* backward row statistic from the bf16-stored output (see below) */
 } oracle_params;
 
 /* ------------------------------------------------------------------------
@@ -136,6 +145,19 @@ static int64_t kv_head_of(const oracle_params* p, int64_t bh)
     int64_t bi = bh / p->h_q, hq = bh % p->h_q;
     int64_t group = p->h_q / p->h_kv;
     return bi * p->h_kv + hq / group;
+}
+
+/* Round to the nearest bf16 value, ties to even (via fp32, which is exact for
+ * every bf16 value; the double-to-float step rounds to nearest). */
+static double round_bf16(double x)
+{
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u) return (double)f;   /* inf / nan */
+    u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
+    memcpy(&f, &u, 4);
+    return (double)f;
 }
 
 /* One query row of the core: scores S_ij = scale * q_i . k_j for visible j
@@ -266,6 +288,17 @@ static void core_row_grad(const oracle_params* p, const double* v, const double*
             rowdot += P[j] * dS[j];
         } else {
             dS[j] = 0.0;
+        }
+    }
+    if (p->stored_o_bf16) {
+        /* The method keeps only its output O (bf16) from the forward pass and
+         * takes the row statistic from it: sum_j P_ij dP_ij = dO_i . O_i, with
+         * O_i here the oracle's own output row rounded to bf16. */
+        rowdot = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            double oc = 0.0;
+            for (int64_t j = 0; j < nk; ++j) oc += P[j] * Z[j] * vh[j * d + c];
+            rowdot += gi[c] * round_bf16(oc);
         }
     }
     for (int64_t j = 0; j < nk; ++j) dS[j] = P[j] * (dS[j] - rowdot);

@@ -313,3 +313,47 @@ def test_fwd_mask_probe_reads_out_mask():
             width = min(d, s - w0)
             got = (o[0, bh, :, :width] != 0).astype(np.uint8)
             assert (got == m[:, w0:w0 + width]).all()
+
+
+# ------------------------------------------------------ stored-output model
+
+def test_stored_output_model_relation():
+    """With the row statistic taken from the bf16-stored output, dS changes by
+    exactly -P_ij (D_stored_i - D_exact_i); so dQ moves by -scale dD_i (P K)_i,
+    dK by -scale sum_i P_ij dD_i q_i, and dV not at all.  Checked against
+    pieces formed independently: the oracle's own O rounded to bf16 by torch,
+    its dense P, and plain matrix products."""
+    b, hq, hkv, s, d = 1, 2, 1, 24, 16
+    base = dict(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=True, p_drop=0.25, seed=31)
+    t = random_inputs(b, hq, hkv, s, d, seed=12)
+    ex = oracle.Problem(**base)
+    st = oracle.Problem(**base, stored_o_bf16=True)
+    o, _ = oracle.fwd(ex, t.q, t.k, t.v)
+    dq0, dk0, dv0 = oracle.bwd(ex, t.q, t.k, t.v, t.dout)
+    dq1, dk1, dv1 = oracle.bwd(st, t.q, t.k, t.v, t.dout)
+    g = t.dout.double().numpy()
+    o16 = torch.from_numpy(o).to(torch.bfloat16).double().numpy()
+    dD = (g * o16).sum(-1) - (g * o).sum(-1)                    # [b, h, s]
+    scale = oracle.resolved_scale(ex)
+    q = t.q.double().numpy()
+    k = t.k.double().numpy()
+    assert np.array_equal(dv0, dv1)
+    exp_dk = np.zeros_like(dk0)
+    for h in range(hq):
+        _, P, _ = oracle.head_matrices(ex, t.q, t.k, h)
+        pk = P @ k[0, h // (hq // hkv)]
+        assert np.max(np.abs((dq1 - dq0)[0, h] + scale * dD[0, h][:, None] * pk)) < 1e-12
+        exp_dk[0, h // (hq // hkv)] -= scale * P.T @ (dD[0, h][:, None] * q[0, h])
+    assert np.max(np.abs((dk1 - dk0) - exp_dk)) < 1e-12
+    # and the perturbation is at the bf16 storage level, not larger
+    assert np.max(np.abs(dD)) <= 2.0 ** -8 * np.max(np.abs(g * o).sum(-1)) + 1e-12
+
+
+def test_stored_output_model_is_exact_when_output_is_bf16():
+    """s = 1 with p = 0: O = V exactly (bf16), so the model equals the exact backward."""
+    base = dict(b=1, h_q=2, h_kv=2, s=1, d=16, causal=True)
+    t = random_inputs(1, 2, 2, 1, 16, seed=13)
+    a = oracle.bwd(oracle.Problem(**base), t.q, t.k, t.v, t.dout)
+    c = oracle.bwd(oracle.Problem(**base, stored_o_bf16=True), t.q, t.k, t.v, t.dout)
+    for x, y in zip(a, c):
+        assert np.max(np.abs(x - y)) < 1e-15
