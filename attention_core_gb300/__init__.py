@@ -21,6 +21,7 @@ from dataclasses import dataclass
 __all__ = [
     "AttnCoreError", "Params", "load_library", "attn_core_fwd", "attn_core_bwd_recompute",
     "attn_core_bwd_workspace_bytes", "attn_core_stored_bytes", "attn_core_strerror",
+    "attn_core_bwd_recompute_noalloc",
     "fwd", "bwd_recompute", "stored_bytes", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED",
     "ERR_MISALIGNED", "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "FLAG_TEST_WAIT_TIMEOUT", "SUPPORTED_HEAD_DIMS",
@@ -107,6 +108,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_core_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_core_bwd_recompute.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.attn_core_bwd_recompute.restype = ctypes.c_int
+    lib.attn_core_bwd_recompute_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.attn_core_bwd_recompute_noalloc.restype = ctypes.c_int
     lib.attn_core_stored_bytes.argtypes = [P, ctypes.POINTER(_CBytes)]
     lib.attn_core_stored_bytes.restype = ctypes.c_int
     lib.attn_core_strerror.argtypes = [ctypes.c_int]
@@ -138,6 +141,16 @@ def attn_core_bwd_recompute(p: Params, q: int, k: int, v: int, o: int, lse: int,
     cp = p.to_c()
     return load_library().attn_core_bwd_recompute(ctypes.byref(cp), q, k, v, o, lse, dout, dq, dk,
                                                   dv, workspace, workspace_bytes, stream or None)
+
+
+def attn_core_bwd_recompute_noalloc(p: Params, q: int, k: int, v: int, o: int, lse: int, dout: int,
+                                    dq: int, dk: int, dv: int, stream: int) -> int:
+    """Backward for callers that cannot allocate device memory: no workspace
+    argument; the library's own fixed scratch array is used (see the header
+    for its size limit and for why calls that overlap on the GPU race)."""
+    cp = p.to_c()
+    return load_library().attn_core_bwd_recompute_noalloc(ctypes.byref(cp), q, k, v, o, lse, dout, dq,
+                                                          dk, dv, stream or None)
 
 
 def attn_core_stored_bytes(p: Params) -> tuple[int, dict]:

@@ -235,4 +235,34 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     return record(p->timing_events, 5, st);
 }
 
+// ---------------------------------------------------------------------------
+// Backward for callers that cannot allocate device memory.  Its workspace is a
+// fixed array of this library's own, 2 * kNoAllocMaxRows fp32 values (8 MiB),
+// which every GPU that loads the library holds until the process exits.  The
+// array's name is only a host-side stand-in in host code; the device address
+// is looked up once per device with cudaGetSymbolAddress and then reused.
+static constexpr size_t kNoAllocMaxRows = (size_t)1 << 20;
+static __device__ __align__(256) float g_noalloc_scratch[2 * kNoAllocMaxRows];
+static void* g_noalloc_addr[128];
+
+int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, const void* k, const void* v,
+                                    const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                    void* dv, void* stream)
+{
+    int rc = check_params(p);
+    if (rc) return rc;
+    if (padded_rows(p) > kNoAllocMaxRows) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_CORE_ERR_CUDA;
+    if (dev < 0 || dev >= 128) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+            return ATTN_CORE_ERR_CUDA;
+        g_noalloc_addr[dev] = addr;
+    }
+    return attn_core_bwd_recompute(p, q, k, v, o, lse, dout, dq, dk, dv, g_noalloc_addr[dev],
+                                   sizeof(float) * 2 * kNoAllocMaxRows, stream);
+}
+
 }  // extern "C"

@@ -124,6 +124,30 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
                             const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Backward with recomputation for callers that cannot allocate device
+ * memory.  Some callers have no allocator to call: code running inside
+ * another framework that owns every byte of device memory through its own
+ * pool, code invoked from a library that forbids allocation in its callbacks,
+ * or services whose memory is planned once at start-up.  They cannot provide
+ * the workspace attn_core_bwd_recompute asks for, so this variant uses a
+ * fixed scratch array inside the library instead and allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).  The paper
+ * has no counterpart to this entry point.
+ *
+ * Same arguments and results as attn_core_bwd_recompute without the
+ * workspace.  Limit: b * h_q * ceil(s / 128) * 128 <= 1048576 padded query
+ * rows (the array holds 8 MiB on every GPU that loads the library, until the
+ * process exits); larger shapes return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL
+ * without launching anything.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls on a device
+ * share the one array and it keeps the last call's contents (nothing in it
+ * needs to start at zero), so calls whose kernels overlap on the GPU --
+ * concurrent streams, or several host threads -- race on it: order them. */
+int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, const void* k, const void* v,
+                                    const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                    void* dv, void* stream);
+
 /* Activation-byte accounting (pure host, integer, exact).  Worked example of
  * the activation-checkpointing page: Llama 3 70B, s = 8192, b = 1, h_q = 64,
  * d = 128, 80 layers -> 1.9 TB none, 182.5 GB selective, 10.7 GB full. */
