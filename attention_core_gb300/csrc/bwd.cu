@@ -157,8 +157,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         mbar_init(bar(bars->s_full), 1);
         mbar_init(bar(bars->dp_full), 1);
-        mbar_init(bar(bars->p_full), 128);
-        mbar_init(bar(bars->ds_full), 128);
+        mbar_init(bar(bars->p_full), kRowThreads);
+        mbar_init(bar(bars->ds_full), kRowThreads);
         mbar_init(bar(bars->acc_done), 1);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
@@ -246,8 +246,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, G::template desc_mn<BQ>(dobase, kk), IDG,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::T_DV, tmem + C::T_S + split_a_col(kk, BQ), G::template desc_mn<BQ>(dobase, kk),
+                           IDG, (it > 0 || kk > 0) ? 1u : 0u);
                 if (it + 1 < n_it) {
                     const int st1 = (it + 1) % ST;
                     ok = wait_bounded(wc, bar(bars->q_full[st1]), ((it + 1) / ST) & 1, timeout_code(kSiteQFull));
@@ -260,17 +260,19 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::T_DK, tmem + C::T_DP + kk * 8, G::template desc_mn<BQ>(qbase, kk), IDG,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::T_DK, tmem + C::T_DP + split_a_col(kk, BQ), G::template desc_mn<BQ>(qbase, kk),
+                           IDG, (it > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(bars->q_empty[st]));
                 if (it + 1 < n_it) issue_dp(it + 1);
             }
             if (ok) mma_commit(bar(bars->acc_done));
         }
     } else if (alive && warp >= 4) {
-        // ---- row threads: one key per thread (= TMEM lane)
-        const int r = (int)threadIdx.x - 128;
-        const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+        // ---- row threads: key = TMEM lane, half = which BQ/2 queries of a tile
+        constexpr int HQ = BQ / 2;
+        const RowThread rt = row_thread();
+        const int h = rt.half, r = rt.row;
+        const uint32_t lane_off = rt.lane_off;
         const int key = kb * 128 + r;
         const uint32_t warp_key0 = (uint32_t)(kb * 128 + (int)(warp & 3u) * 32);
         const float* lse2_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
@@ -279,50 +281,54 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int it = 0; it < n_it; ++it) {
             const int st = it % ST;
             const int bh = bh0 + it / per_head;
-            const int q0 = (qt0 + it % per_head) * BQ;
+            const int q0 = (qt0 + it % per_head) * BQ + HQ * h;     // this half's first query
             ok = __all_sync(0xffffffffu,
                             wait_bounded(wc, bar(bars->q_full[st]), (it / ST) & 1, timeout_code(kSiteQFull)));
             if (ok)
                 ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), it & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
-            const float* l2 = lse2_s + st * BQ;
-            const float* dl = del_s + st * BQ;
-            float p[BQ];
+            const float* l2 = lse2_s + st * BQ + HQ * h;
+            const float* dl = del_s + st * BQ + HQ * h;
+            float p[HQ];
 #pragma unroll
-            for (int c32 = 0; c32 < BQ / 32; ++c32) {
+            for (int c32 = 0; c32 < HQ / 32; ++c32) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + C::T_S + lane_off + c32 * 32, rr);
+                tmem_ld32(tmem + C::T_S + lane_off + HQ * h + c32 * 32, rr);
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     p[c32 * 32 + e] = ex2_approx(fmaf(__uint_as_float(rr[e]), a.scale_log2, -l2[c32 * 32 + e]));
             }
             if (a.causal && q0 < kb * 128 + 128) {
 #pragma unroll
-                for (int c = 0; c < BQ; ++c)
+                for (int c = 0; c < HQ; ++c)
                     if (q0 + c < key) p[c] = 0.f;
             }
-            uint32_t kw[BQ / 32];
+            uint32_t kw[HQ / 32];
             if (DROP) {
                 const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
 #pragma unroll
-                for (int v = 0; v < BQ / 32; ++v) kw[v] = keep_word_col(pk, warp_key0, (uint32_t)(q0 + 32 * v));
+                for (int v = 0; v < HQ / 32; ++v) kw[v] = keep_word_col(pk, warp_key0, (uint32_t)(q0 + 32 * v));
             } else {
 #pragma unroll
-                for (int v = 0; v < BQ / 32; ++v) kw[v] = 0xffffffffu;
+                for (int v = 0; v < HQ / 32; ++v) kw[v] = 0xffffffffu;
             }
-            // P_d^T (without the 1/(1-p) factor, applied to dV at the end) -> TMEM over S^T
+            // P_d^T (without the 1/(1-p) factor, applied to dV at the end) -> TMEM
+            // over the first HQ/2 of this half's S^T columns
+            {
+                uint32_t pw[HQ / 2];
 #pragma unroll
-            for (int h = 0; h < BQ / 64; ++h) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c = h * 64 + 2 * e;
+                for (int e = 0; e < HQ / 2; ++e) {
+                    const int c = 2 * e;
                     const float p0 = ((kw[c >> 5] >> (c & 31)) & 1u) ? p[c] : 0.f;
                     const float p1 = ((kw[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? p[c + 1] : 0.f;
                     pw[e] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(tmem + C::T_S + lane_off + h * 32, pw);
+                if constexpr (HQ / 2 == 32) {
+                    tmem_st32(tmem + C::T_S + lane_off + HQ * h, pw);
+                } else {
+                    tmem_st16(tmem + C::T_S + lane_off + HQ * h, pw);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -332,9 +338,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c32 = 0; c32 < BQ / 32; ++c32) {
+            for (int c32 = 0; c32 < HQ / 32; ++c32) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + C::T_DP + lane_off + c32 * 32, rr);
+                tmem_ld32(tmem + C::T_DP + lane_off + HQ * h + c32 * 32, rr);
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -348,7 +354,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     }
                     w[e] = pack_bf16x2(ds[0], ds[1]);
                 }
-                tmem_st16(tmem + C::T_DP + lane_off + c32 * 16, w);
+                tmem_st16(tmem + C::T_DP + lane_off + HQ * h + c32 * 16, w);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -358,7 +364,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (ok) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c32 = 0; c32 < D / 32; ++c32) {
+            for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
                 stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, a.keep_scale);
@@ -367,8 +373,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (r == 0 && !bars->abort_flag) {
+        named_barrier_sync(1, kRowThreads);
+        if (h == 0 && r == 0 && !bars->abort_flag) {
             for (int ch = 0; ch < G::NCH; ++ch) {
                 tma_store_3d(&tm_dv, sb + C::OFF_V + ch * C::KV_CHUNK, ch * G::CW, kb * 128, bkv);
                 tma_store_3d(&tm_dk, sb + C::OFF_K + ch * C::KV_CHUNK, ch * G::CW, kb * 128, bkv);
@@ -416,7 +422,8 @@ struct DqCfg {
     static constexpr uint32_t OFF_K = 2 * QT;
     static constexpr uint32_t OFF_V = OFF_K + KST * KT;
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KT;
-    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t OFF_RED = OFF_BAR + 256;      // [2 halves][128] partial row statistics
+    static constexpr uint32_t SMEM = OFF_RED + 2 * 128 * 4 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM: S | dP (later dS~ in its first half, P in its second) | dQ~ | PK
     static constexpr uint32_t T_S = 0, T_DP = BN, T_DQ = 2 * BN, T_PK = 2 * BN + D;
@@ -471,9 +478,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(bar(bars->v_empty[st]), 1);
         }
         mbar_init(bar(bars->s_full), 1);
-        mbar_init(bar(bars->s_read), 128);
+        mbar_init(bar(bars->s_read), kRowThreads);
         mbar_init(bar(bars->dp_full), 1);
-        mbar_init(bar(bars->ds_full), 128);
+        mbar_init(bar(bars->ds_full), kRowThreads);
         mbar_init(bar(bars->acc_done), 1);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
@@ -577,8 +584,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bdesc = G::template desc_mn<BN>(kbase, kk);
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tmem + C::T_DQ, tmem + C::T_DP + kk * 8, bdesc, IDQ, acc);
-                    mma_ts(tmem + C::T_PK, tmem + C::T_DP + BN / 2 + kk * 8, bdesc, IDQ, acc);
+                    const uint32_t acol = tmem + C::T_DP + split_a_col(kk, BN);
+                    mma_ts(tmem + C::T_DQ, acol, bdesc, IDQ, acc);
+                    mma_ts(tmem + C::T_PK, acol + BN / 4, bdesc, IDQ, acc);
                 }
                 mma_commit(bar(bars->k_empty[st]));
                 if (j + 1 < nk) ok = issue_dp(j + 1);
@@ -586,58 +594,61 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (ok) mma_commit(bar(bars->acc_done));
         }
     } else if (alive && warp >= 4) {
-        // ---- row threads: one query row per thread (= TMEM lane)
-        const int r = (int)threadIdx.x - 128;
-        const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+        // ---- row threads: query row = TMEM lane, half = which BN/2 keys of a block
+        constexpr int HK = BN / 2;
+        const RowThread rt = row_thread();
+        const int h = rt.half, r = rt.row;
+        const uint32_t lane_off = rt.lane_off;
         const int i = qb * 128 + r;
         const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
         const float lse2 = args.lse2_ws[srow];
         const float d_tilde = args.delta_ws[srow];
         const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+        float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
         float d_exact = 0.f;
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
-            float p[BN];
+            float p[HK];
 #pragma unroll
-            for (int c32 = 0; c32 < BN / 32; ++c32) {
+            for (int c32 = 0; c32 < HK / 32; ++c32) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + C::T_S + lane_off + c32 * 32, rr);
+                tmem_ld32(tmem + C::T_S + lane_off + HK * h + c32 * 32, rr);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) p[c32 * 32 + e] = __uint_as_float(rr[e]);
             }
             tc_fence_before();
             mbar_arrive(bar(bars->s_read));
-            const int key0 = j * BN;
+            const int key0 = j * BN + HK * h;
 #pragma unroll
-            for (int c = 0; c < BN; ++c) p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
-            if (a.causal && key0 + BN > qb * 128) {
+            for (int c = 0; c < HK; ++c) p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
+            if (a.causal && key0 + HK > qb * 128) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
+                for (int c = 0; c < HK; ++c)
                     if (key0 + c > i) p[c] = 0.f;
             }
-            if (!a.causal && key0 + BN > a.s) {
+            if (!a.causal && key0 + HK > a.s) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
+                for (int c = 0; c < HK; ++c)
                     if (key0 + c >= a.s) p[c] = 0.f;
             }
-            uint32_t kw[BN / 32];
+            uint32_t kw[HK / 32];
             if (DROP) {
 #pragma unroll
-                for (int v = 0; v < BN / 32; ++v) kw[v] = keep_word_row(pk, (uint32_t)(key0 >> 5) + v, (uint32_t)i);
+                for (int v = 0; v < HK / 32; ++v) kw[v] = keep_word_row(pk, (uint32_t)(key0 >> 5) + v, (uint32_t)i);
             } else {
 #pragma unroll
-                for (int v = 0; v < BN / 32; ++v) kw[v] = 0xffffffffu;
+                for (int v = 0; v < HK / 32; ++v) kw[v] = 0xffffffffu;
             }
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c32 = 0; c32 < BN / 32; ++c32) {
+            for (int c32 = 0; c32 < HK / 32; ++c32) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + C::T_DP + lane_off + c32 * 32, rr);
+                tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -652,26 +663,33 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                     w[e] = pack_bf16x2(ds[0], ds[1]);
                 }
-                tmem_st16(tmem + C::T_DP + lane_off + c32 * 16, w);
+                tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
             }
-            // P (before dropout) into the second half of the dP columns, all read by now
+            // P (before dropout) after the dS~ words, inside this half's dP columns (all read by now)
+            {
+                uint32_t pw[HK / 2];
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(p[h * 64 + 2 * e], p[h * 64 + 2 * e + 1]);
-                tmem_st32(tmem + C::T_DP + BN / 2 + lane_off + h * 32, pw);
+                for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+                if constexpr (HK / 2 == 32) {
+                    tmem_st32(tmem + C::T_DP + lane_off + HK * h + HK / 2, pw);
+                } else {
+                    tmem_st16(tmem + C::T_DP + lane_off + HK * h + HK / 2, pw);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->ds_full));
         }
+        // exact row statistic: the two halves' partial sums
+        dred[h * 128 + r] = d_exact;
+        named_barrier_sync(1, kRowThreads);
+        d_exact += dred[(h ^ 1) * 128 + r];
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
         if (ok) {
             tc_fence_after();
             const float eps = d_exact - d_tilde;
 #pragma unroll 1
-            for (int c32 = 0; c32 < D / 32; ++c32) {
+            for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rq[32], rp[32];
                 tmem_ld32(tmem + C::T_DQ + lane_off + c32 * 32, rq);
                 tmem_ld32(tmem + C::T_PK + lane_off + c32 * 32, rp);
@@ -680,11 +698,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     rq[e] = __float_as_uint(fmaf(-eps, __uint_as_float(rp[e]), __uint_as_float(rq[e])));
                 stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rq, a.scale);
             }
-            args.delta_ws[srow] = d_exact;
+            if (h == 0) args.delta_ws[srow] = d_exact;
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (r == 0 && !bars->abort_flag) {
+        named_barrier_sync(1, kRowThreads);
+        if (h == 0 && r == 0 && !bars->abort_flag) {
             for (int ch = 0; ch < G::NCH; ++ch)
                 tma_store_3d(&tm_dq, sb + C::OFF_Q + ch * C::QCH, ch * G::CW, qb * 128, bh);
             bulk_commit();

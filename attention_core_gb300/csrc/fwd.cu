@@ -10,14 +10,16 @@
 // Recomputation in Large Transformer Models", Key takeaways, fourth bullet;
 // "Recomputing Activations", "Memory for compute, selectively").
 //
-// Structure of a CTA (256 threads):
+// Structure of a CTA (384 threads):
 //   warp 0  TMA: Q once, then K blocks into a ring of stages
 //   warp 2  TMA: V blocks into their own ring
 //   warp 1  one thread issues tcgen05 MMAs: S_j = Q K_j^T into one of two
 //           TMEM score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM
-//   warps 4-7  one query row per thread (= TMEM lane): online softmax in the
-//           log2 domain, dropout from Philox, P_d written back to TMEM as bf16
-//           over the scores it replaces; epilogue O / l -> bf16 -> TMA store.
+//   warps 4-11  two warpgroups on the same 128 query rows (TMEM lanes), one
+//           per half of the 128 keys of a block: online softmax in the log2
+//           domain (the halves swap their row maxima through shared memory),
+//           dropout from Philox, P_d written back to TMEM as bf16 inside the
+//           half's own score columns; epilogue O / l -> bf16 -> TMA store.
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks skip the rescale; O / l is exact either way.
 #include "kernels.h"
@@ -39,7 +41,9 @@ struct FwdCfg {
     static constexpr uint32_t OFF_K = TILE;
     static constexpr uint32_t OFF_V = TILE * (1 + ST);
     static constexpr uint32_t OFF_BAR = TILE * (1 + 2 * ST);
-    static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t OFF_RED = OFF_BAR + 256;          // [2 buffers][2 halves][128] row maxima
+    static constexpr uint32_t OFF_LRED = OFF_RED + 2 * 2 * 128 * 4;  // [2 halves][128] row sums
+    static constexpr uint32_t SMEM = OFF_LRED + 2 * 128 * 4 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM columns: two score buffers, then the O accumulator.
     static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256;
@@ -51,6 +55,7 @@ struct FwdBars {
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t s_full[2], p_full[2];
     uint64_t o_done;
+    uint64_t xmax[2];      // row-max exchange between the two column halves
     uint64_t never;
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -59,7 +64,7 @@ struct FwdBars {
 // Wait sites reported in bits 8.. of the status word on a timeout.
 enum : int32_t {
     kSiteInject = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull,
-    kSiteSFull, kSiteODone
+    kSiteSFull, kSiteODone, kSiteXmax
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
@@ -101,7 +106,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(bars->s_full[b]), 1);
-            mbar_init(bar(bars->p_full[b]), 128);
+            mbar_init(bar(bars->p_full[b]), kRowThreads);
+            mbar_init(bar(bars->xmax[b]), kRowThreads);
         }
         mbar_init(bar(bars->o_done), 1);
         mbar_init(bar(bars->never), 1);
@@ -173,7 +179,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t tP = tmem + ((i & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + C::T_O, tP + kk * 8, G::template desc_mn<128>(vbase, kk), IDO,
+                    mma_ts(tmem + C::T_O, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk), IDO,
                            (i > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(bars->v_empty[st]));
                 mma_commit(bar(bars->o_done));
@@ -197,41 +203,50 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (ok) issue_pv(nk - 1);
         }
     } else if (alive && warp >= 4) {
-        // ---- softmax / epilogue: one query row per thread
-        const int r = (int)threadIdx.x - 128;
-        const uint32_t lane_off = ((warp & 3u) * 32u) << 16;
+        // ---- softmax / epilogue: row = TMEM lane, half = which 64 keys of a block
+        const RowThread rt = row_thread();
+        const int h = rt.half, r = rt.row;
+        const uint32_t lane_off = rt.lane_off;
         const int i = qb * 128 + r;
-        const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+        const uint32_t t16 = a.thr << 16;
+        float* xmax = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
+        float* lred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_LRED);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
-            const uint32_t tS = tmem + ((j & 1) ? C::T_S1 : C::T_S0) + lane_off;
+            const uint32_t tS = tmem + ((j & 1) ? C::T_S1 : C::T_S0) + lane_off + 64 * h;
             ok = __all_sync(0xffffffffu,
                             wait_bounded(wc, bar(bars->s_full[j & 1]), (j >> 1) & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
-            float x[128];
+            float x[64];
 #pragma unroll
-            for (int c32 = 0; c32 < 4; ++c32) {
+            for (int c32 = 0; c32 < 2; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tS + c32 * 32, rr);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[c32 * 32 + e] = __uint_as_float(rr[e]);
             }
-            const int key0 = j * 128;
+            const int key0 = j * 128 + 64 * h;
             if (a.causal && j == qb) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > r) x[c] = -INFINITY;
+                for (int c = 0; c < 64; ++c)
+                    if (64 * h + c > r) x[c] = -INFINITY;
             }
-            if (!a.causal && key0 + 128 > a.s) {
+            if (!a.causal && key0 + 64 > a.s) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
+                for (int c = 0; c < 64; ++c)
                     if (key0 + c >= a.s) x[c] = -INFINITY;
             }
             float mx = x[0];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            for (int c = 1; c < 64; ++c) mx = fmaxf(mx, x[c]);
+            // swap block maxima with the other half of the row
+            xmax[((j & 1) * 2 + h) * 128 + r] = mx;
+            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xmax[j & 1]), (j >> 1) & 1,
+                                                     timeout_code(kSiteXmax)));
+            if (!ok) break;
+            mx = fmaxf(mx, xmax[((j & 1) * 2 + (h ^ 1)) * 128 + r]);
             const float m_new = fmaxf(m_run, mx * a.scale_log2);
             if (__any_sync(0xffffffffu, m_new > m_run + 8.0f)) {
                 if (j > 0) {
@@ -242,7 +257,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const float f = ex2_approx(m_run - m_new);
                     l_run *= f;
 #pragma unroll 1
-                    for (int c32 = 0; c32 < D / 32; ++c32) {
+                    for (int c32 = h; c32 < D / 32; c32 += 2) {
                         uint32_t rr[32];
                         tmem_ld32(tmem + C::T_O + lane_off + c32 * 32, rr);
 #pragma unroll
@@ -256,49 +271,53 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float neg_m = -m_run;
             float lsum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float p = ex2_approx(fmaf(x[c], a.scale_log2, neg_m));
-                lsum += p;
-                x[c] = p;
+            for (int c = 0; c < 64; ++c) {
+                const float pv = ex2_approx(fmaf(x[c], a.scale_log2, neg_m));
+                lsum += pv;
+                x[c] = pv;
             }
             l_run += lsum;
+            uint32_t pw[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
             if (DROP) {
+                // group g covers keys key0 + 8g .. +7: words 4g .. 4g+3 of pw
 #pragma unroll
-                for (int b32 = 0; b32 < 4; ++b32) {
-                    const uint32_t m = keep_word_row(pk, (uint32_t)(key0 >> 5) + b32, (uint32_t)i);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (!((m >> e) & 1u)) x[b32 * 32 + e] = 0.f;
+                for (int g = 0; g < 8; ++g) {
+                    const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g, (uint32_t)i, (uint32_t)bh, a.offset,
+                                                   a.seed_lo, a.seed_hi);
+                    pw[4 * g + 0] &= keep_mask16x2(w4.x, t16);
+                    pw[4 * g + 1] &= keep_mask16x2(w4.y, t16);
+                    pw[4 * g + 2] &= keep_mask16x2(w4.z, t16);
+                    pw[4 * g + 3] &= keep_mask16x2(w4.w, t16);
                 }
             }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(x[h * 64 + 2 * e], x[h * 64 + 2 * e + 1]);
-                tmem_st32(tS + h * 32, pw);
-            }
+            tmem_st32(tS, pw);   // P_d of these 64 keys over the first 32 of the half's columns
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->p_full[j & 1]));
         }
+        // row sum over both halves (every row thread reaches this point once)
+        lred[h * 128 + r] = l_run;
+        named_barrier_sync(1, kRowThreads);
+        const float l_tot = l_run + lred[(h ^ 1) * 128 + r];
         if (ok)
             ok = __all_sync(0xffffffffu,
                             wait_bounded(wc, bar(bars->o_done), (nk - 1) & 1, timeout_code(kSiteODone)));
         if (ok) {
             tc_fence_after();
-            const float inv = a.keep_scale / l_run;
+            const float inv = a.keep_scale / l_tot;
 #pragma unroll 1
-            for (int c32 = 0; c32 < D / 32; ++c32) {
+            for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_O + lane_off + c32 * 32, rr);
                 stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rr, inv);
             }
-            if (i < a.s) args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_run)) * 0.693147180559945309f;
+            if (h == 0 && i < a.s) args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (r == 0 && !bars->abort_flag) {
+        named_barrier_sync(1, kRowThreads);
+        if (h == 0 && r == 0 && !bars->abort_flag) {
             for (int ch = 0; ch < G::NCH; ++ch)
                 tma_store_3d(&tm_o, sb + C::OFF_Q + ch * C::CHUNK, ch * G::CW, qb * 128, bh);
             bulk_commit();

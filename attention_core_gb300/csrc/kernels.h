@@ -9,9 +9,12 @@ namespace ac {
 // Query / key tile height of every kernel (TMEM has 128 lanes).
 constexpr int kBlockRows = 128;
 // Threads per CTA of the tensor-core kernels: warp 0 loads Q/K (or K/V),
-// warp 1 issues MMAs and owns TMEM, warp 2 loads V (or the per-row
-// statistics), warp 3 idles, warps 4..7 are the 128 row threads.
-constexpr int kThreads = 256;
+// warp 1 issues MMAs and owns TMEM, warp 2 loads V, warp 3 idles, and warps
+// 4..11 are the row threads: two warpgroups that share the 128 TMEM lanes
+// (one row per lane) and split every tile's columns in halves, so each SM
+// sub-partition runs two of them.
+constexpr int kThreads = 384;
+constexpr int kRowThreads = 256;
 
 struct CommonArgs {
     int32_t s;            // sequence length (queries == keys)

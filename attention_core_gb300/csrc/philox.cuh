@@ -28,18 +28,26 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
 {
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        const uint32_t hi_a = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo_a = 0xD2511F53u * c0;
-        const uint32_t hi_b = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t lo_b = 0xCD9E8D57u * c2;
-        c0 = hi_b ^ c1 ^ k0;
-        c1 = lo_b;
-        c2 = hi_a ^ c3 ^ k1;
-        c3 = lo_a;
+        const uint64_t pa = (uint64_t)0xD2511F53u * c0;   // one wide multiply: both halves
+        const uint64_t pb = (uint64_t)0xCD9E8D57u * c2;
+        c0 = (uint32_t)(pb >> 32) ^ c1 ^ k0;
+        c1 = (uint32_t)pb;
+        c2 = (uint32_t)(pa >> 32) ^ c3 ^ k1;
+        c3 = (uint32_t)pa;
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
     return make_uint4(c0, c1, c2, c3);
+}
+
+// Keep mask of the two keys a Philox output word decides (low half: the even
+// key, high half: the odd key), as 16-bit lane masks: 0xffff where the draw
+// is >= thr (kept), 0 where dropped.  t16 = thr << 16.  A high half is >= thr
+// exactly when the whole word is >= thr << 16; a low half when the word
+// shifted left by 16 is.
+__device__ __forceinline__ uint32_t keep_mask16x2(uint32_t w, uint32_t t16)
+{
+    return (w >= t16 ? 0xffff0000u : 0u) | ((w << 16) >= t16 ? 0x0000ffffu : 0u);
 }
 
 // Keep bits of the eight keys 8*group .. 8*group+7 of one query row:

@@ -87,6 +87,36 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx& w, uint32_t bar, uin
     }
 }
 
+// Row threads of a tile: warps 4..11; `half` selects the column half, `row`
+// is the TMEM lane (warp w reads lanes 32 * (w % 4) .. + 31).
+struct RowThread {
+    int half;
+    int row;
+    uint32_t lane_off;   // TMEM address offset of this warp's lanes
+};
+__device__ __forceinline__ RowThread row_thread()
+{
+    const uint32_t w = warp_id();
+    return RowThread{(int)((w - 4) >> 2), (int)(((w & 3u) << 5) | lane_id()), ((w & 3u) * 32u) << 16};
+}
+
+// TMEM column of the kk-th 16-element K slice of an A operand that two
+// column halves wrote as bf16 pairs, each half inside its own columns:
+// half 0 at [0, w), half 1 at [2w, 3w), with w = ncols / 4 words per half of
+// an ncols-wide fp32 tile.
+__device__ __forceinline__ uint32_t split_a_col(int kk, int ncols)
+{
+    return (uint32_t)(8 * kk + (kk >= ncols / 32 ? ncols / 4 : 0));
+}
+
+// Bounded barrier among the 256 row threads (an mbarrier completing once per
+// use); the caller tracks the phase parity.
+__device__ __forceinline__ bool row_barrier(const WaitCtx& w, uint32_t bar, uint32_t parity, int32_t code)
+{
+    mbar_arrive(bar);
+    return wait_bounded(w, bar, parity, code);
+}
+
 // --------------------------------------------------------------- TMA ---
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm)
 {

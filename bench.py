@@ -178,7 +178,7 @@ def _oracle_sample(w, budget_s: float, seed: int):
 
     n = 32
     dt, flops, desc = run(n)
-    while dt < budget_s / 2 and n < 64 * s * g:
+    while dt < budget_s / 2 and n < 512 * s * g:
         n = int(n * min(16.0, max(2.0, budget_s / max(dt, 1e-3))))
         dt, flops, desc = run(n)
     return dt, flops, len(os.sched_getaffinity(0)), desc
