@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn_core.so")
 SOURCES = ["api.cu", "fwd.cu", "bwd.cu"]
-HEADERS = ["ptx.cuh", "philox.cuh", "tile.cuh", "kernels.h"]
+HEADERS = ["ptx.cuh", "philox.cuh", "tile.cuh", "sched.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -44,6 +44,22 @@ int check_device()
     return g_dev_ok[dev] == 1 ? ATTN_CORE_OK : ATTN_CORE_ERR_UNSUPPORTED;
 }
 
+int g_dev_sms[128];
+
+int device_sms(int* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return ATTN_CORE_ERR_CUDA;
+    if (g_dev_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return ATTN_CORE_ERR_CUDA;
+        g_dev_sms[dev] = n;
+    }
+    *out = g_dev_sms[dev];
+    return ATTN_CORE_OK;
+}
+
 bool supported_d(int d) { return d == 64 || d == 96 || d == 128 || d == 160; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -184,6 +200,7 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
     ac::FwdArgs a{};
     a.c = common_args(p);
     a.lse = lse;
+    if ((rc = device_sms(&a.num_sms))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((rc = record(p->timing_events, 0, st))) return rc;
     if (ac::launch_fwd(p->d, a.c.thr != 0, tq, tk, tv, to, a, st) != 0) return ATTN_CORE_ERR_CUDA;

@@ -42,8 +42,9 @@ __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site
 
 // ======================================================= preprocess ======
 // One warp per padded query row: D~_i = sum_c dO_ic O_ic in fp32 and
-// LSE_i * log2(e); rows past s get 0 and +inf (their probabilities
-// recompute to exactly 0).
+// -LSE_i * log2(e), so that P = 2^(S * scale * log2(e) - LSE * log2(e)) is one
+// FMA and an exp2; rows past s get 0 and -inf (their probabilities recompute
+// to exactly 0).
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdArgs a)
 {
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdArgs a)
     if (i >= a.c.s) {
         if (lane == 0) {
             a.delta_ws[row] = 0.f;
-            a.lse2_ws[row] = INFINITY;
+            a.lse2_ws[row] = -INFINITY;
         }
         return;
     }
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdArgs a)
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
         a.delta_ws[row] = acc;
-        a.lse2_ws[row] = a.lse[bh * a.c.s + i] * 1.44269504088896340736f;
+        a.lse2_ws[row] = -a.lse[bh * a.c.s + i] * 1.44269504088896340736f;
     }
 }
 
@@ -288,42 +289,50 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), it & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
-            const float* l2 = lse2_s + st * BQ + HQ * h;
-            const float* dl = del_s + st * BQ + HQ * h;
-            float p[HQ];
+            const float2* nl2 = reinterpret_cast<const float2*>(lse2_s + st * BQ + HQ * h);
+            const float2* dl2 = reinterpret_cast<const float2*>(del_s + st * BQ + HQ * h);
+            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+            uint64_t pp[HQ / 2];
 #pragma unroll
             for (int c32 = 0; c32 < HQ / 32; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_S + lane_off + HQ * h + c32 * 32, rr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    p[c32 * 32 + e] = ex2_approx(fmaf(__uint_as_float(rr[e]), a.scale_log2, -l2[c32 * 32 + e]));
+                for (int e = 0; e < 16; ++e) {
+                    const float2 l = nl2[c32 * 16 + e];
+                    float lo, hi;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2,
+                                     f2_pack(l.x, l.y)), lo, hi);
+                    pp[c32 * 16 + e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
+                }
             }
             if (a.causal && q0 < kb * 128 + 128) {
 #pragma unroll
-                for (int c = 0; c < HQ; ++c)
-                    if (q0 + c < key) p[c] = 0.f;
+                for (int e = 0; e < HQ / 2; ++e) {
+                    float lo, hi;
+                    f2_unpack(pp[e], lo, hi);
+                    if (q0 + 2 * e < key) lo = 0.f;
+                    if (q0 + 2 * e + 1 < key) hi = 0.f;
+                    pp[e] = f2_pack(lo, hi);
+                }
             }
             uint32_t kw[HQ / 32];
             if (DROP) {
                 const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
 #pragma unroll
                 for (int v = 0; v < HQ / 32; ++v) kw[v] = keep_word_col(pk, warp_key0, (uint32_t)(q0 + 32 * v));
-            } else {
-#pragma unroll
-                for (int v = 0; v < HQ / 32; ++v) kw[v] = 0xffffffffu;
             }
-            // P_d^T (without the 1/(1-p) factor, applied to dV at the end) -> TMEM
-            // over the first HQ/2 of this half's S^T columns
+            // dropout factor pair for queries 2e, 2e+1: zs where kept, 0 where dropped
+            auto zpair = [&](int e) -> uint64_t {
+                const int c = 2 * e;
+                return f2_pack(((kw[c >> 5] >> (c & 31)) & 1u) ? a.keep_scale : 0.f,
+                               ((kw[c >> 5] >> ((c + 1) & 31)) & 1u) ? a.keep_scale : 0.f);
+            };
+            // P_d^T = P^T * Z -> TMEM over the first HQ/2 of this half's S^T columns
             {
                 uint32_t pw[HQ / 2];
 #pragma unroll
-                for (int e = 0; e < HQ / 2; ++e) {
-                    const int c = 2 * e;
-                    const float p0 = ((kw[c >> 5] >> (c & 31)) & 1u) ? p[c] : 0.f;
-                    const float p1 = ((kw[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? p[c + 1] : 0.f;
-                    pw[e] = pack_bf16x2(p0, p1);
-                }
+                for (int e = 0; e < HQ / 2; ++e) pw[e] = pack_bf16x2(DROP ? f2_mul(pp[e], zpair(e)) : pp[e]);
                 if constexpr (HQ / 2 == 32) {
                     tmem_st32(tmem + C::T_S + lane_off + HQ * h, pw);
                 } else {
@@ -344,15 +353,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    float ds[2];
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const int c = c32 * 32 + 2 * e + t;
-                        const float dpd = __uint_as_float(rr[2 * e + t]);
-                        const float dpv = ((kw[c32] >> (2 * e + t)) & 1u) ? dpd * a.keep_scale : 0.f;
-                        ds[t] = p[c] * (dpv - dl[c]);
-                    }
-                    w[e] = pack_bf16x2(ds[0], ds[1]);
+                    const int ep = c32 * 16 + e;
+                    uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                    if (DROP) dp = f2_mul(dp, zpair(ep));
+                    const float2 dl = dl2[ep];
+                    w[e] = pack_bf16x2(f2_mul(pp[ep], f2_sub(dp, f2_pack(dl.x, dl.y))));
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HQ * h + c32 * 16, w);
             }
@@ -367,7 +372,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
-                stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, a.keep_scale);
+                stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, 1.0f);
                 tmem_ld32(tmem + C::T_DK + lane_off + c32 * 32, rr);
                 stage_row32<D, 128>(sb + C::OFF_K, r, c32 * 32, rr, a.scale);
             }
@@ -601,46 +606,45 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t lane_off = rt.lane_off;
         const int i = qb * 128 + r;
         const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
-        const float lse2 = args.lse2_ws[srow];
+        const float nl2 = args.lse2_ws[srow];
         const float d_tilde = args.delta_ws[srow];
-        const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+        const uint32_t t16 = a.thr << 16;
         float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
-        float d_exact = 0.f;
+        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+        const uint64_t nl22 = f2_pack(nl2, nl2);
+        const uint64_t dt2 = f2_pack(d_tilde, d_tilde);
+        uint64_t dacc2 = f2_pack(0.f, 0.f);
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
-            float p[HK];
+            uint64_t pp[HK / 2];
 #pragma unroll
             for (int c32 = 0; c32 < HK / 32; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_S + lane_off + HK * h + c32 * 32, rr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) p[c32 * 32 + e] = __uint_as_float(rr[e]);
+                for (int e = 0; e < 16; ++e) pp[c32 * 16 + e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
             }
             tc_fence_before();
             mbar_arrive(bar(bars->s_read));
             const int key0 = j * BN + HK * h;
 #pragma unroll
-            for (int c = 0; c < HK; ++c) p[c] = ex2_approx(fmaf(p[c], a.scale_log2, -lse2));
-            if (a.causal && key0 + HK > qb * 128) {
-#pragma unroll
-                for (int c = 0; c < HK; ++c)
-                    if (key0 + c > i) p[c] = 0.f;
-            }
-            if (!a.causal && key0 + HK > a.s) {
-#pragma unroll
-                for (int c = 0; c < HK; ++c)
-                    if (key0 + c >= a.s) p[c] = 0.f;
-            }
-            uint32_t kw[HK / 32];
-            if (DROP) {
-#pragma unroll
-                for (int v = 0; v < HK / 32; ++v) kw[v] = keep_word_row(pk, (uint32_t)(key0 >> 5) + v, (uint32_t)i);
-            } else {
-#pragma unroll
-                for (int v = 0; v < HK / 32; ++v) kw[v] = 0xffffffffu;
+            for (int e = 0; e < HK / 2; ++e) {
+                float lo, hi;
+                f2_unpack(f2_fma(pp[e], sc2, nl22), lo, hi);
+                lo = ex2_approx(lo);
+                hi = ex2_approx(hi);
+                if (a.causal && key0 + HK > qb * 128) {
+                    if (key0 + 2 * e > i) lo = 0.f;
+                    if (key0 + 2 * e + 1 > i) hi = 0.f;
+                }
+                if (!a.causal && key0 + HK > a.s) {
+                    if (key0 + 2 * e >= a.s) lo = 0.f;
+                    if (key0 + 2 * e + 1 >= a.s) hi = 0.f;
+                }
+                pp[e] = f2_pack(lo, hi);
             }
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
@@ -651,17 +655,22 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
                 uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float ds[2];
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const int c = c32 * 32 + 2 * e + t;
-                        const float dpd = __uint_as_float(rr[2 * e + t]);
-                        const float dpv = ((kw[c32] >> (2 * e + t)) & 1u) ? dpd * a.keep_scale : 0.f;
-                        d_exact = fmaf(p[c], dpv, d_exact);
-                        ds[t] = p[c] * (dpv - d_tilde);
+                for (int g = 0; g < 4; ++g) {          // 8 keys per Philox call
+                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+                    if (DROP) {
+                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + c32 * 4 + g, (uint32_t)i, (uint32_t)bh,
+                                                       a.offset, a.seed_lo, a.seed_hi);
+                        wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
                     }
-                    w[e] = pack_bf16x2(ds[0], ds[1]);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int e = 4 * g + t;               // pair within this chunk
+                        const int ep = c32 * 16 + e;
+                        uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                        if (DROP) dp = f2_mul(dp, keep_factor2(wv[t], t16, a.keep_scale));
+                        dacc2 = f2_fma(pp[ep], dp, dacc2);
+                        w[e] = pack_bf16x2(f2_mul(pp[ep], f2_sub(dp, dt2)));
+                    }
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
             }
@@ -669,7 +678,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             {
                 uint32_t pw[HK / 2];
 #pragma unroll
-                for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+                for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(pp[e]);
                 if constexpr (HK / 2 == 32) {
                     tmem_st32(tmem + C::T_DP + lane_off + HK * h + HK / 2, pw);
                 } else {
@@ -679,6 +688,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->ds_full));
+        }
+        float d_exact;
+        {
+            float lo, hi;
+            f2_unpack(dacc2, lo, hi);
+            d_exact = lo + hi;
         }
         // exact row statistic: the two halves' partial sums
         dred[h * 128 + r] = d_exact;

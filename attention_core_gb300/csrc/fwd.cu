@@ -25,6 +25,7 @@
 #include "kernels.h"
 #include "philox.cuh"
 #include "ptx.cuh"
+#include "sched.cuh"
 #include "tile.cuh"
 
 namespace ac {
@@ -36,26 +37,32 @@ struct FwdCfg {
     using G = TileGeom<D>;
     static constexpr uint32_t TILE = G::template tile_bytes<128>();
     static constexpr uint32_t CHUNK = G::template chunk_bytes<128>();
-    static constexpr int ST = (D <= 96) ? 4 : 2;
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = TILE;
-    static constexpr uint32_t OFF_V = TILE * (1 + ST);
-    static constexpr uint32_t OFF_BAR = TILE * (1 + 2 * ST);
-    static constexpr uint32_t OFF_RED = OFF_BAR + 256;          // [2 buffers][2 halves][128] row maxima
+    // Two O accumulators and two Q buffers (a tile's epilogue then overlaps
+    // the next tile's MMAs) when TMEM has room: 2 x 128 score columns + 2 D.
+    static constexpr int NB = (D <= 128) ? 2 : 1;
+    static constexpr int ST = (D <= 64) ? 4 : (D <= 96 ? 3 : 2);
+    static constexpr uint32_t OFF_Q = 0;                   // NB Q tiles; a finished tile's
+                                                           // Q buffer stages its O for the store
+    static constexpr uint32_t OFF_K = NB * TILE;
+    static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
+    static constexpr uint32_t OFF_BAR = OFF_V + ST * TILE;
+    static constexpr uint32_t OFF_RED = OFF_BAR + 512;               // [2 buffers][2 halves][128] row maxima
     static constexpr uint32_t OFF_LRED = OFF_RED + 2 * 2 * 128 * 4;  // [2 halves][128] row sums
     static constexpr uint32_t SMEM = OFF_LRED + 2 * 128 * 4 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    // TMEM columns: two score buffers, then the O accumulator.
+    // TMEM columns: two score buffers, then NB O accumulators.
     static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256;
-    static_assert(T_O + D <= 512, "TMEM budget");
+    static_assert(T_O + NB * D <= 512, "TMEM budget");
 };
 
 struct FwdBars {
-    uint64_t q_full;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t s_full[2], p_full[2];
-    uint64_t o_done;
-    uint64_t xmax[2];      // row-max exchange between the two column halves
+    uint64_t xmax[2];       // row-max exchange between the two column halves
+    uint64_t lsum;          // row-sum exchange at the end of a tile
+    uint64_t o_done[2], o_free[2];
+    uint64_t stg_full[2];   // O of a tile staged in its Q buffer, ready for the store
     uint64_t never;
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -64,9 +71,24 @@ struct FwdBars {
 // Wait sites reported in bits 8.. of the status word on a timeout.
 enum : int32_t {
     kSiteInject = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull,
-    kSiteSFull, kSiteODone, kSiteXmax
+    kSiteSFull, kSiteODone, kSiteXmax, kSiteQEmpty, kSiteOFree, kSiteStg, kSiteLsum
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
+
+// Work tile t (longest first): query block and flattened query head.
+struct FwdTile {
+    int qb, bh, bkv, nk;
+};
+__device__ __forceinline__ FwdTile fwd_tile(const CommonArgs& a, int t)
+{
+    FwdTile w;
+    w.qb = a.n_blk - 1 - t / a.n_bh;
+    w.bh = t % a.n_bh;
+    const int group = a.h_q / a.h_kv;
+    w.bkv = (w.bh / a.h_q) * a.h_kv + (w.bh % a.h_q) / group;
+    w.nk = a.causal ? (w.qb + 1) : a.n_blk;
+    return w;
+}
 
 }  // namespace
 
@@ -79,6 +101,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     using G = TileGeom<D>;
     using C = FwdCfg<D>;
     constexpr int ST = C::ST;
+    constexpr int NB = C::NB;
     const CommonArgs& a = args.c;
 
     extern __shared__ uint8_t smem_raw[];
@@ -88,28 +111,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     FwdBars* bars = reinterpret_cast<FwdBars*>(smem_raw + pad + C::OFF_BAR);
     auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
-    const int n_bh = a.n_bh;
-    const int qb = a.n_blk - 1 - (int)(blockIdx.x / n_bh);   // longest causal rows first
-    const int bh = (int)(blockIdx.x % n_bh);
-    const int group = a.h_q / a.h_kv;
-    const int bkv = (bh / a.h_q) * a.h_kv + (bh % a.h_q) / group;
-    const int nk = a.causal ? (qb + 1) : a.n_blk;
+    const TileSched sched{a.n_blk * a.n_bh, (int)gridDim.x, (int)blockIdx.x};
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(bars->q_full), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(bars->q_full[b]), 1);
+            mbar_init(bar(bars->q_empty[b]), 2);     // last S MMA of the tile + store of its O
+            mbar_init(bar(bars->s_full[b]), 1);
+            mbar_init(bar(bars->p_full[b]), kRowThreads);
+            mbar_init(bar(bars->xmax[b]), kRowThreads);
+            mbar_init(bar(bars->o_done[b]), 1);
+            mbar_init(bar(bars->o_free[b]), kRowThreads);
+            mbar_init(bar(bars->stg_full[b]), kRowThreads);
+        }
         for (int st = 0; st < ST; ++st) {
             mbar_init(bar(bars->k_full[st]), 1);
             mbar_init(bar(bars->k_empty[st]), 1);
             mbar_init(bar(bars->v_full[st]), 1);
             mbar_init(bar(bars->v_empty[st]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(bars->s_full[b]), 1);
-            mbar_init(bar(bars->p_full[b]), kRowThreads);
-            mbar_init(bar(bars->xmax[b]), kRowThreads);
-        }
-        mbar_init(bar(bars->o_done), 1);
+        mbar_init(bar(bars->lsum), kRowThreads);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -135,193 +157,301 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (alive && warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer: Q, then the K ring
-            mbar_arrive_expect_tx(bar(bars->q_full), C::TILE);
-            for (int ch = 0; ch < G::NCH; ++ch)
-                tma_load_3d(sb + C::OFF_Q + ch * C::CHUNK, &tm_q, ch * G::CW, qb * 128, bh, bar(bars->q_full));
-            for (int j = 0; j < nk; ++j) {
-                const int st = j % ST;
-                if (!wait_bounded(wc, bar(bars->k_empty[st]), ((j / ST) & 1) ^ 1, timeout_code(kSiteKEmpty)))
-                    break;
-                mbar_arrive_expect_tx(bar(bars->k_full[st]), C::TILE);
+            // ---- TMA producer: the K ring over all blocks of all tiles
+            int g = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const FwdTile w = fwd_tile(a, t);
+                for (int j = 0; j < w.nk; ++j, ++g) {
+                    const int st = g % ST;
+                    ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteKEmpty));
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(bars->k_full[st]), C::TILE);
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_load_3d(sb + C::OFF_K + st * C::TILE + ch * C::CHUNK, &tm_k, ch * G::CW, j * 128, w.bkv,
+                                    bar(bars->k_full[st]));
+                }
+            }
+        } else if (lane == 1) {
+            // ---- TMA producer: each tile's Q as soon as its buffer is free
+            for (int u = 0;; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const FwdTile w = fwd_tile(a, t);
+                const int b = u % NB;
+                if (!wait_bounded(wc, bar(bars->q_empty[b]), ((u / NB) & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
+                mbar_arrive_expect_tx(bar(bars->q_full[b]), C::TILE);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_K + st * C::TILE + ch * C::CHUNK, &tm_k, ch * G::CW, j * 128, bkv,
-                                bar(bars->k_full[st]));
+                    tma_load_3d(sb + C::OFF_Q + b * C::TILE + ch * C::CHUNK, &tm_q, ch * G::CW, w.qb * 128, w.bh,
+                                bar(bars->q_full[b]));
             }
         }
     } else if (alive && warp == 2) {
         if (lane == 0) {
             // ---- TMA producer: the V ring
-            for (int j = 0; j < nk; ++j) {
-                const int st = j % ST;
-                if (!wait_bounded(wc, bar(bars->v_empty[st]), ((j / ST) & 1) ^ 1, timeout_code(kSiteVEmpty)))
-                    break;
-                mbar_arrive_expect_tx(bar(bars->v_full[st]), C::TILE);
-                for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_V + st * C::TILE + ch * C::CHUNK, &tm_v, ch * G::CW, j * 128, bkv,
-                                bar(bars->v_full[st]));
+            int g = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const FwdTile w = fwd_tile(a, t);
+                for (int j = 0; j < w.nk; ++j, ++g) {
+                    const int st = g % ST;
+                    ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteVEmpty));
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(bars->v_full[st]), C::TILE);
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_load_3d(sb + C::OFF_V + st * C::TILE + ch * C::CHUNK, &tm_v, ch * G::CW, j * 128, w.bkv,
+                                    bar(bars->v_full[st]));
+                }
             }
         }
     } else if (alive && warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer
+            // ---- MMA issuer.  One stream over all blocks of all tiles of this CTA:
+            // S_g, then O += P_{g-1} V_{g-1} for the block before (which may belong to
+            // the previous tile), so the next tile's first scores overlap the last
+            // softmax of the current one.
             constexpr uint32_t IDS = idesc_bf16(128, 128, false, false);  // S = Q K^T
             constexpr uint32_t IDO = idesc_bf16(128, D, false, true);     // O += P V
-            bool ok = wait_bounded(wc, bar(bars->q_full), 0, timeout_code(kSiteQFull));
-            auto issue_pv = [&](int i) -> bool {
-                if (!wait_bounded(wc, bar(bars->p_full[i & 1]), (i >> 1) & 1, timeout_code(kSitePFull)))
+            struct Blk {
+                int g, j, nk, u;
+            };
+            auto issue_pv = [&](const Blk& k) -> bool {
+                const int ob = k.u % NB;
+                if (k.j == 0 &&
+                    !wait_bounded(wc, bar(bars->o_free[ob]), ((k.u / NB) & 1) ^ 1, timeout_code(kSiteOFree)))
                     return false;
-                const int st = i % ST;
-                if (!wait_bounded(wc, bar(bars->v_full[st]), (i / ST) & 1, timeout_code(kSiteVFull)))
+                if (!wait_bounded(wc, bar(bars->p_full[k.g & 1]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
+                    return false;
+                const int st = k.g % ST;
+                if (!wait_bounded(wc, bar(bars->v_full[st]), (k.g / ST) & 1, timeout_code(kSiteVFull)))
                     return false;
                 tc_fence_after();
                 const uint32_t vbase = sb + C::OFF_V + st * C::TILE;
-                const uint32_t tP = tmem + ((i & 1) ? C::T_S1 : C::T_S0);
+                const uint32_t tP = tmem + ((k.g & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + C::T_O, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk), IDO,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::T_O + ob * D, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk),
+                           IDO, (k.j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(bars->v_empty[st]));
-                mma_commit(bar(bars->o_done));
+                mma_commit(bar(bars->o_done[ob]));
                 return true;
             };
-            for (int j = 0; j < nk && ok; ++j) {
-                const int st = j % ST;
-                ok = wait_bounded(wc, bar(bars->k_full[st]), (j / ST) & 1, timeout_code(kSiteKFull));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
-                const uint32_t tS = tmem + ((j & 1) ? C::T_S1 : C::T_S0);
+            Blk prev{-1, 0, 0, 0};
+            int g = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const FwdTile w = fwd_tile(a, t);
+                const int b = u % NB;
+                // At a tile boundary the previous tile's last P.V goes first unless this
+                // tile's Q and first K block are already resident: it must never wait on
+                // this tile's loads (with one Q buffer they wait on that P.V's tile).
+                if (prev.g >= 0 &&
+                    (NB == 1 || !mbar_test_wait(bar(bars->q_full[b]), (u / NB) & 1) ||
+                     !mbar_test_wait(bar(bars->k_full[g % ST]), (g / ST) & 1))) {
+                    ok = issue_pv(prev);
+                    prev.g = -1;
+                    if (!ok) break;
+                }
+                ok = wait_bounded(wc, bar(bars->q_full[b]), (u / NB) & 1, timeout_code(kSiteQFull));
+                for (int j = 0; j < w.nk && ok; ++j, ++g) {
+                    const int st = g % ST;
+                    ok = wait_bounded(wc, bar(bars->k_full[st]), (g / ST) & 1, timeout_code(kSiteKFull));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
+                    const uint32_t qbase = sb + C::OFF_Q + b * C::TILE;
+                    const uint32_t tS = tmem + ((g & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tS, G::template desc_k<128>(sb + C::OFF_Q, kk), G::template desc_k<128>(kbase, kk),
-                           IDS, kk > 0 ? 1u : 0u);
-                mma_commit(bar(bars->k_empty[st]));
-                mma_commit(bar(bars->s_full[j & 1]));
-                if (j > 0) ok = issue_pv(j - 1);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tS, G::template desc_k<128>(qbase, kk), G::template desc_k<128>(kbase, kk), IDS,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(bar(bars->k_empty[st]));
+                    mma_commit(bar(bars->s_full[g & 1]));
+                    if (j == w.nk - 1) mma_commit(bar(bars->q_empty[b]));
+                    if (prev.g >= 0) ok = issue_pv(prev);
+                    prev = Blk{g, j, w.nk, u};
+                }
             }
-            if (ok) issue_pv(nk - 1);
+            if (ok && prev.g >= 0) issue_pv(prev);
+        }
+    } else if (alive && warp == 3) {
+        if (lane == 0) {
+            // ---- store: a tile's O once the row threads have staged it
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const FwdTile w = fwd_tile(a, t);
+                const int b = u % NB;
+                ok = wait_bounded(wc, bar(bars->stg_full[b]), (u / NB) & 1, timeout_code(kSiteStg));
+                if (!ok) break;
+                for (int ch = 0; ch < G::NCH; ++ch)
+                    tma_store_3d(&tm_o, sb + C::OFF_Q + b * C::TILE + ch * C::CHUNK, ch * G::CW, w.qb * 128, w.bh);
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(bar(bars->q_empty[b]));
+            }
         }
     } else if (alive && warp >= 4) {
         // ---- softmax / epilogue: row = TMEM lane, half = which 64 keys of a block
         const RowThread rt = row_thread();
         const int h = rt.half, r = rt.row;
         const uint32_t lane_off = rt.lane_off;
-        const int i = qb * 128 + r;
-        const uint32_t t16 = a.thr << 16;
         float* xmax = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
         float* lred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_LRED);
-        float m_run = -INFINITY, l_run = 0.f;
+        int pv_done[2] = {0, 0};   // PV products completed into each O buffer by earlier tiles
+        int g0 = 0;
         bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            const uint32_t tS = tmem + ((j & 1) ? C::T_S1 : C::T_S0) + lane_off + 64 * h;
-            ok = __all_sync(0xffffffffu,
-                            wait_bounded(wc, bar(bars->s_full[j & 1]), (j >> 1) & 1, timeout_code(kSiteSFull)));
-            if (!ok) break;
-            tc_fence_after();
-            float x[64];
+        for (int u = 0; ok; ++u) {
+            const int t = sched.tile(u);
+            if (t < 0) break;
+            const FwdTile w = fwd_tile(a, t);
+            const int b = u % NB, ob = u % NB;
+            const int qb = w.qb, bh = w.bh, nk = w.nk;
+            const int i = qb * 128 + r;
+            const uint32_t tO = tmem + C::T_O + ob * D + lane_off;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nk; ++j) {
+                const int g = g0 + j;
+                const uint32_t tS = tmem + ((g & 1) ? C::T_S1 : C::T_S0) + lane_off + 64 * h;
+                ok = __all_sync(0xffffffffu,
+                                wait_bounded(wc, bar(bars->s_full[g & 1]), (g >> 1) & 1, timeout_code(kSiteSFull)));
+                if (!ok) break;
+                tc_fence_after();
+                float x[64];
 #pragma unroll
-            for (int c32 = 0; c32 < 2; ++c32) {
-                uint32_t rr[32];
-                tmem_ld32(tS + c32 * 32, rr);
+                for (int c32 = 0; c32 < 2; ++c32) {
+                    uint32_t rr[32];
+                    tmem_ld32(tS + c32 * 32, rr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[c32 * 32 + e] = __uint_as_float(rr[e]);
-            }
-            const int key0 = j * 128 + 64 * h;
-            if (a.causal && j == qb) {
+                    for (int e = 0; e < 32; ++e) x[c32 * 32 + e] = __uint_as_float(rr[e]);
+                }
+                const int key0 = j * 128 + 64 * h;
+                if (a.causal && j == qb) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (64 * h + c > r) x[c] = -INFINITY;
-            }
-            if (!a.causal && key0 + 64 > a.s) {
+                    for (int c = 0; c < 64; ++c)
+                        if (64 * h + c > r) x[c] = -INFINITY;
+                }
+                if (!a.causal && key0 + 64 > a.s) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (key0 + c >= a.s) x[c] = -INFINITY;
-            }
-            float mx = x[0];
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c >= a.s) x[c] = -INFINITY;
+                }
+                float mx = fmax3(x[0], x[1], x[2]);
 #pragma unroll
-            for (int c = 1; c < 64; ++c) mx = fmaxf(mx, x[c]);
-            // swap block maxima with the other half of the row
-            xmax[((j & 1) * 2 + h) * 128 + r] = mx;
-            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xmax[j & 1]), (j >> 1) & 1,
-                                                     timeout_code(kSiteXmax)));
-            if (!ok) break;
-            mx = fmaxf(mx, xmax[((j & 1) * 2 + (h ^ 1)) * 128 + r]);
-            const float m_new = fmaxf(m_run, mx * a.scale_log2);
-            if (__any_sync(0xffffffffu, m_new > m_run + 8.0f)) {
-                if (j > 0) {
-                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done), (j - 1) & 1,
-                                                              timeout_code(kSiteODone)));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const float f = ex2_approx(m_run - m_new);
-                    l_run *= f;
+                for (int c = 3; c < 63; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
+                mx = fmaxf(mx, x[63]);
+                // swap block maxima with the other half of the row
+                xmax[((g & 1) * 2 + h) * 128 + r] = mx;
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xmax[g & 1]), (g >> 1) & 1,
+                                                         timeout_code(kSiteXmax)));
+                if (!ok) break;
+                mx = fmaxf(mx, xmax[((g & 1) * 2 + (h ^ 1)) * 128 + r]);
+                const float m_new = fmaxf(m_run, mx * a.scale_log2);
+                if (__any_sync(0xffffffffu, m_new > m_run + 8.0f)) {
+                    if (j > 0) {
+                        ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done[ob]),
+                                                                  (pv_done[ob] + j - 1) & 1, timeout_code(kSiteODone)));
+                        if (!ok) break;
+                        tc_fence_after();
+                        const float f = ex2_approx(m_run - m_new);
+                        l_run *= f;
+                        const uint64_t f2 = f2_pack(f, f);
 #pragma unroll 1
-                    for (int c32 = h; c32 < D / 32; c32 += 2) {
-                        uint32_t rr[32];
-                        tmem_ld32(tmem + C::T_O + lane_off + c32 * 32, rr);
+                        for (int c32 = h; c32 < D / 32; c32 += 2) {
+                            uint32_t rr[32];
+                            tmem_ld32(tO + c32 * 32, rr);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * f);
-                        tmem_st32(tmem + C::T_O + lane_off + c32 * 32, rr);
+                            for (int e = 0; e < 16; ++e) {
+                                const uint64_t o2 =
+                                    f2_mul(f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), f2);
+                                float lo, hi;
+                                f2_unpack(o2, lo, hi);
+                                rr[2 * e] = __float_as_uint(lo);
+                                rr[2 * e + 1] = __float_as_uint(hi);
+                            }
+                            tmem_st32(tO + c32 * 32, rr);
+                        }
+                        tmem_st_wait();
                     }
-                    tmem_st_wait();
+                    m_run = m_new;
                 }
-                m_run = m_new;
-            }
-            const float neg_m = -m_run;
-            float lsum = 0.f;
+                // p = 2^(x * scale_log2 - m), two at a time; row sum before dropout
+                const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+                const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                uint64_t acc2 = f2_pack(0.f, 0.f);
+                uint64_t pp[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float pv = ex2_approx(fmaf(x[c], a.scale_log2, neg_m));
-                lsum += pv;
-                x[c] = pv;
-            }
-            l_run += lsum;
-            uint32_t pw[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-            if (DROP) {
-                // group g covers keys key0 + 8g .. +7: words 4g .. 4g+3 of pw
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g, (uint32_t)i, (uint32_t)bh, a.offset,
-                                                   a.seed_lo, a.seed_hi);
-                    pw[4 * g + 0] &= keep_mask16x2(w4.x, t16);
-                    pw[4 * g + 1] &= keep_mask16x2(w4.y, t16);
-                    pw[4 * g + 2] &= keep_mask16x2(w4.z, t16);
-                    pw[4 * g + 3] &= keep_mask16x2(w4.w, t16);
+                for (int e = 0; e < 32; ++e) {
+                    float lo, hi;
+                    f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), lo, hi);
+                    pp[e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
+                    acc2 = f2_add(acc2, pp[e]);
                 }
+                {
+                    float lo, hi;
+                    f2_unpack(acc2, lo, hi);
+                    l_run += lo + hi;
+                }
+                uint32_t pw[32];
+                if (DROP) {
+                    // group g8 covers keys key0 + 8 g8 .. +7, i.e. pairs 4 g8 .. 4 g8 + 3;
+                    // Philox word t decides pair 4 g8 + t (low half: even key, high: odd key)
+                    const uint32_t t16 = a.thr << 16;
+#pragma unroll
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g8, (uint32_t)i, (uint32_t)bh,
+                                                       a.offset, a.seed_lo, a.seed_hi);
+                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int tt = 0; tt < 4; ++tt) {
+                            float lo, hi;
+                            f2_unpack(pp[4 * g8 + tt], lo, hi);
+                            lo = (wv[tt] << 16) >= t16 ? lo : 0.f;
+                            hi = wv[tt] >= t16 ? hi : 0.f;
+                            pw[4 * g8 + tt] = pack_bf16x2(lo, hi);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(pp[e]);
+                }
+                tmem_st32(tS, pw);   // P_d of these 64 keys over the first 32 of the half's columns
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(bars->p_full[g & 1]));
             }
-            tmem_st32(tS, pw);   // P_d of these 64 keys over the first 32 of the half's columns
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(bars->p_full[j & 1]));
-        }
-        // row sum over both halves (every row thread reaches this point once)
-        lred[h * 128 + r] = l_run;
-        named_barrier_sync(1, kRowThreads);
-        const float l_tot = l_run + lred[(h ^ 1) * 128 + r];
-        if (ok)
-            ok = __all_sync(0xffffffffu,
-                            wait_bounded(wc, bar(bars->o_done), (nk - 1) & 1, timeout_code(kSiteODone)));
-        if (ok) {
+            if (!ok) break;
+            // row sum over both halves
+            lred[h * 128 + r] = l_run;
+            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->lsum), u & 1, timeout_code(kSiteLsum)));
+            if (!ok) break;
+            const float l_tot = l_run + lred[(h ^ 1) * 128 + r];
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done[ob]), (pv_done[ob] + nk - 1) & 1,
+                                                      timeout_code(kSiteODone)));
+            if (!ok) break;
             tc_fence_after();
             const float inv = a.keep_scale / l_tot;
+            const uint32_t stage = sb + C::OFF_Q + b * C::TILE;   // this tile's Q: all its S MMAs are done
 #pragma unroll 1
             for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + C::T_O + lane_off + c32 * 32, rr);
-                stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rr, inv);
+                tmem_ld32(tO + c32 * 32, rr);
+                stage_row32<D, 128>(stage, r, c32 * 32, rr, inv);
             }
             if (h == 0 && i < a.s) args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
-        }
-        fence_proxy_async_smem();
-        named_barrier_sync(1, kRowThreads);
-        if (h == 0 && r == 0 && !bars->abort_flag) {
-            for (int ch = 0; ch < G::NCH; ++ch)
-                tma_store_3d(&tm_o, sb + C::OFF_Q + ch * C::CHUNK, ch * G::CW, qb * 128, bh);
-            bulk_commit();
-            bulk_wait_read0();
+            tc_fence_before();
+            mbar_arrive(bar(bars->o_free[ob]));
+            fence_proxy_async_smem();
+            mbar_arrive(bar(bars->stg_full[b]));
+            pv_done[ob] += nk;
+            g0 += nk;
         }
     }
 
@@ -346,7 +476,8 @@ static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     auto kern = attn_fwd_kernel<D, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
-    const unsigned grid = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
+    const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
+    const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, a);
     return (int)cudaGetLastError();
 }

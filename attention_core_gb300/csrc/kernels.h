@@ -35,6 +35,7 @@ struct CommonArgs {
 struct FwdArgs {
     CommonArgs c;
     float* lse;           // [b*h_q*s]
+    int32_t num_sms;      // persistent grid size
 };
 
 struct BwdArgs {
@@ -43,7 +44,7 @@ struct BwdArgs {
     const uint16_t* o;    // bf16 [b*h_q*s*d]
     const uint16_t* dout; // bf16 [b*h_q*s*d]
     const float* lse;     // [b*h_q*s]
-    float* lse2_ws;       // [b*h_q*s_pad]  LSE * log2(e); +inf past s
+    float* lse2_ws;       // [b*h_q*s_pad]  -LSE * log2(e); -inf past s
     float* delta_ws;      // [b*h_q*s_pad]  row statistic D: rowsum(dO * O) from the
                           // preprocess, replaced by sum_j P_ij dP_ij by the dQ kernel
     int32_t d;

@@ -14,6 +14,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace ac {
 
 struct PhiloxKey {
@@ -48,6 +50,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
 __device__ __forceinline__ uint32_t keep_mask16x2(uint32_t w, uint32_t t16)
 {
     return (w >= t16 ? 0xffff0000u : 0u) | ((w << 16) >= t16 ? 0x0000ffffu : 0u);
+}
+
+// Dropout factors of the two keys a Philox output word decides: z = zs where
+// the draw is >= thr (kept), 0 where dropped, packed (even key, odd key).
+// t16 = thr << 16 (see keep_mask16x2).
+__device__ __forceinline__ uint64_t keep_factor2(uint32_t w, uint32_t t16, float zs)
+{
+    return f2_pack((w << 16) >= t16 ? zs : 0.f, w >= t16 ? zs : 0.f);
 }
 
 // Keep bits of the eight keys 8*group .. 8*group+7 of one query row:
