@@ -199,6 +199,7 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
         return rc;
     ac::FwdArgs a{};
     a.c = common_args(p);
+    a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     if ((rc = device_sms(&a.num_sms))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

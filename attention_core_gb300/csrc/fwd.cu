@@ -11,7 +11,8 @@
 // "Recomputing Activations", "Memory for compute, selectively").
 //
 // Structure of a CTA (384 threads):
-//   warp 0  TMA: Q once, then K blocks into a ring of stages
+//   warp 0  TMA: lane 0 the K ring, lane 1 each tile's Q as soon as the
+//           previous tile's last S MMA has read the Q buffer
 //   warp 2  TMA: V blocks into their own ring
 //   warp 1  one thread issues tcgen05 MMAs: S_j = Q K_j^T into one of two
 //           TMEM score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM
@@ -19,7 +20,9 @@
 //           per half of the 128 keys of a block: online softmax in the log2
 //           domain (the halves swap their row maxima through shared memory),
 //           dropout from Philox, P_d written back to TMEM as bf16 inside the
-//           half's own score columns; epilogue O / l -> bf16 -> TMA store.
+//           half's own score columns; epilogue O / l -> bf16 stored straight
+//           from registers (no staging buffer, so shared memory goes to
+//           deeper K/V rings).
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks skip the rescale; O / l is exact either way.
 #include "kernels.h"
@@ -37,32 +40,31 @@ struct FwdCfg {
     using G = TileGeom<D>;
     static constexpr uint32_t TILE = G::template tile_bytes<128>();
     static constexpr uint32_t CHUNK = G::template chunk_bytes<128>();
-    // Two O accumulators and two Q buffers (a tile's epilogue then overlaps
-    // the next tile's MMAs) when TMEM has room: 2 x 128 score columns + 2 D.
-    static constexpr int NB = (D <= 128) ? 2 : 1;
-    static constexpr int ST = (D <= 64) ? 4 : (D <= 96 ? 3 : 2);
-    static constexpr uint32_t OFF_Q = 0;                   // NB Q tiles; a finished tile's
-                                                           // Q buffer stages its O for the store
-    static constexpr uint32_t OFF_K = NB * TILE;
+    // K and V rings: a block's load is issued when the block ST earlier has
+    // been consumed, so ST blocks of work must cover one TMA round trip.
+    static constexpr int ST = (D <= 64) ? 6 : (D <= 96 ? 4 : (D <= 128 ? 3 : 2));
+    static constexpr uint32_t OFF_Q = 0;                   // one Q tile
+    static constexpr uint32_t OFF_K = TILE;
     static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
     static constexpr uint32_t OFF_BAR = OFF_V + ST * TILE;
-    static constexpr uint32_t OFF_RED = OFF_BAR + 512;               // [2 buffers][2 halves][128] row maxima
-    static constexpr uint32_t OFF_LRED = OFF_RED + 2 * 2 * 128 * 4;  // [2 halves][128] row sums
-    static constexpr uint32_t SMEM = OFF_LRED + 2 * 128 * 4 + 1024;
+    static constexpr uint32_t SMEM = OFF_BAR + 320 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    // TMEM columns: two score buffers, then NB O accumulators.
-    static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256;
-    static_assert(T_O + NB * D <= 512, "TMEM budget");
+    // TMEM columns: two score buffers, the O accumulator, then six exchange
+    // columns through which the two halves of a row swap their block maxima
+    // (2 buffers x 2 halves) and row sums (2 halves).
+    static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_X = 256 + D;
+    static_assert(T_X + 6 <= 512, "TMEM budget");
 };
 
 struct FwdBars {
-    uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+    uint64_t q_full, q_empty;
+    uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
     uint64_t s_full[2], p_full[2];
     uint64_t xmax[2];       // row-max exchange between the two column halves
     uint64_t lsum;          // row-sum exchange at the end of a tile
-    uint64_t o_done[2], o_free[2];
-    uint64_t stg_full[2];   // O of a tile staged in its Q buffer, ready for the store
+    uint64_t o_done, o_free;
+    uint64_t o_tile;        // a tile's last P.V product is done (its O is final)
+    uint64_t drain;         // every MMA of this CTA is done (before TMEM is released)
     uint64_t never;
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -71,7 +73,7 @@ struct FwdBars {
 // Wait sites reported in bits 8.. of the status word on a timeout.
 enum : int32_t {
     kSiteInject = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull,
-    kSiteSFull, kSiteODone, kSiteXmax, kSiteQEmpty, kSiteOFree, kSiteStg, kSiteLsum
+    kSiteSFull, kSiteODone, kSiteXmax, kSiteQEmpty, kSiteOFree, kSiteLsum, kSiteOTile, kSiteDrain
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
@@ -101,7 +103,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     using G = TileGeom<D>;
     using C = FwdCfg<D>;
     constexpr int ST = C::ST;
-    constexpr int NB = C::NB;
     const CommonArgs& a = args.c;
 
     extern __shared__ uint8_t smem_raw[];
@@ -115,16 +116,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
+        mbar_init(bar(bars->q_full), 1);
+        mbar_init(bar(bars->q_empty), 1);            // the tile's last S MMA is done
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(bars->q_full[b]), 1);
-            mbar_init(bar(bars->q_empty[b]), 2);     // last S MMA of the tile + store of its O
             mbar_init(bar(bars->s_full[b]), 1);
             mbar_init(bar(bars->p_full[b]), kRowThreads);
             mbar_init(bar(bars->xmax[b]), kRowThreads);
-            mbar_init(bar(bars->o_done[b]), 1);
-            mbar_init(bar(bars->o_free[b]), kRowThreads);
-            mbar_init(bar(bars->stg_full[b]), kRowThreads);
         }
+        mbar_init(bar(bars->o_done), 1);
+        mbar_init(bar(bars->o_free), kRowThreads);
+        mbar_init(bar(bars->o_tile), 1);
+        mbar_init(bar(bars->drain), 1);
         for (int st = 0; st < ST; ++st) {
             mbar_init(bar(bars->k_full[st]), 1);
             mbar_init(bar(bars->k_empty[st]), 1);
@@ -180,12 +182,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int t = sched.tile(u);
                 if (t < 0) break;
                 const FwdTile w = fwd_tile(a, t);
-                const int b = u % NB;
-                if (!wait_bounded(wc, bar(bars->q_empty[b]), ((u / NB) & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
-                mbar_arrive_expect_tx(bar(bars->q_full[b]), C::TILE);
+                if (!wait_bounded(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
+                mbar_arrive_expect_tx(bar(bars->q_full), C::TILE);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_Q + b * C::TILE + ch * C::CHUNK, &tm_q, ch * G::CW, w.qb * 128, w.bh,
-                                bar(bars->q_full[b]));
+                    tma_load_3d(sb + C::OFF_Q + ch * C::CHUNK, &tm_q, ch * G::CW, w.qb * 128, w.bh, bar(bars->q_full));
             }
         }
     } else if (alive && warp == 2) {
@@ -220,9 +220,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 int g, j, nk, u;
             };
             auto issue_pv = [&](const Blk& k) -> bool {
-                const int ob = k.u % NB;
-                if (k.j == 0 &&
-                    !wait_bounded(wc, bar(bars->o_free[ob]), ((k.u / NB) & 1) ^ 1, timeout_code(kSiteOFree)))
+                if (k.j == 0 && !wait_bounded(wc, bar(bars->o_free), (k.u & 1) ^ 1, timeout_code(kSiteOFree)))
                     return false;
                 if (!wait_bounded(wc, bar(bars->p_full[k.g & 1]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
                     return false;
@@ -234,10 +232,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t tP = tmem + ((k.g & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + C::T_O + ob * D, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk),
-                           IDO, (k.j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::T_O, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk), IDO,
+                           (k.j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(bars->v_empty[st]));
-                mma_commit(bar(bars->o_done[ob]));
+                mma_commit(bar(bars->o_done));
+                if (k.j == k.nk - 1) mma_commit(bar(bars->o_tile));
                 return true;
             };
             Blk prev{-1, 0, 0, 0};
@@ -247,25 +246,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int t = sched.tile(u);
                 if (t < 0) break;
                 const FwdTile w = fwd_tile(a, t);
-                const int b = u % NB;
                 // At a tile boundary the previous tile's last P.V goes first unless this
                 // tile's Q and first K block are already resident: it must never wait on
-                // this tile's loads (with one Q buffer they wait on that P.V's tile).
-                if (prev.g >= 0 &&
-                    (NB == 1 || !mbar_test_wait(bar(bars->q_full[b]), (u / NB) & 1) ||
-                     !mbar_test_wait(bar(bars->k_full[g % ST]), (g / ST) & 1))) {
+                // this tile's loads.
+                if (prev.g >= 0 && (!mbar_test_wait(bar(bars->q_full), u & 1) ||
+                                    !mbar_test_wait(bar(bars->k_full[g % ST]), (g / ST) & 1))) {
                     ok = issue_pv(prev);
                     prev.g = -1;
                     if (!ok) break;
                 }
-                ok = wait_bounded(wc, bar(bars->q_full[b]), (u / NB) & 1, timeout_code(kSiteQFull));
+                ok = wait_bounded(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
                 for (int j = 0; j < w.nk && ok; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->k_full[st]), (g / ST) & 1, timeout_code(kSiteKFull));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
-                    const uint32_t qbase = sb + C::OFF_Q + b * C::TILE;
+                    const uint32_t qbase = sb + C::OFF_Q;
                     const uint32_t tS = tmem + ((g & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -273,49 +270,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                kk > 0 ? 1u : 0u);
                     mma_commit(bar(bars->k_empty[st]));
                     mma_commit(bar(bars->s_full[g & 1]));
-                    if (j == w.nk - 1) mma_commit(bar(bars->q_empty[b]));
+                    if (j == w.nk - 1) mma_commit(bar(bars->q_empty));
                     if (prev.g >= 0) ok = issue_pv(prev);
                     prev = Blk{g, j, w.nk, u};
                 }
             }
-            if (ok && prev.g >= 0) issue_pv(prev);
-        }
-    } else if (alive && warp == 3) {
-        if (lane == 0) {
-            // ---- store: a tile's O once the row threads have staged it
-            bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const FwdTile w = fwd_tile(a, t);
-                const int b = u % NB;
-                ok = wait_bounded(wc, bar(bars->stg_full[b]), (u / NB) & 1, timeout_code(kSiteStg));
-                if (!ok) break;
-                for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_store_3d(&tm_o, sb + C::OFF_Q + b * C::TILE + ch * C::CHUNK, ch * G::CW, w.qb * 128, w.bh);
-                bulk_commit();
-                bulk_wait_read0();
-                mbar_arrive(bar(bars->q_empty[b]));
-            }
+            if (ok && prev.g >= 0) ok = issue_pv(prev);
+            // every MMA must be complete before the CTA releases TMEM
+            mma_commit(bar(bars->drain));
+            wait_bounded(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 4) {
         // ---- softmax / epilogue: row = TMEM lane, half = which 64 keys of a block
         const RowThread rt = row_thread();
         const int h = rt.half, r = rt.row;
         const uint32_t lane_off = rt.lane_off;
-        float* xmax = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
-        float* lred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_LRED);
-        int pv_done[2] = {0, 0};   // PV products completed into each O buffer by earlier tiles
+        const uint32_t tX = tmem + C::T_X + lane_off;   // exchange columns of this warp's rows
+        int pv_done = 0;            // P.V products completed into O by earlier tiles
         int g0 = 0;
         bool ok = true;
         for (int u = 0; ok; ++u) {
             const int t = sched.tile(u);
             if (t < 0) break;
             const FwdTile w = fwd_tile(a, t);
-            const int b = u % NB, ob = u % NB;
             const int qb = w.qb, bh = w.bh, nk = w.nk;
             const int i = qb * 128 + r;
-            const uint32_t tO = tmem + C::T_O + ob * D + lane_off;
+            const uint32_t tO = tmem + C::T_O + lane_off;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nk; ++j) {
                 const int g = g0 + j;
@@ -347,17 +327,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int c = 3; c < 63; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
                 mx = fmaxf(mx, x[63]);
-                // swap block maxima with the other half of the row
-                xmax[((g & 1) * 2 + h) * 128 + r] = mx;
+                // swap block maxima with the other half of the row through TMEM
+                tmem_st1(tX + (g & 1) * 2 + h, __float_as_uint(mx));
+                tmem_st_wait();
+                tc_fence_before();
                 ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xmax[g & 1]), (g >> 1) & 1,
                                                          timeout_code(kSiteXmax)));
                 if (!ok) break;
-                mx = fmaxf(mx, xmax[((g & 1) * 2 + (h ^ 1)) * 128 + r]);
+                tc_fence_after();
+                mx = fmaxf(mx, __uint_as_float(tmem_ld1(tX + (g & 1) * 2 + (h ^ 1))));
                 const float m_new = fmaxf(m_run, mx * a.scale_log2);
                 if (__any_sync(0xffffffffu, m_new > m_run + 8.0f)) {
                     if (j > 0) {
-                        ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done[ob]),
-                                                                  (pv_done[ob] + j - 1) & 1, timeout_code(kSiteODone)));
+                        ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done), (pv_done + j - 1) & 1,
+                                                                  timeout_code(kSiteODone)));
                         if (!ok) break;
                         tc_fence_after();
                         const float f = ex2_approx(m_run - m_new);
@@ -382,45 +365,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     m_run = m_new;
                 }
-                // p = 2^(x * scale_log2 - m), two at a time; row sum before dropout
+                // p = 2^(x * scale_log2 - m), two at a time, and the dropout mask, in eight
+                // independent units of 8 keys (one Philox call each) so that the exp2
+                // (MUFU) and Philox (integer multiply) work of different units overlap;
+                // the row sum is taken before dropout.
                 const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
                 const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                const uint32_t t16 = a.thr << 16;
                 uint64_t acc2 = f2_pack(0.f, 0.f);
-                uint64_t pp[32];
+                uint32_t pw[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float lo, hi;
-                    f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), lo, hi);
-                    pp[e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
-                    acc2 = f2_add(acc2, pp[e]);
+                for (int g8 = 0; g8 < 8; ++g8) {
+                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+                    if (DROP) {
+                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g8, (uint32_t)i, (uint32_t)bh,
+                                                       a.offset, a.seed_lo, a.seed_hi);
+                        wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
+                    }
+#pragma unroll
+                    for (int tt = 0; tt < 4; ++tt) {
+                        const int e = 4 * g8 + tt;       // pair e: keys key0 + 2e, 2e + 1
+                        float lo, hi;
+                        f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), lo, hi);
+                        lo = ex2_approx(lo);
+                        hi = ex2_approx(hi);
+                        acc2 = f2_add(acc2, f2_pack(lo, hi));
+                        if (DROP) {
+                            // Philox word tt decides pair 4 g8 + tt (low half: even key, high: odd)
+                            lo = (wv[tt] << 16) >= t16 ? lo : 0.f;
+                            hi = wv[tt] >= t16 ? hi : 0.f;
+                        }
+                        pw[e] = pack_bf16x2(lo, hi);
+                    }
                 }
                 {
                     float lo, hi;
                     f2_unpack(acc2, lo, hi);
                     l_run += lo + hi;
-                }
-                uint32_t pw[32];
-                if (DROP) {
-                    // group g8 covers keys key0 + 8 g8 .. +7, i.e. pairs 4 g8 .. 4 g8 + 3;
-                    // Philox word t decides pair 4 g8 + t (low half: even key, high: odd key)
-                    const uint32_t t16 = a.thr << 16;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g8, (uint32_t)i, (uint32_t)bh,
-                                                       a.offset, a.seed_lo, a.seed_hi);
-                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                        for (int tt = 0; tt < 4; ++tt) {
-                            float lo, hi;
-                            f2_unpack(pp[4 * g8 + tt], lo, hi);
-                            lo = (wv[tt] << 16) >= t16 ? lo : 0.f;
-                            hi = wv[tt] >= t16 ? hi : 0.f;
-                            pw[4 * g8 + tt] = pack_bf16x2(lo, hi);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) pw[e] = pack_bf16x2(pp[e]);
                 }
                 tmem_st32(tS, pw);   // P_d of these 64 keys over the first 32 of the half's columns
                 tmem_st_wait();
@@ -428,29 +409,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(bar(bars->p_full[g & 1]));
             }
             if (!ok) break;
-            // row sum over both halves
-            lred[h * 128 + r] = l_run;
+            // row sum over both halves, through TMEM
+            tmem_st1(tX + 4 + h, __float_as_uint(l_run));
+            tmem_st_wait();
+            tc_fence_before();
             ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->lsum), u & 1, timeout_code(kSiteLsum)));
             if (!ok) break;
-            const float l_tot = l_run + lred[(h ^ 1) * 128 + r];
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done[ob]), (pv_done[ob] + nk - 1) & 1,
-                                                      timeout_code(kSiteODone)));
+            tc_fence_after();
+            const float l_tot = l_run + __uint_as_float(tmem_ld1(tX + 4 + (h ^ 1)));
+            // the tile's final P.V: a barrier of its own, completing once per tile (the
+            // shared o_done may still be two phases behind here)
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_tile), u & 1, timeout_code(kSiteOTile)));
             if (!ok) break;
             tc_fence_after();
             const float inv = a.keep_scale / l_tot;
-            const uint32_t stage = sb + C::OFF_Q + b * C::TILE;   // this tile's Q: all its S MMAs are done
+            // O row i straight to global memory: 16-byte stores of this half's
+            // 32-column chunks.  The TMEM loads are warp-collective, so every
+            // lane takes them; only the stores are guarded (rows past s).
+            {
+                const bool live = i < a.s;
+                uint4* orow = reinterpret_cast<uint4*>(args.o + ((size_t)bh * a.s + (live ? i : 0)) * D);
 #pragma unroll 1
-            for (int c32 = h; c32 < D / 32; c32 += 2) {
-                uint32_t rr[32];
-                tmem_ld32(tO + c32 * 32, rr);
-                stage_row32<D, 128>(stage, r, c32 * 32, rr, inv);
+                for (int c32 = h; c32 < D / 32; c32 += 2) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + c32 * 32, rr);
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16x2(__uint_as_float(rr[8 * u4 + 2 * e]) * inv,
+                                                __uint_as_float(rr[8 * u4 + 2 * e + 1]) * inv);
+                        if (live) orow[c32 * 4 + u4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+                if (live && h == 0)
+                    args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
             }
-            if (h == 0 && i < a.s) args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
             tc_fence_before();
-            mbar_arrive(bar(bars->o_free[ob]));
-            fence_proxy_async_smem();
-            mbar_arrive(bar(bars->stg_full[b]));
-            pv_done[ob] += nk;
+            mbar_arrive(bar(bars->o_free));
+            pv_done += nk;
             g0 += nk;
         }
     }

@@ -34,6 +34,7 @@ struct CommonArgs {
 
 struct FwdArgs {
     CommonArgs c;
+    uint16_t* o;          // bf16 [b*h_q*s*d]
     float* lse;           // [b*h_q*s]
     int32_t num_sms;      // persistent grid size
 };
