@@ -225,8 +225,9 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
     const int bq = ac::dkdv_query_tile(p->d);
     const int bn = ac::dq_key_tile(p->d);
-    CUtensorMap tq128, tdo128, tqb, tdob, tk, tv, tkb, tvb, tdq, tdk, tdv;
+    CUtensorMap tq128, tdo128, to128, tqb, tdob, tk, tv, tkb, tvb, tdq, tdk, tdv;
     if ((rc = encode_map(&tq128, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tdo128, dout, p->d, p->s, nq, 128)) ||
+        (rc = encode_map(&to128, o, p->d, p->s, nq, 128)) ||
         (rc = encode_map(&tqb, q, p->d, p->s, nq, bq)) || (rc = encode_map(&tdob, dout, p->d, p->s, nq, bq)) ||
         (rc = encode_map(&tk, k, p->d, p->s, nkv, 128)) || (rc = encode_map(&tv, v, p->d, p->s, nkv, 128)) ||
         (rc = encode_map(&tkb, k, p->d, p->s, nkv, bn)) || (rc = encode_map(&tvb, v, p->d, p->s, nkv, bn)) ||
@@ -245,12 +246,10 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool drop = a.c.thr != 0;
     if ((rc = record(p->timing_events, 0, st))) return rc;
-    if (ac::launch_bwd_pre(a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, to128, tdq, a, st) != 0) return ATTN_CORE_ERR_CUDA;
     if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
-    if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, tdq, a, st) != 0) return ATTN_CORE_ERR_CUDA;
-    if ((rc = record(p->timing_events, 3, st)) || (rc = record(p->timing_events, 4, st))) return rc;
     if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
-    return record(p->timing_events, 5, st);
+    return record(p->timing_events, 3, st);
 }
 
 // ---------------------------------------------------------------------------

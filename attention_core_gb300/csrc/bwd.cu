@@ -10,14 +10,13 @@
 //     dV = (P * Z)^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K
 // (D_i equals sum_j P_ij dP_ij because O_i = sum_j P_ij Z_ij V_j).
 //
-// Three kernels, launched in this order:
-//   bwd_pre   per query row, LSE_i * log2(e) and a first estimate
-//             D~_i = rowsum(dO_i * O_i) from the bf16 output, into a padded
-//             workspace
+// Two kernels, launched in this order:
 //   bwd_dq    one (query head, 128-query block) per CTA; queries on TMEM
-//             lanes; recomputes S and dP per key block, accumulates dQ in TMEM
-//             with the exact statistic D_i = sum_j P_ij dP_ij (see below) and
-//             writes that D_i back to the workspace
+//             lanes; forms -LSE_i * log2(e) and a first estimate
+//             D~_i = rowsum(dO_i * O_i) from the bf16 output, recomputes S and
+//             dP per key block, accumulates dQ in TMEM with the exact
+//             statistic D_i = sum_j P_ij dP_ij (see below) and writes both
+//             row statistics to a padded workspace
 //   bwd_dkdv  one (KV head, 128-key block) per CTA; keys on TMEM lanes; loops
 //             over the query heads of the GQA group and their query tiles;
 //             recomputes S^T and dP^T, accumulates dV and dK in TMEM
@@ -34,52 +33,11 @@ namespace {
 
 enum : int32_t {
     kSiteInject = 1, kSiteKvFull, kSiteQEmpty, kSiteQFull, kSitePFull, kSiteDsFull, kSiteSFull,
-    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSiteSRead
+    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSiteSRead, kSiteOFull, kSiteOFree
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
 }  // namespace
-
-// ======================================================= preprocess ======
-// One warp per padded query row: D~_i = sum_c dO_ic O_ic in fp32 and
-// -LSE_i * log2(e), so that P = 2^(S * scale * log2(e) - LSE * log2(e)) is one
-// FMA and an exp2; rows past s get 0 and -inf (their probabilities recompute
-// to exactly 0).
-__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const BwdArgs a)
-{
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int64_t n_rows = (int64_t)a.c.n_bh * a.s_pad;
-    if (row >= n_rows) return;
-    const int64_t bh = row / a.s_pad;
-    const int64_t i = row % a.s_pad;
-    if (i >= a.c.s) {
-        if (lane == 0) {
-            a.delta_ws[row] = 0.f;
-            a.lse2_ws[row] = -INFINITY;
-        }
-        return;
-    }
-    const int64_t base = (bh * a.c.s + i) * a.d;
-    float acc = 0.f;
-    for (int c8 = lane; c8 < a.d / 8; c8 += 32) {
-        const uint4 o4 = *reinterpret_cast<const uint4*>(a.o + base + c8 * 8);
-        const uint4 g4 = *reinterpret_cast<const uint4*>(a.dout + base + c8 * 8);
-        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
-        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
-            acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(gw[e] & 0xFFFF0000u), acc);
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        a.delta_ws[row] = acc;
-        a.lse2_ws[row] = -a.lse[bh * a.c.s + i] * 1.44269504088896340736f;
-    }
-}
 
 // ============================================================ dK / dV ====
 namespace {
@@ -429,6 +387,11 @@ struct DqCfg {
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KT;
     static constexpr uint32_t OFF_RED = OFF_BAR + 256;      // [2 halves][128] partial row statistics
     static constexpr uint32_t SMEM = OFF_RED + 2 * 128 * 4 + 1024;
+    // The O tile (for the first estimate D~) is staged once at the end of the V
+    // ring; V stages from O_ST0 on are loaded only after the row threads have read it.
+    static_assert(VST * KT >= QT, "O tile must fit in the V ring");
+    static constexpr uint32_t OFF_O = OFF_V + VST * KT - QT;
+    static constexpr int O_ST0 = (int)((VST * KT - QT) / KT);
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM: S | dP (later dS~ in its first half, P in its second) | dQ~ | PK
     static constexpr uint32_t T_S = 0, T_DP = BN, T_DQ = 2 * BN, T_PK = 2 * BN + D;
@@ -439,6 +402,7 @@ struct DqBars {
     uint64_t qdo_full;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full, s_read, dp_full, ds_full, acc_done;
+    uint64_t o_full, o_free;
     uint64_t never;
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -450,7 +414,8 @@ template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args)
+                   const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dq,
+                   const BwdArgs args)
 {
     using G = TileGeom<D>;
     using C = DqCfg<D>;
@@ -487,6 +452,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(bar(bars->dp_full), 1);
         mbar_init(bar(bars->ds_full), kRowThreads);
         mbar_init(bar(bars->acc_done), 1);
+        mbar_init(bar(bars->o_full), 1);
+        mbar_init(bar(bars->o_free), kRowThreads);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -496,6 +463,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_o);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_base), 512);
@@ -518,6 +486,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
                 tma_load_3d(sb + C::OFF_DO + ch * C::QCH, &tm_do, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
             }
+            mbar_arrive_expect_tx(bar(bars->o_full), C::QT);
+            for (int ch = 0; ch < G::NCH; ++ch)
+                tma_load_3d(sb + C::OFF_O + ch * C::QCH, &tm_o, ch * G::CW, qb * 128, bh, bar(bars->o_full));
             for (int j = 0; j < nk; ++j) {
                 const int st = j % KST;
                 if (!wait_bounded(wc, bar(bars->k_empty[st]), ((j / KST) & 1) ^ 1, timeout_code(kSiteKEmpty)))
@@ -534,6 +505,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int j = 0; j < nk; ++j) {
                 const int st = j % VST;
                 if (!wait_bounded(wc, bar(bars->v_empty[st]), ((j / VST) & 1) ^ 1, timeout_code(kSiteVEmpty)))
+                    break;
+                if (j < VST && j >= C::O_ST0 &&
+                    !wait_bounded(wc, bar(bars->o_free), 0, timeout_code(kSiteOFree)))
                     break;
                 mbar_arrive_expect_tx(bar(bars->v_full[st]), C::KT);
                 for (int ch = 0; ch < G::NCH; ++ch)
@@ -606,16 +580,46 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t lane_off = rt.lane_off;
         const int i = qb * 128 + r;
         const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
-        const float nl2 = args.lse2_ws[srow];
-        const float d_tilde = args.delta_ws[srow];
         const uint32_t t16 = a.thr << 16;
         float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
+        // Row statistics of this query: -LSE * log2(e) (-inf past s, so its
+        // probabilities recompute to 0), and the first estimate
+        // D~ = rowsum(dO * O) from the staged bf16 O and dO tiles (rows past s
+        // were filled with zeros by TMA).  Each half sums its D/2 columns; the
+        // halves meet in shared memory.
+        const float nl2 = i < a.s ? -args.lse[(size_t)bh * a.s + i] * 1.44269504088896340736f : -INFINITY;
+        if (h == 0) args.lse2_ws[srow] = nl2;
+        bool ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_full), 0, timeout_code(kSiteOFull)));
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->qdo_full), 0, timeout_code(kSiteQFull)));
+        float d_tilde = 0.f;
+        if (ok) {
+            uint64_t acc2 = f2_pack(0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < D / 16; ++u) {
+                const uint32_t off = G::template unit_offset<128>(r, h * (D / 2) + 8 * u);
+                const uint4 ov = ld_shared_v4(sb + C::OFF_O + off);
+                const uint4 gv = ld_shared_v4(sb + C::OFF_DO + off);
+                const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc2 = f2_fma(f2_pack(__uint_as_float(ow[e] << 16), __uint_as_float(ow[e] & 0xFFFF0000u)),
+                                  f2_pack(__uint_as_float(gw[e] << 16), __uint_as_float(gw[e] & 0xFFFF0000u)), acc2);
+            }
+            float lo, hi;
+            f2_unpack(acc2, lo, hi);
+            d_tilde = lo + hi;
+        }
+        mbar_arrive(bar(bars->o_free));     // the V producer may now overwrite the O tile
+        dred[h * 128 + r] = d_tilde;
+        named_barrier_sync(1, kRowThreads);
+        d_tilde += dred[(h ^ 1) * 128 + r];
+        named_barrier_sync(1, kRowThreads);     // dred is reused for the exact statistic
         const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
         const uint64_t nl22 = f2_pack(nl2, nl2);
         const uint64_t dt2 = f2_pack(d_tilde, d_tilde);
         uint64_t dacc2 = f2_pack(0.f, 0.f);
-        bool ok = true;
-        for (int j = 0; j < nk; ++j) {
+        for (int j = 0; j < nk && ok; ++j) {
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
@@ -737,13 +741,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 // ========================================================== launchers ====
-int launch_bwd_pre(const BwdArgs& a, cudaStream_t stream)
-{
-    const int64_t rows = (int64_t)a.c.n_bh * a.s_pad;
-    const unsigned grid = (unsigned)((rows + 7) / 8);
-    attn_bwd_pre_kernel<<<grid, 256, 0, stream>>>(a);
-    return (int)cudaGetLastError();
-}
 
 template <int D, bool DROP>
 static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -762,14 +759,14 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 template <int D, bool DROP>
 static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
+                       const CUtensorMap& to, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
 {
     constexpr uint32_t smem = DqCfg<D>::SMEM;
     auto kern = attn_bwd_dq_kernel<D, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned grid = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
-    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
     return (int)cudaGetLastError();
 }
 
@@ -792,12 +789,13 @@ int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMa
 }
 
 int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
+                  const CUtensorMap& tdo, const CUtensorMap& to, const CUtensorMap& tdq, const BwdArgs& a,
+                  cudaStream_t stream)
 {
 #define AC_DQ_CASE(DD)                                                                              \
     case DD:                                                                                        \
-        return dropout ? launch_dq_t<DD, true>(tq, tk, tv, tdo, tdq, a, stream)                     \
-                       : launch_dq_t<DD, false>(tq, tk, tv, tdo, tdq, a, stream);
+        return dropout ? launch_dq_t<DD, true>(tq, tk, tv, tdo, to, tdq, a, stream)                 \
+                       : launch_dq_t<DD, false>(tq, tk, tv, tdo, to, tdq, a, stream);
     switch (d) {
         AC_DQ_CASE(64)
         AC_DQ_CASE(96)

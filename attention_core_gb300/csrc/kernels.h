@@ -46,20 +46,20 @@ struct BwdArgs {
     const uint16_t* dout; // bf16 [b*h_q*s*d]
     const float* lse;     // [b*h_q*s]
     float* lse2_ws;       // [b*h_q*s_pad]  -LSE * log2(e); -inf past s
-    float* delta_ws;      // [b*h_q*s_pad]  row statistic D: rowsum(dO * O) from the
-                          // preprocess, replaced by sum_j P_ij dP_ij by the dQ kernel
+    float* delta_ws;      // [b*h_q*s_pad]  exact row statistic D = sum_j P_ij dP_ij
+                          // (written by the dQ kernel, read by the dK/dV kernel)
     int32_t d;
 };
 
 // Host launchers; return a cudaError_t value.
 int launch_fwd(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& to, const FwdArgs& a, cudaStream_t stream);
-int launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk,
                     const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
                     const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);
 int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream);
+                  const CUtensorMap& tdo, const CUtensorMap& to, const CUtensorMap& tdq, const BwdArgs& a,
+                  cudaStream_t stream);
 
 // Query-tile height of the dK/dV kernel for head dimension d (TMEM budget).
 constexpr int dkdv_query_tile(int d) { return (2 * d + 2 * 128 <= 512) ? 128 : 64; }

@@ -61,6 +61,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // Scale 32 fp32 accumulator columns [c0, c0 + 32) of row r, round to bf16
 // and write them into a staged [ROWS x D] output tile (TMA-store layout).
 template <int D, int ROWS>

@@ -2,8 +2,8 @@
 """Benchmark of the attention core under selective activation recomputation.
 
 One step = forward (S = QK^T with causal mask and scale, softmax, softmax
-dropout, O = P_d V, LSE) plus the recompute-backward (row statistics, dK/dV,
-dQ) over one batch of synthetic bf16 inputs of the named workload, through the
+dropout, O = P_d V, LSE) plus the recompute-backward (dQ with the row
+statistics, then dK/dV) over one batch of synthetic bf16 inputs of the named workload, through the
 library's C ABI.  Default workload: the GPT-3-style 175B layer, one
 tensor-parallel rank's shard (b=2, 12 local heads, s=2048, d_head=128,
 causal, p=0.1).
@@ -290,13 +290,14 @@ def run_ours(args, w):
         step(sets[i % n_sets])
     torch.cuda.synchronize(dev)
 
-    # per-kernel events: fwd, pre, dq, dkdv -> 8 events per step
+    # per-kernel events: fwd, dq, dkdv -> 6 events per step
     K = args.steps
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(8 * K)]
+    NE = 6
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(NE * K)]
     for e in evs:              # torch creates the CUDA event at its first record
         e.record(stream)
     torch.cuda.synchronize(dev)
-    ev_arr = (ctypes.c_void_p * (8 * K))(*[e.cuda_event for e in evs])
+    ev_arr = (ctypes.c_void_p * (NE * K))(*[e.cuda_event for e in evs])
     ev_base = ctypes.addressof(ev_arr)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
@@ -309,7 +310,7 @@ def run_ours(args, w):
     wall0 = time.perf_counter()
     t_start.record(stream)
     for i in range(K):
-        step(sets[i % n_sets], ev_base + 8 * i * ctypes.sizeof(ctypes.c_void_p))
+        step(sets[i % n_sets], ev_base + NE * i * ctypes.sizeof(ctypes.c_void_p))
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -324,14 +325,14 @@ def run_ours(args, w):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
 
-    names = ["fwd", "pre", "dq", "dkdv"]
+    names = ["fwd", "dq", "dkdv"]
     kt = {n: [] for n in names}
     for i in range(K):
         for j, n in enumerate(names):
-            kt[n].append(evs[8 * i + 2 * j].elapsed_time(evs[8 * i + 2 * j + 1]))
+            kt[n].append(evs[NE * i + 2 * j].elapsed_time(evs[NE * i + 2 * j + 1]))
     kavg = {n: sum(v) / len(v) for n, v in kt.items()}
     fwd_ms = kavg["fwd"]
-    bwd_ms = kavg["pre"] + kavg["dkdv"] + kavg["dq"]
+    bwd_ms = kavg["dkdv"] + kavg["dq"]
 
     pk = _peaks()
     total_units = fl["total"] * K * world
@@ -374,7 +375,7 @@ def run_ours(args, w):
                          "traffic": _traffic(kname, w["name"])},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 4 * K,
+            "gpu_launches": 3 * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

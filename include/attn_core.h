@@ -81,8 +81,8 @@ typedef struct {
     int32_t flags;              /* ATTN_CORE_FLAG_* */
     uint32_t wait_timeout_ms;   /* limit of each in-kernel wait; 0 selects 2000 ms */
     /* Optional profiling hook: an array of cudaEvent_t handles, two per
-     * kernel the call launches (fwd: 1 kernel; bwd: 3 kernels, in order
-     * row statistics, dQ, dK/dV), recorded on `stream` immediately before and
+     * kernel the call launches (fwd: 1 kernel; bwd: 2 kernels, in order
+     * dQ, dK/dV), recorded on `stream` immediately before and
      * after each launch.  May be NULL. */
     void** timing_events;
 } attn_core_params;
@@ -115,8 +115,8 @@ size_t attn_core_bwd_workspace_bytes(const attn_core_params* p);
  * and (seed, offset); the mask is bit-identical to the forward's.  The
  * softmax row statistic sum_j P_ij dP_ij is formed exactly from the
  * recomputed P and dP (a first estimate from the stored bf16 O is corrected
- * in fp32), not rounded through the stored output.  Launches three kernels
- * (row statistics, dQ, dK/dV).  `workspace` is caller-owned
+ * in fp32), not rounded through the stored output.  Launches two kernels
+ * (dQ with the row statistics, then dK/dV).  `workspace` is caller-owned
  * device memory of at least attn_core_bwd_workspace_bytes(p) bytes, 256-byte
  * aligned; its contents on entry do not matter.  dQ, dK, dV are written
  * whole (no accumulation into existing contents). */
