@@ -235,6 +235,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int key = kb * 128 + r;
         const uint32_t warp_key0 = (uint32_t)(kb * 128 + (int)(warp & 3u) * 32);
         const float* lse2_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
+        const KeepSwar ks(a.thr);
+        const uint32_t zs_bits = __float_as_uint(a.keep_scale);
         const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DEL);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
@@ -274,23 +276,19 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     pp[e] = f2_pack(lo, hi);
                 }
             }
-            uint32_t kw[HQ / 32];
+            // keep bytes of this lane's key over the half's queries (transposed draw)
+            uint32_t klo[HQ / 8], khi[HQ / 8];
             if (DROP) {
                 const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
-#pragma unroll
-                for (int v = 0; v < HQ / 32; ++v) kw[v] = keep_word_col(pk, warp_key0, (uint32_t)(q0 + 32 * v));
+                keep_bytes_col<HQ>(pk, ks, warp_key0 / 8u + lane / 8u, (uint32_t)q0, klo, khi);
             }
-            // dropout factor pair for queries 2e, 2e+1: zs where kept, 0 where dropped
-            auto zpair = [&](int e) -> uint64_t {
-                const int c = 2 * e;
-                return f2_pack(((kw[c >> 5] >> (c & 31)) & 1u) ? a.keep_scale : 0.f,
-                               ((kw[c >> 5] >> ((c + 1) & 31)) & 1u) ? a.keep_scale : 0.f);
-            };
-            // P_d^T = P^T * Z -> TMEM over the first HQ/2 of this half's S^T columns
+            // P^T masked by the keep mask (dropped entries +0) -> TMEM over the first HQ/2
+            // of this half's S^T columns; the factor 1/(1-p) is applied to dV at the end
             {
                 uint32_t pw[HQ / 2];
 #pragma unroll
-                for (int e = 0; e < HQ / 2; ++e) pw[e] = pack_bf16x2(DROP ? f2_mul(pp[e], zpair(e)) : pp[e]);
+                for (int e = 0; e < HQ / 2; ++e)
+                    pw[e] = DROP ? pack_bf16x2(pp[e]) & keep_pair_mask<HQ>(klo, khi, e) : pack_bf16x2(pp[e]);
                 if constexpr (HQ / 2 == 32) {
                     tmem_st32(tmem + C::T_S + lane_off + HQ * h, pw);
                 } else {
@@ -313,7 +311,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 for (int e = 0; e < 16; ++e) {
                     const int ep = c32 * 16 + e;
                     uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                    if (DROP) dp = f2_mul(dp, zpair(ep));
+                    if (DROP) {
+                        // dP = dP_d * Z: factor 1/(1-p) where kept, 0 where dropped
+                        const uint32_t m = keep_pair_mask<HQ>(klo, khi, ep);
+                        dp = f2_mul(dp, f2_pack(__uint_as_float(prmt(m, 0u, 0x9999u) & zs_bits),
+                                                __uint_as_float(prmt(m, 0u, 0xBBBBu) & zs_bits)));
+                    }
                     const float2 dl = dl2[ep];
                     w[e] = pack_bf16x2(f2_mul(pp[ep], f2_sub(dp, f2_pack(dl.x, dl.y))));
                 }
@@ -330,7 +333,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
-                stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, 1.0f);
+                stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, DROP ? a.keep_scale : 1.0f);
                 tmem_ld32(tmem + C::T_DK + lane_off + c32 * 32, rr);
                 stage_row32<D, 128>(sb + C::OFF_K, r, c32 * 32, rr, a.scale);
             }

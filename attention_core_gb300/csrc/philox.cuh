@@ -60,56 +60,92 @@ __device__ __forceinline__ uint64_t keep_factor2(uint32_t w, uint32_t t16, float
     return f2_pack((w << 16) >= t16 ? zs : 0.f, w >= t16 ? zs : 0.f);
 }
 
-// Keep bits of the eight keys 8*group .. 8*group+7 of one query row:
-// bit e is 1 iff key 8*group + e survives.
-__device__ __forceinline__ uint32_t keep_byte(const PhiloxKey& pk, uint32_t group, uint32_t query)
+// Byte permute (PRMT): result byte i is byte sel_i & 7 of {b, a} (a holds
+// bytes 0-3), or that byte's sign bit replicated when sel_i & 8.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
-    const uint4 w = philox4x32_10(group, query, pk.bh, pk.offset, pk.k0, pk.k1);
-    const uint32_t t = pk.thr;
-    uint32_t b = 0;
-    b |= (uint32_t)((w.x & 0xFFFFu) >= t) << 0;
-    b |= (uint32_t)((w.x >> 16) >= t) << 1;
-    b |= (uint32_t)((w.y & 0xFFFFu) >= t) << 2;
-    b |= (uint32_t)((w.y >> 16) >= t) << 3;
-    b |= (uint32_t)((w.z & 0xFFFFu) >= t) << 4;
-    b |= (uint32_t)((w.z >> 16) >= t) << 5;
-    b |= (uint32_t)((w.w & 0xFFFFu) >= t) << 6;
-    b |= (uint32_t)((w.w >> 16) >= t) << 7;
-    return b;
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
 }
 
-// Keep bits of 32 consecutive keys [32*blk32, 32*blk32 + 32) of one query
-// row (lanes are queries): bit c is key 32*blk32 + c.
-__device__ __forceinline__ uint32_t keep_word_row(const PhiloxKey& pk, uint32_t blk32, uint32_t query)
+// Both draws of a Philox output word against thr at once (SWAR): returns a
+// word whose bit 15 is "low draw kept" and bit 31 "high draw kept".  With
+// low15 the draw's low 15 bits, adding k = 0x8000 - thr (thr <= 0x8000) to
+// low15 carries into the half's top bit exactly when low15 >= thr, and a draw
+// with its own top bit set is kept as well (OR); for thr > 0x8000,
+// k = 0x10000 - thr and the draw's top bit is required (AND).  No half can
+// carry into the next.  kk = k replicated in both halves; f = all ones for
+// the OR case, 0 for the AND case (a bitwise majority picks between them).
+__device__ __forceinline__ uint32_t keep_swar(uint32_t w, uint32_t kk, uint32_t f)
 {
-    uint32_t m = 0;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) m |= keep_byte(pk, blk32 * 4 + g, query) << (8 * g);
-    return m;
+    const uint32_t d = (w & 0x7FFF7FFFu) + kk;
+    return (d & w) | (f & (d | w));
 }
+
+struct KeepSwar {
+    uint32_t kk, f;
+    __device__ __forceinline__ explicit KeepSwar(uint32_t thr)
+    {
+        const uint32_t k = thr <= 0x8000u ? 0x8000u - thr : 0x10000u - thr;
+        kk = k | (k << 16);
+        f = thr <= 0x8000u ? 0xFFFFFFFFu : 0u;
+    }
+};
 
 // Transposed orientation (lanes are keys).  The calling warp holds 32
-// consecutive keys starting at a multiple of 8 (lane L is key key0 + L).
-// Returns, for this lane's key, the keep bits of the 32 queries
-// [q0, q0 + 32): bit c is query q0 + c.  Each lane of an 8-lane group draws
-// the groups of four of the queries and the eight lanes swap bytes.
-__device__ __forceinline__ uint32_t keep_word_col(const PhiloxKey& pk, uint32_t key0, uint32_t q0)
+// consecutive keys starting at a multiple of 8 (lane L is key 8*group + t,
+// t = L & 7); the half-tile covers the HQ queries [q0, q0 + HQ).
+//
+// Lane t draws the Philox calls (group, q0 + 16*(u>>1) + 2t + (u&1)) for
+// u = 0 .. HQ/8-1; each call decides the group's 8 keys for one query.  The
+// keep decisions become byte sign bits (two words: keys 0-3, 4-7), and an
+// 8-lane butterfly of byte permutes (three shuffles) transposes each 8x8
+// block, so that afterwards, for this lane's key,
+//     byte t of (lo[u], hi[u]) has its sign bit set iff query
+//     q0 + 16*(u>>1) + 2t + (u&1) is kept.
+// The queries 2e and 2e+1 of a bf16 pair thus sit in bytes t = e & 7 of
+// blocks u = 2(e>>3) and u + 1 (see keep_pair_mask).
+template <int HQ>
+__device__ __forceinline__ void keep_bytes_col(const PhiloxKey& pk, const KeepSwar& ks, uint32_t group, uint32_t q0,
+                                               uint32_t (&lo)[HQ / 8], uint32_t (&hi)[HQ / 8])
 {
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t t = lane & 7;                   // this lane's key within its group of 8
-    const uint32_t group = (key0 + lane) >> 3;     // same for the 8 lanes
-    // byte u of w: keep bits (over the 8 keys) of query q0 + 8u + t
-    uint32_t w = 0;
+    static_assert(HQ % 16 == 0, "query half-tile must be a multiple of 16");
+    const uint32_t t = threadIdx.x & 7;
+    const bool b2 = t & 4, b1 = t & 2, b0 = t & 1;
+    // stage selectors (swap bytes whose index differs from the lane in bit 1 / bit 0)
+    const uint32_t s2_send = b1 ? 0x5410u : 0x7632u, s2_lo = b1 ? 0x3254u : 0x5410u, s2_hi = b1 ? 0x3276u : 0x7610u;
+    const uint32_t s1_send = b0 ? 0x6420u : 0x7531u, s1_lo = b0 ? 0x3514u : 0x5240u, s1_hi = b0 ? 0x3716u : 0x7260u;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) w |= keep_byte(pk, group, q0 + 8 * u + t) << (8 * u);
-    uint32_t m = 0;
-#pragma unroll
-    for (int src = 0; src < 8; ++src) {
-        const uint32_t x = __shfl_sync(0xffffffffu, w, (lane & ~7u) | (uint32_t)src);
-        // bit 8u + t of x is query q0 + 8u + src for this lane's key
-        m |= ((x >> t) & 0x01010101u) << src;
+    for (int u = 0; u < HQ / 8; ++u) {
+        const uint32_t q = q0 + 16u * (uint32_t)(u >> 1) + 2u * t + (uint32_t)(u & 1);
+        const uint4 w = philox4x32_10(group, q, pk.bh, pk.offset, pk.k0, pk.k1);
+        uint32_t l = prmt(keep_swar(w.x, ks.kk, ks.f), keep_swar(w.y, ks.kk, ks.f), 0x7531u);
+        uint32_t h = prmt(keep_swar(w.z, ks.kk, ks.f), keep_swar(w.w, ks.kk, ks.f), 0x7531u);
+        // bit 2: whole words
+        uint32_t r = __shfl_xor_sync(0xffffffffu, b2 ? l : h, 4);
+        if (b2) l = r; else h = r;
+        // bit 1: 16-bit halves
+        r = __shfl_xor_sync(0xffffffffu, prmt(l, h, s2_send), 2);
+        l = prmt(l, r, s2_lo);
+        h = prmt(h, r, s2_hi);
+        // bit 0: bytes
+        r = __shfl_xor_sync(0xffffffffu, prmt(l, h, s1_send), 1);
+        l = prmt(l, r, s1_lo);
+        h = prmt(h, r, s1_hi);
+        lo[u] = l;
+        hi[u] = h;
     }
-    return m;
+}
+
+// 16-bit lane mask of the query pair (2e, 2e+1) of the half-tile, for this
+// lane's key: low half 0xffff iff query 2e is kept, high half iff 2e+1 is.
+template <int HQ>
+__device__ __forceinline__ uint32_t keep_pair_mask(const uint32_t (&lo)[HQ / 8], const uint32_t (&hi)[HQ / 8], int e)
+{
+    const int a = e >> 3, t = e & 7, j = t & 3;
+    const uint32_t sel = (uint32_t)((8 | j) | ((8 | j) << 4) | ((12 | j) << 8) | ((12 | j) << 12));
+    return t < 4 ? prmt(lo[2 * a], lo[2 * a + 1], sel) : prmt(hi[2 * a], hi[2 * a + 1], sel);
 }
 
 }  // namespace ac
