@@ -33,7 +33,7 @@ namespace {
 
 enum : int32_t {
     kSiteInject = 1, kSiteKvFull, kSiteQEmpty, kSiteQFull, kSitePFull, kSiteDsFull, kSiteSFull,
-    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSiteSRead, kSiteOFull, kSiteOFree
+    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePRead, kSiteOFull, kSiteOFree
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
@@ -238,10 +238,20 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const KeepSwar ks(a.thr);
         const uint32_t zs_bits = __float_as_uint(a.keep_scale);
         const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DEL);
+        // Keep bytes of this lane's key over the half's queries (transposed draw).  Those
+        // of tile it + 1 are drawn right after tile it's dS, while the tensor core forms
+        // S_{it+1}: the draw needs no score.
+        uint32_t klo[HQ / 8], khi[HQ / 8];
+        auto draw_mask = [&](int it) {
+            const int bh = bh0 + it / per_head;
+            const int q0 = (qt0 + it % per_head) * BQ + HQ * h;
+            const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+            keep_bytes_col<HQ>(pk, ks, warp_key0 / 8u + lane / 8u, (uint32_t)q0, klo, khi);
+        };
+        if (DROP && n_it > 0) draw_mask(0);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int st = it % ST;
-            const int bh = bh0 + it / per_head;
             const int q0 = (qt0 + it % per_head) * BQ + HQ * h;     // this half's first query
             ok = __all_sync(0xffffffffu,
                             wait_bounded(wc, bar(bars->q_full[st]), (it / ST) & 1, timeout_code(kSiteQFull)));
@@ -275,12 +285,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     if (q0 + 2 * e + 1 < key) hi = 0.f;
                     pp[e] = f2_pack(lo, hi);
                 }
-            }
-            // keep bytes of this lane's key over the half's queries (transposed draw)
-            uint32_t klo[HQ / 8], khi[HQ / 8];
-            if (DROP) {
-                const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
-                keep_bytes_col<HQ>(pk, ks, warp_key0 / 8u + lane / 8u, (uint32_t)q0, klo, khi);
             }
             // P^T masked by the keep mask (dropped entries +0) -> TMEM over the first HQ/2
             // of this half's S^T columns; the factor 1/(1-p) is applied to dV at the end
@@ -325,6 +329,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->ds_full));
+            if (DROP && it + 1 < n_it) draw_mask(it + 1);
         }
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
         if (ok) {
@@ -396,7 +401,7 @@ struct DqCfg {
     static constexpr uint32_t OFF_O = OFF_V + VST * KT - QT;
     static constexpr int O_ST0 = (int)((VST * KT - QT) / KT);
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    // TMEM: S | dP (later dS~ in its first half, P in its second) | dQ~ | PK
+    // TMEM: S (later P in the first half of each row half) | dP (later dS~) | dQ~ | PK
     static constexpr uint32_t T_S = 0, T_DP = BN, T_DQ = 2 * BN, T_PK = 2 * BN + D;
     static_assert(T_PK + D <= 512, "TMEM budget");
 };
@@ -404,7 +409,7 @@ struct DqCfg {
 struct DqBars {
     uint64_t qdo_full;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full, s_read, dp_full, ds_full, acc_done;
+    uint64_t s_full, p_full, dp_full, ds_full, acc_done;
     uint64_t o_full, o_free;
     uint64_t never;
     uint32_t tmem_base;
@@ -451,7 +456,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(bar(bars->v_empty[st]), 1);
         }
         mbar_init(bar(bars->s_full), 1);
-        mbar_init(bar(bars->s_read), kRowThreads);
+        mbar_init(bar(bars->p_full), kRowThreads);
         mbar_init(bar(bars->dp_full), 1);
         mbar_init(bar(bars->ds_full), kRowThreads);
         mbar_init(bar(bars->acc_done), 1);
@@ -520,7 +525,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     } else if (alive && warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer.  Order: S0 dP0 | S1 dQ0 PK0 dP1 | S2 dQ1 PK1 dP2 | ...
+            // ---- MMA issuer.  Order: S0 dP0 | PK0 S1 dQ0 dP1 | PK1 S2 dQ1 dP2 | ...
+            // PK_j reads P_j from the S columns as soon as the row threads have
+            // stored it, so after dS_j only dQ_j and dP_{j+1} stand between the
+            // row threads and their next dS.
             constexpr uint32_t IDS = idesc_bf16(128, BN, false, false);  // S = Q K^T, dP_d = dO V^T
             constexpr uint32_t IDQ = idesc_bf16(128, D, false, true);    // dQ~ += dS~ K, PK += P K
             auto issue_s = [&](int j) -> bool {
@@ -552,24 +560,26 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (ok) ok = issue_s(0);
             if (ok) ok = issue_dp(0);
             for (int j = 0; j < nk && ok; ++j) {
+                const int st = j % KST;
+                const uint32_t kbase = sb + C::OFF_K + st * C::KT;
+                ok = wait_bounded(wc, bar(bars->p_full), j & 1, timeout_code(kSitePRead));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + C::T_PK, tmem + C::T_S + split_a_col(kk, BN), G::template desc_mn<BN>(kbase, kk), IDQ,
+                           (j > 0 || kk > 0) ? 1u : 0u);
                 if (j + 1 < nk) {
-                    ok = wait_bounded(wc, bar(bars->s_read), j & 1, timeout_code(kSiteSRead));
-                    if (ok) ok = issue_s(j + 1);
+                    ok = issue_s(j + 1);      // overwrites P_j: after PK_j in the tensor pipe
                     if (!ok) break;
                 }
                 ok = wait_bounded(wc, bar(bars->ds_full), j & 1, timeout_code(kSiteDsFull));
                 if (!ok) break;
                 tc_fence_after();
-                const int st = j % KST;
-                const uint32_t kbase = sb + C::OFF_K + st * C::KT;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bdesc = G::template desc_mn<BN>(kbase, kk);
-                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    const uint32_t acol = tmem + C::T_DP + split_a_col(kk, BN);
-                    mma_ts(tmem + C::T_DQ, acol, bdesc, IDQ, acc);
-                    mma_ts(tmem + C::T_PK, acol + BN / 4, bdesc, IDQ, acc);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + C::T_DQ, tmem + C::T_DP + split_a_col(kk, BN), G::template desc_mn<BN>(kbase, kk),
+                           IDQ, (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(bars->k_empty[st]));
                 if (j + 1 < nk) ok = issue_dp(j + 1);
             }
@@ -634,8 +644,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pp[c32 * 16 + e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
             }
-            tc_fence_before();
-            mbar_arrive(bar(bars->s_read));
             const int key0 = j * BN + HK * h;
 #pragma unroll
             for (int e = 0; e < HK / 2; ++e) {
@@ -653,6 +661,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
                 pp[e] = f2_pack(lo, hi);
             }
+            // P (before dropout) over the first HK/2 of this half's S columns, for PK += P K
+            {
+                uint32_t pw[HK / 2];
+#pragma unroll
+                for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(pp[e]);
+                if constexpr (HK / 2 == 32) {
+                    tmem_st32(tmem + C::T_S + lane_off + HK * h, pw);
+                } else {
+                    tmem_st16(tmem + C::T_S + lane_off + HK * h, pw);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(bars->p_full));
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
             tc_fence_after();
@@ -680,17 +702,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
-            }
-            // P (before dropout) after the dS~ words, inside this half's dP columns (all read by now)
-            {
-                uint32_t pw[HK / 2];
-#pragma unroll
-                for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(pp[e]);
-                if constexpr (HK / 2 == 32) {
-                    tmem_st32(tmem + C::T_DP + lane_off + HK * h + HK / 2, pw);
-                } else {
-                    tmem_st16(tmem + C::T_DP + lane_off + HK * h + HK / 2, pw);
-                }
             }
             tmem_st_wait();
             tc_fence_before();

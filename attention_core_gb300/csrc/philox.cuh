@@ -116,12 +116,17 @@ __device__ __forceinline__ void keep_bytes_col(const PhiloxKey& pk, const KeepSw
     // stage selectors (swap bytes whose index differs from the lane in bit 1 / bit 0)
     const uint32_t s2_send = b1 ? 0x5410u : 0x7632u, s2_lo = b1 ? 0x3254u : 0x5410u, s2_hi = b1 ? 0x3276u : 0x7610u;
     const uint32_t s1_send = b0 ? 0x6420u : 0x7531u, s1_lo = b0 ? 0x3514u : 0x5240u, s1_hi = b0 ? 0x3716u : 0x7260u;
+    // all Philox calls first (independent chains the scheduler can interleave)
+    uint4 w[HQ / 8];
 #pragma unroll
     for (int u = 0; u < HQ / 8; ++u) {
         const uint32_t q = q0 + 16u * (uint32_t)(u >> 1) + 2u * t + (uint32_t)(u & 1);
-        const uint4 w = philox4x32_10(group, q, pk.bh, pk.offset, pk.k0, pk.k1);
-        uint32_t l = prmt(keep_swar(w.x, ks.kk, ks.f), keep_swar(w.y, ks.kk, ks.f), 0x7531u);
-        uint32_t h = prmt(keep_swar(w.z, ks.kk, ks.f), keep_swar(w.w, ks.kk, ks.f), 0x7531u);
+        w[u] = philox4x32_10(group, q, pk.bh, pk.offset, pk.k0, pk.k1);
+    }
+#pragma unroll
+    for (int u = 0; u < HQ / 8; ++u) {
+        uint32_t l = prmt(keep_swar(w[u].x, ks.kk, ks.f), keep_swar(w[u].y, ks.kk, ks.f), 0x7531u);
+        uint32_t h = prmt(keep_swar(w[u].z, ks.kk, ks.f), keep_swar(w[u].w, ks.kk, ks.f), 0x7531u);
         // bit 2: whole words
         uint32_t r = __shfl_xor_sync(0xffffffffu, b2 ? l : h, 4);
         if (b2) l = r; else h = r;
