@@ -21,8 +21,8 @@
 //           domain (the halves swap their row maxima through shared memory),
 //           dropout from Philox, P_d written back to TMEM as bf16 inside the
 //           half's own score columns; epilogue O / l -> bf16 stored straight
-//           from registers (no staging buffer, so shared memory goes to
-//           deeper K/V rings).
+//           from registers (no staging buffer, so shared memory holds two
+//           Q tiles and the K/V rings).
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks skip the rescale; O / l is exact either way.
 #include "kernels.h"
@@ -41,10 +41,12 @@ struct FwdCfg {
     static constexpr uint32_t TILE = G::template tile_bytes<128>();
     static constexpr uint32_t CHUNK = G::template chunk_bytes<128>();
     // K and V rings: a block's load is issued when the block ST earlier has
-    // been consumed, so ST blocks of work must cover one TMA round trip.
-    static constexpr int ST = (D <= 64) ? 6 : (D <= 96 ? 4 : (D <= 128 ? 3 : 2));
-    static constexpr uint32_t OFF_Q = 0;                   // one Q tile
-    static constexpr uint32_t OFF_K = TILE;
+    // been consumed, so ST blocks of work must cover one TMA round trip.  Two Q
+    // buffers (where they fit) let the next tile's Q land during this tile.
+    static constexpr int NQ = (D <= 128) ? 2 : 1;
+    static constexpr int ST = (D <= 64) ? 6 : (D <= 96 ? 3 : 2);
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = NQ * TILE;
     static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
     static constexpr uint32_t OFF_BAR = OFF_V + ST * TILE;
     static constexpr uint32_t SMEM = OFF_BAR + 320 + 1024;
@@ -57,7 +59,7 @@ struct FwdCfg {
 };
 
 struct FwdBars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
     uint64_t s_full[2], p_full[2];
     uint64_t xmax[2];       // row-max exchange between the two column halves
@@ -116,8 +118,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(bars->q_full), 1);
-        mbar_init(bar(bars->q_empty), 1);            // the tile's last S MMA is done
+        for (int qs = 0; qs < 2; ++qs) {
+            mbar_init(bar(bars->q_full[qs]), 1);
+            mbar_init(bar(bars->q_empty[qs]), 1);    // the tile's last S MMA is done
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(bars->s_full[b]), 1);
             mbar_init(bar(bars->p_full[b]), kRowThreads);
@@ -182,10 +186,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int t = sched.tile(u);
                 if (t < 0) break;
                 const FwdTile w = fwd_tile(a, t);
-                if (!wait_bounded(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
-                mbar_arrive_expect_tx(bar(bars->q_full), C::TILE);
+                const int qs = u % C::NQ;
+                if (!wait_bounded(wc, bar(bars->q_empty[qs]), ((u / C::NQ) & 1) ^ 1, timeout_code(kSiteQEmpty)))
+                    break;
+                mbar_arrive_expect_tx(bar(bars->q_full[qs]), C::TILE);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_Q + ch * C::CHUNK, &tm_q, ch * G::CW, w.qb * 128, w.bh, bar(bars->q_full));
+                    tma_load_3d(sb + C::OFF_Q + qs * C::TILE + ch * C::CHUNK, &tm_q, ch * G::CW, w.qb * 128, w.bh,
+                                bar(bars->q_full[qs]));
             }
         }
     } else if (alive && warp == 2) {
@@ -249,20 +256,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // At a tile boundary the previous tile's last P.V goes first unless this
                 // tile's Q and first K block are already resident: it must never wait on
                 // this tile's loads.
-                if (prev.g >= 0 && (!mbar_test_wait(bar(bars->q_full), u & 1) ||
+                const int qs = u % C::NQ;
+                if (prev.g >= 0 && (!mbar_test_wait(bar(bars->q_full[qs]), (u / C::NQ) & 1) ||
                                     !mbar_test_wait(bar(bars->k_full[g % ST]), (g / ST) & 1))) {
                     ok = issue_pv(prev);
                     prev.g = -1;
                     if (!ok) break;
                 }
-                ok = wait_bounded(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
+                ok = wait_bounded(wc, bar(bars->q_full[qs]), (u / C::NQ) & 1, timeout_code(kSiteQFull));
                 for (int j = 0; j < w.nk && ok; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->k_full[st]), (g / ST) & 1, timeout_code(kSiteKFull));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
-                    const uint32_t qbase = sb + C::OFF_Q;
+                    const uint32_t qbase = sb + C::OFF_Q + qs * C::TILE;
                     const uint32_t tS = tmem + ((g & 1) ? C::T_S1 : C::T_S0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
@@ -270,7 +278,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                kk > 0 ? 1u : 0u);
                     mma_commit(bar(bars->k_empty[st]));
                     mma_commit(bar(bars->s_full[g & 1]));
-                    if (j == w.nk - 1) mma_commit(bar(bars->q_empty));
+                    if (j == w.nk - 1) mma_commit(bar(bars->q_empty[qs]));
                     if (prev.g >= 0) ok = issue_pv(prev);
                     prev = Blk{g, j, w.nk, u};
                 }
