@@ -43,13 +43,18 @@ struct FwdCfg {
     // K and V rings: a block's load is issued when the block ST earlier has
     // been consumed, so ST blocks of work must cover one TMA round trip.  Two Q
     // buffers (where they fit) let the next tile's Q land during this tile.
+    // O is staged in shared memory and written by one coalesced TMA store per
+    // tile where the stage fits (d <= 128); d = 160 stores rows from registers.
     static constexpr int NQ = (D <= 128) ? 2 : 1;
-    static constexpr int ST = (D <= 64) ? 6 : (D <= 96 ? 3 : 2);
+    static constexpr bool STAGE_O = (D <= 128);
+    static constexpr int ST = (D <= 64) ? 5 : (D <= 96 ? 3 : 2);
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = NQ * TILE;
     static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
-    static constexpr uint32_t OFF_BAR = OFF_V + ST * TILE;
-    static constexpr uint32_t SMEM = OFF_BAR + 320 + 1024;
+    static constexpr uint32_t OFF_OST = OFF_V + ST * TILE;
+    static constexpr uint32_t OFF_BAR = OFF_OST + (STAGE_O ? TILE : 0);
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM columns: two score buffers, the O accumulator, then six exchange
     // columns through which the two halves of a row swap their block maxima
@@ -67,15 +72,18 @@ struct FwdBars {
     uint64_t o_done, o_free;
     uint64_t o_tile;        // a tile's last P.V product is done (its O is final)
     uint64_t drain;         // every MMA of this CTA is done (before TMEM is released)
+    uint64_t ost_free;      // the O stage is free for this tile's rows (row threads)
+    uint64_t ost_full;      // this tile's rows are in the O stage (row threads)
     uint64_t never;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
+static_assert(sizeof(FwdBars) <= FwdCfg<64>::BAR_BYTES, "barrier block");
 
 // Wait sites reported in bits 8.. of the status word on a timeout.
 enum : int32_t {
     kSiteInject = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull, kSitePFull,
-    kSiteSFull, kSiteODone, kSiteXmax, kSiteQEmpty, kSiteOFree, kSiteLsum, kSiteOTile, kSiteDrain
+    kSiteSFull, kSiteODone, kSiteXmax, kSiteQEmpty, kSiteOFree, kSiteLsum, kSiteOTile, kSiteDrain, kSiteStage
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
@@ -131,6 +139,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(bar(bars->o_free), kRowThreads);
         mbar_init(bar(bars->o_tile), 1);
         mbar_init(bar(bars->drain), 1);
+        mbar_init(bar(bars->ost_free), kRowThreads);
+        mbar_init(bar(bars->ost_full), kRowThreads);
         for (int st = 0; st < ST; ++st) {
             mbar_init(bar(bars->k_full[st]), 1);
             mbar_init(bar(bars->k_empty[st]), 1);
@@ -431,10 +441,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok) break;
             tc_fence_after();
             const float inv = a.keep_scale / l_tot;
-            // O row i straight to global memory: 16-byte stores of this half's
-            // 32-column chunks.  The TMEM loads are warp-collective, so every
-            // lane takes them; only the stores are guarded (rows past s).
-            {
+            if constexpr (C::STAGE_O) {
+                // O / l -> bf16 into the stage, then one TMA store of the tile (rows past s
+                // are clipped by the tensor map).  The stage is reused only after the
+                // previous tile's store has read it.
+                if (h == 0 && r == 0) bulk_wait_read0();
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_free), u & 1, timeout_code(kSiteStage)));
+                if (!ok) break;
+#pragma unroll 1
+                for (int c32 = h; c32 < D / 32; c32 += 2) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + c32 * 32, rr);
+                    stage_row32<D, 128>(sb + C::OFF_OST, r, c32 * 32, rr, inv);
+                }
+                if (i < a.s && h == 0)
+                    args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+                fence_proxy_async_smem();
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_full), u & 1, timeout_code(kSiteStage)));
+                if (!ok) break;
+                if (h == 0 && r == 0 && !bars->abort_flag) {
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_store_3d(&tm_o, sb + C::OFF_OST + ch * C::CHUNK, ch * G::CW, qb * 128, bh);
+                    bulk_commit();
+                }
+            } else {
+                // O row i straight to global memory: 16-byte stores of this half's
+                // 32-column chunks.  The TMEM loads are warp-collective, so every
+                // lane takes them; only the stores are guarded (rows past s).
                 const bool live = i < a.s;
                 uint4* orow = reinterpret_cast<uint4*>(args.o + ((size_t)bh * a.s + (live ? i : 0)) * D);
 #pragma unroll 1
@@ -459,6 +492,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             pv_done += nk;
             g0 += nk;
         }
+        // the last tile's O store must have read the stage before the CTA exits
+        if (C::STAGE_O && h == 0 && r == 0) bulk_wait_read0();
     }
 
     __syncthreads();
