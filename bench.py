@@ -271,7 +271,8 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    def step(ts, ev_ptr=0):
+    def step(ts, ev_ptr=0, on=None):
+        sh = (on if on is not None else stream).cuda_stream
         pr.dev_status = status.data_ptr()
         pr.timing_events = ev_ptr
         rc = ac.attn_core_fwd(pr, ts["q"].data_ptr(), ts["k"].data_ptr(), ts["v"].data_ptr(),
@@ -290,9 +291,12 @@ def run_ours(args, w):
         step(sets[i % n_sets])
     torch.cuda.synchronize(dev)
 
-    # per-kernel events: fwd, dq, dkdv -> 6 events per step
+    # per-kernel events (fwd, dq, dkdv: 6 per timed step) on every EVERY-th step of
+    # the timed region: an event between two launches costs about 2 us of GPU
+    # time, so recording them on every step would slow the very loop they time
     K = args.steps
     NE = 6
+    EVERY = 4
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(NE * K)]
     for e in evs:              # torch creates the CUDA event at its first record
         e.record(stream)
@@ -310,7 +314,7 @@ def run_ours(args, w):
     wall0 = time.perf_counter()
     t_start.record(stream)
     for i in range(K):
-        step(sets[i % n_sets], ev_base + NE * i * ctypes.sizeof(ctypes.c_void_p))
+        step(sets[i % n_sets], ev_base + NE * i * ctypes.sizeof(ctypes.c_void_p) if i % EVERY == 0 else 0)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -327,7 +331,7 @@ def run_ours(args, w):
 
     names = ["fwd", "dq", "dkdv"]
     kt = {n: [] for n in names}
-    for i in range(K):
+    for i in range(0, K, EVERY):
         for j, n in enumerate(names):
             kt[n].append(evs[NE * i + 2 * j].elapsed_time(evs[NE * i + 2 * j + 1]))
     kavg = {n: sum(v) / len(v) for n, v in kt.items()}
@@ -341,6 +345,12 @@ def run_ours(args, w):
     dom_flops = fl["k_" + dom]
     achieved = dom_flops / (kavg[dom] / 1e3) / 1e12
     kname = {"fwd": "attn_fwd_kernel", "dkdv": "attn_bwd_dkdv_kernel", "dq": "attn_bwd_dq_kernel"}[dom]
+
+    # the same steps captured once into a CUDA graph and replayed (no per-kernel
+    # events: they cannot be captured)
+    graph = None
+    if not args.no_graph:
+        graph = _graph_replay(args, sets, step, n_sets, dev, fl, world, dist, status)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -375,13 +385,55 @@ def run_ours(args, w):
                          "traffic": _traffic(kname, w["name"])},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "cuda_graph": graph,
             "gpu_launches": 3 * K,
+            "kernel_ms_sampled": f"per-kernel events on every {EVERY}th timed step ({len(kt['fwd'])} samples)",
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def _graph_replay(args, sets, step, n_sets, dev, fl, world, dist, status):
+    """The timed loop's steps (one per rotating input set) captured once into a
+    CUDA graph and replayed, as a training loop that captures its step would run
+    them: the launches go back to back without host round trips.  Timed with
+    events on the replay stream around whole replays, inputs resident."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for i in range(n_sets):
+            step(sets[i], on=side)
+        side.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n_sets):
+                step(sets[i], on=side)
+        for _ in range(3):
+            g.replay()
+        side.synchronize()
+        reps = max(1, args.steps // n_sets)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        e0.record(side)
+        for _ in range(reps):
+            g.replay()
+        e1.record(side)
+        side.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} during the graph replays")
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    steps = reps * n_sets
+    return {"value": fl["total"] * steps * world / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "steps": steps, "ms_per_step": ms / steps, "gpu_launches": 3 * steps}
 
 
 def _e2e(args, w, pr, base, dev, stream, ws_bytes, fl, world, dist):
@@ -479,6 +531,7 @@ def main():
     ap.add_argument("--workload", default="gpt175b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay figure")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the CPU-oracle baseline sample")
     args = ap.parse_args()
