@@ -4,7 +4,7 @@
 // and the dropout seed/offset; the backward pass recomputes the scores,
 // probabilities and dropout mask on chip ("Reducing Activation Recomputation
 // in Large Transformer Models", Key takeaways, fourth bullet; "Recomputing
-// Activations": the scores are "recomputed during the backward pass").
+// Activations", second paragraph: the backward pass rebuilds the scores).
 // With Z = M / (1 - p) the gradients are
 //     dP_d = dO V^T,  dP = dP_d * Z,  dS = P * (dP - D),  D_i = rowsum(dO_i * O_i)
 //     dV = (P * Z)^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K

@@ -1,6 +1,6 @@
 // fwd.cu -- forward pass of the attention core on sm_103a.
 //
-// Computes, for one (query head, 128-query block) per CTA,
+// Computes, for every (query head, 128-query block) tile,
 //     S = scale * Q K^T  (causal: key j visible to query i iff j <= i),
 //     P = softmax(S) row-wise, P_d = P * M / (1 - p)  (softmax dropout),
 //     O = P_d V,  LSE_i = ln sum_j exp(S_ij),
@@ -10,19 +10,20 @@
 // Recomputation in Large Transformer Models", Key takeaways, fourth bullet;
 // "Recomputing Activations", "Memory for compute, selectively").
 //
-// Structure of a CTA (384 threads):
-//   warp 0  TMA: lane 0 the K ring, lane 1 each tile's Q as soon as the
-//           previous tile's last S MMA has read the Q buffer
+// Persistent: one CTA per SM walks its share of the tiles (sched.cuh), with
+// one MMA stream across tile boundaries.  Structure of a CTA (384 threads):
+//   warp 0  TMA: lane 0 the K ring over all blocks of all tiles, lane 1 each
+//           tile's Q into the free one of two Q buffers (one for d = 160)
 //   warp 2  TMA: V blocks into their own ring
 //   warp 1  one thread issues tcgen05 MMAs: S_j = Q K_j^T into one of two
 //           TMEM score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM
 //   warps 4-11  two warpgroups on the same 128 query rows (TMEM lanes), one
 //           per half of the 128 keys of a block: online softmax in the log2
-//           domain (the halves swap their row maxima through shared memory),
-//           dropout from Philox, P_d written back to TMEM as bf16 inside the
-//           half's own score columns; epilogue O / l -> bf16 stored straight
-//           from registers (no staging buffer, so shared memory holds two
-//           Q tiles and the K/V rings).
+//           domain (the halves swap their row maxima and sums through spare
+//           TMEM columns), dropout from Philox, P_d written back to TMEM as
+//           bf16 inside the half's own score columns; epilogue O / l -> bf16
+//           staged in shared memory and written by one TMA store per tile
+//           (d <= 128; d = 160 stores rows from registers)
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks skip the rescale; O / l is exact either way.
 #include "kernels.h"

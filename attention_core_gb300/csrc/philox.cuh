@@ -42,19 +42,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
     return make_uint4(c0, c1, c2, c3);
 }
 
-// Keep mask of the two keys a Philox output word decides (low half: the even
-// key, high half: the odd key), as 16-bit lane masks: 0xffff where the draw
-// is >= thr (kept), 0 where dropped.  t16 = thr << 16.  A high half is >= thr
-// exactly when the whole word is >= thr << 16; a low half when the word
-// shifted left by 16 is.
-__device__ __forceinline__ uint32_t keep_mask16x2(uint32_t w, uint32_t t16)
-{
-    return (w >= t16 ? 0xffff0000u : 0u) | ((w << 16) >= t16 ? 0x0000ffffu : 0u);
-}
-
 // Dropout factors of the two keys a Philox output word decides: z = zs where
 // the draw is >= thr (kept), 0 where dropped, packed (even key, odd key).
-// t16 = thr << 16 (see keep_mask16x2).
+// t16 = thr << 16: the high half is >= thr exactly when the whole word is
+// >= thr << 16, the low half when the word shifted left by 16 is.
 __device__ __forceinline__ uint64_t keep_factor2(uint32_t w, uint32_t t16, float zs)
 {
     return f2_pack((w << 16) >= t16 ? zs : 0.f, w >= t16 ? zs : 0.f);
