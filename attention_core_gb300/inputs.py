@@ -36,12 +36,15 @@ class Tensors:
     dout: torch.Tensor
 
 
-def random_inputs(b: int, h_q: int, h_kv: int, s: int, d: int, seed: int) -> Tensors:
-    """bf16 Q [b,h_q,s,d], K/V [b,h_kv,s,d], dO [b,h_q,s,d], all N(0,1), on the CPU."""
+def random_inputs(b: int, h_q: int, h_kv: int, s: int, d: int, seed: int, s_kv: int = 0) -> Tensors:
+    """bf16 Q [b,h_q,s,d], K/V [b,h_kv,s_kv,d], dO [b,h_q,s,d], all N(0,1), on the CPU.
+
+    s_kv = 0 means s_kv = s (self-attention)."""
+    s_kv = s_kv or s
     g = torch.Generator(device="cpu").manual_seed(int(seed))
     q = torch.randn((b, h_q, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    k = torch.randn((b, h_kv, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn((b, h_kv, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((b, h_kv, s_kv, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((b, h_kv, s_kv, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
     dout = torch.randn((b, h_q, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
     return Tensors(q, k, v, dout)
 

@@ -44,7 +44,7 @@ class _Params(ctypes.Structure):
                 ("s", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("p_drop", ctypes.c_float), ("scale", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
-                ("stored_o_bf16", ctypes.c_int32)]
+                ("stored_o_bf16", ctypes.c_int32), ("s_kv", ctypes.c_int32)]
 
 
 class _Bytes(ctypes.Structure):
@@ -102,11 +102,18 @@ class Problem:
     # way a method that stores only the bf16 output must form it.  False: the
     # exact definition.
     stored_o_bf16: bool = False
+    # Keys (and value rows) per KV head; 0 means s (self-attention).
+    s_kv: int = 0
+
+    @property
+    def keys(self) -> int:
+        return self.s_kv or self.s
 
     def _c(self) -> _Params:
         return _Params(self.b, self.h_q, self.h_kv, self.s, self.d, int(bool(self.causal)),
                        float(self.p_drop), float(self.scale), int(self.seed) & (2**64 - 1),
-                       int(self.offset) & (2**64 - 1), int(bool(self.stored_o_bf16)))
+                       int(self.offset) & (2**64 - 1), int(bool(self.stored_o_bf16)),
+                       int(self.s_kv))
 
 
 def _f64(x) -> np.ndarray:
@@ -177,31 +184,31 @@ def fwd_rows(pr: Problem, q, k, v, bh, rows):
 
 
 def head_matrices(pr: Problem, q, k, bh: int):
-    """Dense S, P (fp64, s x s) and keep mask M (uint8) of one query head."""
+    """Dense S, P (fp64, s x s_kv) and keep mask M (uint8) of one query head."""
     lib = _load()
     q, k = _f64(q), _f64(k)
-    S = np.zeros((pr.s, pr.s))
-    P = np.zeros((pr.s, pr.s))
-    M = np.zeros((pr.s, pr.s), dtype=np.uint8)
+    S = np.zeros((pr.s, pr.keys))
+    P = np.zeros((pr.s, pr.keys))
+    M = np.zeros((pr.s, pr.keys), dtype=np.uint8)
     lib.oracle_head_matrices(ctypes.byref(pr._c()), _dp(q), _dp(k), bh, _dp(S), _dp(P),
                              M.ctypes.data_as(_U8))
     return S, P, M
 
 
 def mask_rows(pr: Problem, bh: int, i0: int, i1: int) -> np.ndarray:
-    """Keep mask (uint8, rows [i0,i1) x s keys) of one query head; hidden keys are 0."""
-    M = np.zeros((i1 - i0, pr.s), dtype=np.uint8)
+    """Keep mask (uint8, rows [i0,i1) x s_kv keys) of one query head; hidden keys are 0."""
+    M = np.zeros((i1 - i0, pr.keys), dtype=np.uint8)
     _load().oracle_mask_rows(ctypes.byref(pr._c()), bh, i0, i1, M.ctypes.data_as(_U8))
     return M
 
 
 def bwd(pr: Problem, q, k, v, dout):
-    """Full backward: (dQ [b,h_q,s,d], dK [b,h_kv,s,d], dV [b,h_kv,s,d]), fp64."""
+    """Full backward: (dQ [b,h_q,s,d], dK [b,h_kv,s_kv,d], dV [b,h_kv,s_kv,d]), fp64."""
     lib = _load()
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     dq = np.zeros((pr.b, pr.h_q, pr.s, pr.d))
-    dk = np.zeros((pr.b, pr.h_kv, pr.s, pr.d))
-    dv = np.zeros((pr.b, pr.h_kv, pr.s, pr.d))
+    dk = np.zeros((pr.b, pr.h_kv, pr.keys, pr.d))
+    dv = np.zeros((pr.b, pr.h_kv, pr.keys, pr.d))
     lib.oracle_bwd(ctypes.byref(pr._c()), _dp(q), _dp(k), _dp(v), _dp(dout), _dp(dq), _dp(dk),
                    _dp(dv))
     return dq, dk, dv

@@ -20,6 +20,13 @@
  * LSE, top-left causal alignment, GQA head h -> h / (h_q/h_kv)) are listed in
  * the project's design notes and in the public ABI header.
  *
+ * Query and key counts: s queries and s_kv keys (s_kv = 0 means s).  The
+ * core's definition -- scores of every query against every visible key,
+ * softmax over the keys, dropout, weighted sum of the value rows -- does not
+ * need the two counts to be equal, so with s_kv != s the same functions give
+ * cross-attention.  Causal masking is top-left: query i sees keys
+ * 0 .. min(i, s_kv - 1).
+ *
  * Every function works in double precision.  Inputs arrive as doubles (the
  * caller widens bf16 exactly).  Work is split over rows or heads with OpenMP;
  * there is no blocking, fusion or reordering beyond that.
@@ -50,6 +57,7 @@ typedef struct {
     uint64_t seed;      /* Philox key */
     uint64_t offset;    /* Philox stream offset, < 2^32 */
     int32_t stored_o_bf16; /* backward row statistic from the bf16-stored output (see below) */
+    int32_t s_kv;       /* keys (and value rows) per KV head; 0 means s */
 } oracle_params;
 
 /* ------------------------------------------------------------------------
@@ -133,10 +141,18 @@ double oracle_resolved_scale(const oracle_params* p)
     return (double)sc;
 }
 
-/* Number of keys query i may attend to. */
+/* Keys per KV head. */
+static int64_t n_keys(const oracle_params* p)
+{
+    return p->s_kv > 0 ? (int64_t)p->s_kv : (int64_t)p->s;
+}
+
+/* Number of keys query i may attend to (keys 0 .. visible_keys - 1). */
 static int64_t visible_keys(const oracle_params* p, int64_t i)
 {
-    return p->causal ? (i + 1) : (int64_t)p->s;
+    const int64_t sk = n_keys(p);
+    if (!p->causal) return sk;
+    return i + 1 < sk ? i + 1 : sk;
 }
 
 /* KV head used by flattened query head bh. */
@@ -163,19 +179,19 @@ static double round_bf16(double x)
 /* One query row of the core: scores S_ij = scale * q_i . k_j for visible j
  * (masked keys are -inf and are simply not formed: exp(-inf) = 0 exactly),
  * the softmax P_ij = exp(S_ij - m_i) / l_i, the dropout factors Z_ij, and
- * LSE_i = m_i + ln l_i.  S, P, Z have room for s entries; entries past the
+ * LSE_i = m_i + ln l_i.  S, P, Z have room for s_kv entries; entries past the
  * visible keys are set to -inf, 0 and 0. */
 static void core_row(const oracle_params* p, const double* q, const double* k,
                      int64_t bh, int64_t i, double* S, double* P, double* Z, double* lse)
 {
-    const int64_t s = p->s, d = p->d;
+    const int64_t s = p->s, d = p->d, sk = n_keys(p);
     const double scale = oracle_resolved_scale(p);
     const double zs = keep_scale(p);
     const double* qi = q + (bh * s + i) * d;
-    const double* kh = k + kv_head_of(p, bh) * s * d;
+    const double* kh = k + kv_head_of(p, bh) * sk * d;
     const int64_t nk = visible_keys(p, i);
     double m = -INFINITY;
-    for (int64_t j = 0; j < s; ++j) {
+    for (int64_t j = 0; j < sk; ++j) {
         if (j < nk) {
             double acc = 0.0;
             for (int64_t c = 0; c < d; ++c) acc += qi[c] * kh[j * d + c];
@@ -187,7 +203,7 @@ static void core_row(const oracle_params* p, const double* q, const double* k,
     }
     double l = 0.0;
     for (int64_t j = 0; j < nk; ++j) l += exp(S[j] - m);
-    for (int64_t j = 0; j < s; ++j) {
+    for (int64_t j = 0; j < sk; ++j) {
         if (j < nk) {
             P[j] = exp(S[j] - m) / l;
             Z[j] = oracle_keep(p, bh, i, j) ? zs : 0.0;
@@ -205,20 +221,20 @@ void oracle_fwd_rows(const oracle_params* p, const double* q, const double* k, c
                      int64_t n, const int64_t* bh_list, const int64_t* row_list,
                      double* o, double* lse)
 {
-    const int64_t s = p->s, d = p->d;
+    const int64_t d = p->d, sk = n_keys(p);
 #pragma omp parallel
     {
-        double* S = (double*)malloc(sizeof(double) * s);
-        double* P = (double*)malloc(sizeof(double) * s);
-        double* Z = (double*)malloc(sizeof(double) * s);
+        double* S = (double*)malloc(sizeof(double) * sk);
+        double* P = (double*)malloc(sizeof(double) * sk);
+        double* Z = (double*)malloc(sizeof(double) * sk);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t r = 0; r < n; ++r) {
             int64_t bh = bh_list[r], i = row_list[r];
             core_row(p, q, k, bh, i, S, P, Z, &lse[r]);
-            const double* vh = v + kv_head_of(p, bh) * s * d;
+            const double* vh = v + kv_head_of(p, bh) * sk * d;
             double* oi = o + r * d;
             for (int64_t c = 0; c < d; ++c) oi[c] = 0.0;
-            for (int64_t j = 0; j < s; ++j) {
+            for (int64_t j = 0; j < sk; ++j) {
                 double w = P[j] * Z[j];
                 if (w == 0.0) continue;
                 for (int64_t c = 0; c < d; ++c) oi[c] += w * vh[j * d + c];
@@ -241,46 +257,46 @@ void oracle_fwd(const oracle_params* p, const double* q, const double* k, const 
 }
 
 /* Dense matrices of one query head (for self-tests): S, P and the 0/1 keep
- * mask M, each s*s, row-major (query, key). */
+ * mask M, each s*s_kv, row-major (query, key). */
 void oracle_head_matrices(const oracle_params* p, const double* q, const double* k, int64_t bh,
                           double* S, double* P, uint8_t* M)
 {
-    const int64_t s = p->s;
-    double* Z = (double*)malloc(sizeof(double) * s);
+    const int64_t s = p->s, sk = n_keys(p);
+    double* Z = (double*)malloc(sizeof(double) * sk);
     for (int64_t i = 0; i < s; ++i) {
-        core_row(p, q, k, bh, i, S + i * s, P + i * s, Z, NULL);
-        for (int64_t j = 0; j < s; ++j)
-            M[i * s + j] = (uint8_t)((j < visible_keys(p, i)) ? oracle_keep(p, bh, i, j) : 0);
+        core_row(p, q, k, bh, i, S + i * sk, P + i * sk, Z, NULL);
+        for (int64_t j = 0; j < sk; ++j)
+            M[i * sk + j] = (uint8_t)((j < visible_keys(p, i)) ? oracle_keep(p, bh, i, j) : 0);
     }
     free(Z);
 }
 
-/* Keep mask of one query head for rows [i0, i1), all s keys, row-major;
+/* Keep mask of one query head for rows [i0, i1), all s_kv keys, row-major;
  * keys a causal mask hides are reported as 0. */
 void oracle_mask_rows(const oracle_params* p, int64_t bh, int64_t i0, int64_t i1, uint8_t* M)
 {
-    const int64_t s = p->s;
+    const int64_t sk = n_keys(p);
 #pragma omp parallel for schedule(static)
     for (int64_t i = i0; i < i1; ++i)
-        for (int64_t j = 0; j < s; ++j)
-            M[(i - i0) * s + j] = (uint8_t)((j < visible_keys(p, i)) ? oracle_keep(p, bh, i, j) : 0);
+        for (int64_t j = 0; j < sk; ++j)
+            M[(i - i0) * sk + j] = (uint8_t)((j < visible_keys(p, i)) ? oracle_keep(p, bh, i, j) : 0);
 }
 
 /* Backward quantities of one query row, given the upstream gradient dO:
  *   dPd_ij = dO_i . v_j        (gradient w.r.t. the dropped-out probabilities)
  *   dP_ij  = dPd_ij * Z_ij     (through the dropout)
  *   dS_ij  = P_ij (dP_ij - sum_k P_ik dP_ik)   (through the softmax)
- * dS has room for s entries (zero past the visible keys). */
+ * dS has room for s_kv entries (zero past the visible keys). */
 static void core_row_grad(const oracle_params* p, const double* v, const double* dout,
                           int64_t bh, int64_t i, const double* P, const double* Z, double* dS,
                           double* rowdot_out)
 {
-    const int64_t s = p->s, d = p->d;
-    const double* vh = v + kv_head_of(p, bh) * s * d;
+    const int64_t s = p->s, d = p->d, sk = n_keys(p);
+    const double* vh = v + kv_head_of(p, bh) * sk * d;
     const double* gi = dout + (bh * s + i) * d;
     const int64_t nk = visible_keys(p, i);
     double rowdot = 0.0;
-    for (int64_t j = 0; j < s; ++j) {
+    for (int64_t j = 0; j < sk; ++j) {
         if (j < nk) {
             double acc = 0.0;
             for (int64_t c = 0; c < d; ++c) acc += gi[c] * vh[j * d + c];
@@ -311,23 +327,23 @@ void oracle_dq_rows(const oracle_params* p, const double* q, const double* k, co
                     const double* dout, int64_t n, const int64_t* bh_list, const int64_t* row_list,
                     double* dq)
 {
-    const int64_t s = p->s, d = p->d;
+    const int64_t d = p->d, sk = n_keys(p);
     const double scale = oracle_resolved_scale(p);
 #pragma omp parallel
     {
-        double* S = (double*)malloc(sizeof(double) * s);
-        double* P = (double*)malloc(sizeof(double) * s);
-        double* Z = (double*)malloc(sizeof(double) * s);
-        double* dS = (double*)malloc(sizeof(double) * s);
+        double* S = (double*)malloc(sizeof(double) * sk);
+        double* P = (double*)malloc(sizeof(double) * sk);
+        double* Z = (double*)malloc(sizeof(double) * sk);
+        double* dS = (double*)malloc(sizeof(double) * sk);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t r = 0; r < n; ++r) {
             int64_t bh = bh_list[r], i = row_list[r];
             core_row(p, q, k, bh, i, S, P, Z, NULL);
             core_row_grad(p, v, dout, bh, i, P, Z, dS, NULL);
-            const double* kh = k + kv_head_of(p, bh) * s * d;
+            const double* kh = k + kv_head_of(p, bh) * sk * d;
             double* gq = dq + r * d;
             for (int64_t c = 0; c < d; ++c) gq[c] = 0.0;
-            for (int64_t j = 0; j < s; ++j) {
+            for (int64_t j = 0; j < sk; ++j) {
                 if (dS[j] == 0.0) continue;
                 for (int64_t c = 0; c < d; ++c) gq[c] += dS[j] * kh[j * d + c];
             }
@@ -347,7 +363,7 @@ void oracle_dkdv_rows(const oracle_params* p, const double* q, const double* k, 
                       const double* dout, int64_t n, const int64_t* bkv_list, const int64_t* row_list,
                       double* dk, double* dv)
 {
-    const int64_t s = p->s, d = p->d;
+    const int64_t s = p->s, d = p->d, sk = n_keys(p);
     const int64_t group = p->h_q / p->h_kv;
     const int64_t nbh = (int64_t)p->b * p->h_q;
     const double scale = oracle_resolved_scale(p);
@@ -377,10 +393,10 @@ void oracle_dkdv_rows(const oracle_params* p, const double* q, const double* k, 
     double* rdot_all = (double*)malloc(sizeof(double) * nbh * s);
 #pragma omp parallel
     {
-        double* S = (double*)malloc(sizeof(double) * s);
-        double* P = (double*)malloc(sizeof(double) * s);
-        double* Z = (double*)malloc(sizeof(double) * s);
-        double* dS = (double*)malloc(sizeof(double) * s);
+        double* S = (double*)malloc(sizeof(double) * sk);
+        double* P = (double*)malloc(sizeof(double) * sk);
+        double* Z = (double*)malloc(sizeof(double) * sk);
+        double* dS = (double*)malloc(sizeof(double) * sk);
 #pragma omp for schedule(dynamic, 4)
         for (int64_t t = 0; t < ntask; ++t) {
             int64_t bh = task_bh[t], i = task_i[t];
@@ -394,8 +410,8 @@ void oracle_dkdv_rows(const oracle_params* p, const double* q, const double* k, 
     for (int64_t r = 0; r < n; ++r) {
         int64_t bkv = bkv_list[r], j = row_list[r];
         int64_t bi = bkv / p->h_kv, hk = bkv % p->h_kv;
-        const double* kj = k + (bkv * s + j) * d;
-        const double* vj = v + (bkv * s + j) * d;
+        const double* kj = k + (bkv * sk + j) * d;
+        const double* vj = v + (bkv * sk + j) * d;
         double* gk = dk + r * d;
         double* gv = dv + r * d;
         for (int64_t c = 0; c < d; ++c) { gk[c] = 0.0; gv[c] = 0.0; }
@@ -421,30 +437,30 @@ void oracle_dkdv_rows(const oracle_params* p, const double* q, const double* k, 
     free(first); free(task_bh); free(task_i); free(lse_all); free(rdot_all);
 }
 
-/* Full backward: dQ [b, h_q, s, d], dK and dV [b, h_kv, s, d].  One KV head
- * per task: every query row of its group is formed once and its dS row is
- * scattered into dK and dV. */
+/* Full backward: dQ [b, h_q, s, d], dK and dV [b, h_kv, s_kv, d].  One KV
+ * head per task: every query row of its group is formed once and its dS row
+ * is scattered into dK and dV. */
 void oracle_bwd(const oracle_params* p, const double* q, const double* k, const double* v,
                 const double* dout, double* dq, double* dk, double* dv)
 {
-    const int64_t s = p->s, d = p->d;
+    const int64_t s = p->s, d = p->d, sk = n_keys(p);
     const int64_t group = p->h_q / p->h_kv;
     const int64_t n_kv = (int64_t)p->b * p->h_kv;
     const double scale = oracle_resolved_scale(p);
 #pragma omp parallel
     {
-        double* S = (double*)malloc(sizeof(double) * s);
-        double* P = (double*)malloc(sizeof(double) * s);
-        double* Z = (double*)malloc(sizeof(double) * s);
-        double* dS = (double*)malloc(sizeof(double) * s);
+        double* S = (double*)malloc(sizeof(double) * sk);
+        double* P = (double*)malloc(sizeof(double) * sk);
+        double* Z = (double*)malloc(sizeof(double) * sk);
+        double* dS = (double*)malloc(sizeof(double) * sk);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t bkv = 0; bkv < n_kv; ++bkv) {
             int64_t bi = bkv / p->h_kv, hk = bkv % p->h_kv;
-            const double* kh = k + bkv * s * d;
-            double* gkh = dk + bkv * s * d;
-            double* gvh = dv + bkv * s * d;
-            memset(gkh, 0, sizeof(double) * s * d);
-            memset(gvh, 0, sizeof(double) * s * d);
+            const double* kh = k + bkv * sk * d;
+            double* gkh = dk + bkv * sk * d;
+            double* gvh = dv + bkv * sk * d;
+            memset(gkh, 0, sizeof(double) * sk * d);
+            memset(gvh, 0, sizeof(double) * sk * d);
             for (int64_t g = 0; g < group; ++g) {
                 int64_t bh = bi * p->h_q + hk * group + g;
                 for (int64_t i = 0; i < s; ++i) {
@@ -477,24 +493,27 @@ void oracle_bwd(const oracle_params* p, const double* q, const double* k, const 
  * the local hidden size h = a * d_head (one rank's shard), H the local head
  * count a and T the sequence length s, so a layer of s*b tokens holds
  * sbh(34 + 5as/h) bytes -- the form the anthology page's takeaways quote.
+ * The layer terms describe a self-attention layer of s tokens; the core terms
+ * count the actual tensors, with s_kv keys: 5 a s s_kv b score bytes avoided
+ * and bf16 Q, O (s rows) and K, V (s_kv rows) kept.
  * ---------------------------------------------------------------------- */
 typedef struct {
     int64_t layer_none;           /* 34 s b h + 5 a s^2 b */
     int64_t layer_selective;      /* 34 s b h */
     int64_t layer_full;           /* 2 s b h */
-    int64_t core_scores_avoided;  /* 5 a s^2 b */
+    int64_t core_scores_avoided;  /* 5 a s s_kv b */
     int64_t core_kept;            /* bf16 Q, K, V and O actually kept */
     int64_t core_recompute_state; /* fp32 LSE per query row + seed + offset */
 } oracle_bytes;
 
 void oracle_stored_bytes(const oracle_params* p, oracle_bytes* out)
 {
-    const int64_t s = p->s, b = p->b, a = p->h_q, akv = p->h_kv, dh = p->d;
+    const int64_t s = p->s, sk = n_keys(p), b = p->b, a = p->h_q, akv = p->h_kv, dh = p->d;
     const int64_t h = a * dh;
     out->layer_selective = 34 * s * b * h;
-    out->core_scores_avoided = 5 * a * s * s * b;
-    out->layer_none = out->layer_selective + out->core_scores_avoided;
+    out->layer_none = out->layer_selective + 5 * a * s * s * b;
     out->layer_full = 2 * s * b * h;
-    out->core_kept = 2 * s * dh * b * (2 * a + 2 * akv);
+    out->core_scores_avoided = 5 * a * s * sk * b;
+    out->core_kept = 2 * dh * b * (2 * a * s + 2 * akv * sk);
     out->core_recompute_state = 4 * b * a * s + 16;
 }

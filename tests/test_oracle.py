@@ -149,6 +149,18 @@ def test_stored_bytes_layer_formula_and_core_terms():
     assert sb["core_recompute_state"] == 4 * b * a * s + 16
 
 
+def test_stored_bytes_cross_attention_core_terms():
+    """With s_kv keys the core avoids 5 a s s_kv b score bytes and keeps Q, O
+    (s rows) and K, V (s_kv rows); the layer terms stay those of s tokens."""
+    s, skv, b, a, akv, d = 512, 1536, 3, 8, 2, 64
+    sq = oracle.stored_bytes(oracle.Problem(b=b, h_q=a, h_kv=akv, s=s, d=d))
+    sx = oracle.stored_bytes(oracle.Problem(b=b, h_q=a, h_kv=akv, s=s, d=d, s_kv=skv))
+    assert sx["core_scores_avoided"] == 5 * a * s * skv * b
+    assert sx["core_kept"] == 2 * b * d * (2 * a * s + 2 * akv * skv)
+    for name in ("layer_none", "layer_selective", "layer_full", "core_recompute_state"):
+        assert sx[name] == sq[name], name
+
+
 # ------------------------------------------------------ softmax invariants -
 
 def test_softmax_rows_and_lse():
@@ -182,7 +194,7 @@ def _torch_reference(t, pr, z=None):
         vv = v.repeat_interleave(g, dim=1)
         s = (q @ kk.transpose(-1, -2)) * scale
         if pr.causal:
-            s = s.masked_fill(torch.triu(torch.ones(pr.s, pr.s, dtype=torch.bool), 1), -math.inf)
+            s = s.masked_fill(torch.triu(torch.ones(pr.s, pr.keys, dtype=torch.bool), 1), -math.inf)
         o = (torch.softmax(s, dim=-1) * z) @ vv
     o.backward(t.dout.double())
     return o.detach().numpy(), q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
@@ -199,6 +211,65 @@ def test_p0_equals_textbook_attention(causal, shape):
     ro, rdq, rdk, rdv = _torch_reference(t, pr)
     for a, r in ((o, ro), (dq, rdq), (dk, rdk), (dv, rdv)):
         assert np.max(np.abs(a - r)) < 1e-11
+
+
+# (b, h_q, h_kv, s queries, s_kv keys, d)
+CROSS_SHAPES = [(1, 2, 2, 21, 37, 16), (2, 4, 2, 30, 9, 8), (1, 2, 1, 1, 19, 8)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", CROSS_SHAPES)
+def test_p0_cross_attention_equals_textbook(causal, shape):
+    """s_kv != s: textbook attention of s queries over s_kv keys (torch's causal
+    mask for unequal lengths is also top-left aligned)."""
+    b, hq, hkv, s, skv, d = shape
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=causal, s_kv=skv)
+    t = random_inputs(b, hq, hkv, s, d, seed=21, s_kv=skv)
+    assert tuple(t.k.shape) == (b, hkv, skv, d) and tuple(t.q.shape) == (b, hq, s, d)
+    o, lse = oracle.fwd(pr, t.q, t.k, t.v)
+    dq, dk, dv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    ro, rdq, rdk, rdv = _torch_reference(t, pr)
+    for a, r in ((o, ro), (dq, rdq), (dk, rdk), (dv, rdv)):
+        assert a.shape == r.shape
+        assert np.max(np.abs(a - r)) < 1e-11
+    # LSE against its definition, straight from the inputs
+    q, k = t.q.double(), t.k.double()
+    g = hq // hkv
+    sc = (q @ k.repeat_interleave(g, dim=1).transpose(-1, -2)) * oracle.resolved_scale(pr)
+    if causal:
+        sc = sc.masked_fill(torch.triu(torch.ones(s, skv, dtype=torch.bool), 1), -math.inf)
+    assert np.max(np.abs(lse - torch.logsumexp(sc, dim=-1).numpy())) < 1e-12
+
+
+@pytest.mark.parametrize("shape", CROSS_SHAPES[:2])
+def test_cross_attention_dropout_matches_autograd_with_oracle_mask(shape):
+    b, hq, hkv, s, skv, d = shape
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=False, p_drop=0.3,
+                        seed=77, offset=4, s_kv=skv)
+    t = random_inputs(b, hq, hkv, s, d, seed=22, s_kv=skv)
+    p_eff = oracle.drop_threshold(0.3) / 65536
+    z = np.zeros((b, hq, s, skv))
+    for bh in range(b * hq):
+        m = oracle.mask_rows(pr, bh, 0, s)
+        assert m.shape == (s, skv)
+        z[bh // hq, bh % hq] = m / (1 - p_eff)
+    assert 0 < (z == 0).sum() < z.size
+    o, _ = oracle.fwd(pr, t.q, t.k, t.v)
+    dq, dk, dv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    ro, rdq, rdk, rdv = _torch_reference(t, pr, torch.from_numpy(z))
+    for a, r in ((o, ro), (dq, rdq), (dk, rdk), (dv, rdv)):
+        assert np.max(np.abs(a - r)) < 1e-11
+
+
+def test_cross_attention_mask_is_the_self_attention_mask():
+    """The keep decision of (i, j) depends only on (seed, offset, head, i, j),
+    not on how many queries or keys the call has."""
+    base = dict(b=1, h_q=2, h_kv=2, d=16, p_drop=0.3, seed=5, offset=2, causal=False)
+    m_sq = oracle.mask_rows(oracle.Problem(s=40, **base), 1, 0, 40)
+    m_x = oracle.mask_rows(oracle.Problem(s=25, s_kv=40, **base), 1, 0, 25)
+    m_y = oracle.mask_rows(oracle.Problem(s=40, s_kv=13, **base), 1, 0, 40)
+    assert (m_x == m_sq[:25]).all()
+    assert (m_y == m_sq[:, :13]).all()
 
 
 def test_p0_custom_scale():
@@ -259,6 +330,35 @@ def test_gradients_by_central_differences():
         assert err < 1e-7, (name, err)
 
 
+def test_cross_attention_gradients_by_central_differences():
+    b, hq, hkv, s, skv, d = 1, 2, 1, 6, 11, 8
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=False, p_drop=0.3, seed=98,
+                        s_kv=skv)
+    t = random_inputs(b, hq, hkv, s, d, seed=23, s_kv=skv)
+    q, k, v = (x.double().numpy().copy() for x in (t.q, t.k, t.v))
+    g = t.dout.double().numpy()
+    dq, dk, dv = oracle.bwd(pr, q, k, v, g)
+
+    def loss(qq, kk, vv):
+        return float((oracle.fwd(pr, qq, kk, vv)[0] * g).sum())
+
+    h = 1e-4
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            orig = x[idx]
+            x[idx] = orig + h
+            lp = loss(q, k, v)
+            x[idx] = orig - h
+            lm = loss(q, k, v)
+            x[idx] = orig
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.max(np.abs(fd - grad)) / max(np.max(np.abs(grad)), 1e-30)
+        assert err < 1e-7, (name, err)
+
+
 # -------------------------------------------------- sampled-row entry points
 
 def test_sampled_rows_agree_with_full():
@@ -281,6 +381,27 @@ def test_sampled_rows_agree_with_full():
         sdk, sdv = oracle.dkdv_rows(pr, t.q, t.k, t.v, t.dout, bkv, krows)
         assert np.max(np.abs(sdk - dk.reshape(-1, s, d)[bkv, krows])) < 1e-12
         assert np.max(np.abs(sdv - dv.reshape(-1, s, d)[bkv, krows])) < 1e-12
+
+
+def test_sampled_rows_agree_with_full_cross_attention():
+    b, hq, hkv, s, skv, d = 1, 4, 2, 50, 83, 16
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=False, p_drop=0.15, seed=8,
+                        s_kv=skv)
+    t = random_inputs(b, hq, hkv, s, d, seed=24, s_kv=skv)
+    o, lse = oracle.fwd(pr, t.q, t.k, t.v)
+    dq, dk, dv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    bh = np.array([0, 1, 3, 2])
+    rows = np.array([0, 49, 33, 5])
+    so, slse = oracle.fwd_rows(pr, t.q, t.k, t.v, bh, rows)
+    sdq = oracle.dq_rows(pr, t.q, t.k, t.v, t.dout, bh, rows)
+    assert np.max(np.abs(so - o.reshape(-1, s, d)[bh, rows])) < 1e-12
+    assert np.max(np.abs(slse - lse.reshape(-1, s)[bh, rows])) < 1e-12
+    assert np.max(np.abs(sdq - dq.reshape(-1, s, d)[bh, rows])) < 1e-12
+    bkv = np.array([0, 1, 1])
+    krows = np.array([0, 82, 60])
+    sdk, sdv = oracle.dkdv_rows(pr, t.q, t.k, t.v, t.dout, bkv, krows)
+    assert np.max(np.abs(sdk - dk.reshape(-1, skv, d)[bkv, krows])) < 1e-12
+    assert np.max(np.abs(sdv - dv.reshape(-1, skv, d)[bkv, krows])) < 1e-12
 
 
 def test_sampled_rows_p0_against_textbook():
