@@ -53,7 +53,8 @@ class _CParams(ctypes.Structure):
                 ("p_drop", ctypes.c_float), ("scale", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
                 ("dev_status", ctypes.c_void_p), ("flags", ctypes.c_int32),
-                ("wait_timeout_ms", ctypes.c_uint32), ("timing_events", ctypes.c_void_p)]
+                ("wait_timeout_ms", ctypes.c_uint32), ("timing_events", ctypes.c_void_p),
+                ("s_kv", ctypes.c_int32)]
 
 
 class _CBytes(ctypes.Structure):
@@ -79,12 +80,17 @@ class Params:
     flags: int = 0
     wait_timeout_ms: int = 0
     timing_events: int = 0       # address of a void*[2 * n_kernels] array, or 0
+    s_kv: int = 0                # keys per KV head; 0 means s
+
+    @property
+    def keys(self) -> int:
+        return self.s_kv or self.s
 
     def to_c(self) -> _CParams:
         return _CParams(self.b, self.h_q, self.h_kv, self.s, self.d, int(self.causal),
                         float(self.p_drop), float(self.scale), int(self.seed) & (2**64 - 1),
                         int(self.offset) & (2**64 - 1), self.dev_status or None, int(self.flags),
-                        int(self.wait_timeout_ms), self.timing_events or None)
+                        int(self.wait_timeout_ms), self.timing_events or None, int(self.s_kv))
 
 
 _lib = None
@@ -182,17 +188,20 @@ def _stream() -> int:
 def _params_from(q, k, causal, p_drop, seed, offset, scale, **kw) -> Params:
     b, h_q, s, d = q.shape
     return Params(b=b, h_q=h_q, h_kv=k.shape[1], s=s, d=d, causal=causal, p_drop=p_drop,
-                  scale=scale, seed=seed, offset=offset, **kw)
+                  scale=scale, seed=seed, offset=offset, s_kv=k.shape[2], **kw)
 
 
 def fwd(q, k, v, *, causal: bool = True, p_drop: float = 0.0, seed: int = 0, offset: int = 0,
         scale: float = 0.0, out=None, lse=None, **kw):
-    """Forward of the attention core.  Returns (O bf16 [b,h_q,s,d], LSE fp32 [b,h_q,s])."""
+    """Forward of the attention core.  Returns (O bf16 [b,h_q,s,d], LSE fp32 [b,h_q,s]).
+
+    K and V may have a different sequence length from Q (s_kv keys,
+    cross-attention) when ``causal`` is False."""
     import torch
     p = _params_from(q, k, causal, p_drop, seed, offset, scale, **kw)
     _check(q, "q", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
-    _check(k, "k", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
-    _check(v, "v", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
+    _check(k, "k", torch.bfloat16, (p.b, p.h_kv, p.keys, p.d))
+    _check(v, "v", torch.bfloat16, (p.b, p.h_kv, p.keys, p.d))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -213,14 +222,17 @@ def bwd_recompute(q, k, v, o, lse, dout, *, causal: bool = True, p_drop: float =
     import torch
     p = _params_from(q, k, causal, p_drop, seed, offset, scale, **kw)
     _check(q, "q", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
-    _check(k, "k", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
-    _check(v, "v", torch.bfloat16, (p.b, p.h_kv, p.s, p.d))
+    _check(k, "k", torch.bfloat16, (p.b, p.h_kv, p.keys, p.d))
+    _check(v, "v", torch.bfloat16, (p.b, p.h_kv, p.keys, p.d))
     _check(o, "o", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
     _check(dout, "dout", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
     _check(lse, "lse", torch.float32, (p.b, p.h_q, p.s))
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check(dq, "dq", torch.bfloat16, (p.b, p.h_q, p.s, p.d))
+    _check(dk, "dk", torch.bfloat16, (p.b, p.h_kv, p.keys, p.d))
+    _check(dv, "dv", torch.bfloat16, (p.b, p.h_kv, p.keys, p.d))
     ws_bytes = attn_core_bwd_workspace_bytes(p)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
@@ -233,9 +245,10 @@ def bwd_recompute(q, k, v, o, lse, dout, *, causal: bool = True, p_drop: float =
     return dq, dk, dv
 
 
-def stored_bytes(b: int, h_q: int, h_kv: int, s: int, d: int) -> dict:
+def stored_bytes(b: int, h_q: int, h_kv: int, s: int, d: int, s_kv: int = 0) -> dict:
     """Activation-byte accounting of one layer shard (see attn_core_bytes)."""
-    rc, out = attn_core_stored_bytes(Params(b=b, h_q=h_q, h_kv=h_kv, s=s, d=d))
+    rc, out = attn_core_stored_bytes(Params(b=b, h_q=h_q, h_kv=h_kv, s=s, d=d, s_kv=s_kv,
+                                            causal=not s_kv or s_kv == s))
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_stored_bytes")
     return out

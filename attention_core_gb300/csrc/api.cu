@@ -64,10 +64,16 @@ bool supported_d(int d) { return d == 64 || d == 96 || d == 128 || d == 160; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Keys per KV head: s_kv, or s when s_kv is 0.
+int keys_of(const attn_core_params* p) { return p->s_kv ? p->s_kv : p->s; }
+
 int check_params(const attn_core_params* p)
 {
     if (p == nullptr) return ATTN_CORE_ERR_INVALID_ARG;
-    if (p->b <= 0 || p->h_q <= 0 || p->h_kv <= 0 || p->s <= 0 || p->d <= 0) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->b <= 0 || p->h_q <= 0 || p->h_kv <= 0 || p->s <= 0 || p->d <= 0 || p->s_kv < 0)
+        return ATTN_CORE_ERR_INVALID_ARG;
+    // Causal masking is defined for square score matrices only (s_kv == s).
+    if (p->causal && keys_of(p) != p->s) return ATTN_CORE_ERR_INVALID_ARG;
     if (p->h_q % p->h_kv != 0) return ATTN_CORE_ERR_INVALID_ARG;
     if (p->causal != 0 && p->causal != 1) return ATTN_CORE_ERR_INVALID_ARG;
     if (!(p->p_drop >= 0.0f && p->p_drop < 1.0f)) return ATTN_CORE_ERR_INVALID_ARG;
@@ -76,7 +82,10 @@ int check_params(const attn_core_params* p)
     // Counter words and grid sizes are 32-bit.
     const int64_t n_bh = (int64_t)p->b * p->h_q;
     const int64_t n_blk = ((int64_t)p->s + kBlockRows - 1) / kBlockRows;
-    if (n_bh * n_blk >= (int64_t)INT32_MAX || (int64_t)p->s * n_bh >= ((int64_t)1 << 40)) return ATTN_CORE_ERR_INVALID_ARG;
+    const int64_t n_blk_k = ((int64_t)keys_of(p) + kBlockRows - 1) / kBlockRows;
+    if (n_bh * n_blk >= (int64_t)INT32_MAX || n_bh * n_blk_k >= (int64_t)INT32_MAX ||
+        (int64_t)p->s * n_bh >= ((int64_t)1 << 40))
+        return ATTN_CORE_ERR_INVALID_ARG;
     return ATTN_CORE_OK;
 }
 
@@ -93,9 +102,11 @@ ac::CommonArgs common_args(const attn_core_params* p)
 {
     ac::CommonArgs c{};
     c.s = p->s;
+    c.s_k = keys_of(p);
     c.h_q = p->h_q;
     c.h_kv = p->h_kv;
     c.n_blk = (p->s + kBlockRows - 1) / kBlockRows;
+    c.n_blk_k = (c.s_k + kBlockRows - 1) / kBlockRows;
     c.n_bh = p->b * p->h_q;
     c.causal = p->causal;
     const float scale = (p->scale > 0.0f) ? p->scale : 1.0f / sqrtf((float)p->d);
@@ -164,13 +175,13 @@ int attn_core_stored_bytes(const attn_core_params* p, attn_core_bytes* out)
     int rc = check_params(p);
     if (rc) return rc;
     if (!out) return ATTN_CORE_ERR_INVALID_ARG;
-    const int64_t s = p->s, b = p->b, a = p->h_q, akv = p->h_kv, d = p->d;
+    const int64_t s = p->s, sk = keys_of(p), b = p->b, a = p->h_q, akv = p->h_kv, d = p->d;
     const int64_t h = a * d;
     out->layer_selective = 34 * s * b * h;
-    out->core_scores_avoided = 5 * a * s * s * b;
-    out->layer_none = out->layer_selective + out->core_scores_avoided;
+    out->layer_none = out->layer_selective + 5 * a * s * s * b;
     out->layer_full = 2 * s * b * h;
-    out->core_kept = 2 * s * d * b * (2 * a + 2 * akv);
+    out->core_scores_avoided = 5 * a * s * sk * b;
+    out->core_kept = 2 * d * b * (2 * a * s + 2 * akv * sk);
     out->core_recompute_state = 4 * b * a * s + 16;
     return ATTN_CORE_OK;
 }
@@ -194,8 +205,9 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
     if ((rc = get_encoder())) return rc;
     const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
     CUtensorMap tq, tk, tv, to;
-    if ((rc = encode_map(&tq, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tk, k, p->d, p->s, nkv, 128)) ||
-        (rc = encode_map(&tv, v, p->d, p->s, nkv, 128)) || (rc = encode_map(&to, o, p->d, p->s, nq, 128)))
+    const int sk = keys_of(p);
+    if ((rc = encode_map(&tq, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tk, k, p->d, sk, nkv, 128)) ||
+        (rc = encode_map(&tv, v, p->d, sk, nkv, 128)) || (rc = encode_map(&to, o, p->d, p->s, nq, 128)))
         return rc;
     ac::FwdArgs a{};
     a.c = common_args(p);
@@ -225,14 +237,15 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
     const int bq = ac::dkdv_query_tile(p->d);
     const int bn = ac::dq_key_tile(p->d);
+    const int sk = keys_of(p);
     CUtensorMap tq128, tdo128, to128, tqb, tdob, tk, tv, tkb, tvb, tdq, tdk, tdv;
     if ((rc = encode_map(&tq128, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tdo128, dout, p->d, p->s, nq, 128)) ||
         (rc = encode_map(&to128, o, p->d, p->s, nq, 128)) ||
         (rc = encode_map(&tqb, q, p->d, p->s, nq, bq)) || (rc = encode_map(&tdob, dout, p->d, p->s, nq, bq)) ||
-        (rc = encode_map(&tk, k, p->d, p->s, nkv, 128)) || (rc = encode_map(&tv, v, p->d, p->s, nkv, 128)) ||
-        (rc = encode_map(&tkb, k, p->d, p->s, nkv, bn)) || (rc = encode_map(&tvb, v, p->d, p->s, nkv, bn)) ||
-        (rc = encode_map(&tdq, dq, p->d, p->s, nq, 128)) || (rc = encode_map(&tdk, dk, p->d, p->s, nkv, 128)) ||
-        (rc = encode_map(&tdv, dv, p->d, p->s, nkv, 128)))
+        (rc = encode_map(&tk, k, p->d, sk, nkv, 128)) || (rc = encode_map(&tv, v, p->d, sk, nkv, 128)) ||
+        (rc = encode_map(&tkb, k, p->d, sk, nkv, bn)) || (rc = encode_map(&tvb, v, p->d, sk, nkv, bn)) ||
+        (rc = encode_map(&tdq, dq, p->d, p->s, nq, 128)) || (rc = encode_map(&tdk, dk, p->d, sk, nkv, 128)) ||
+        (rc = encode_map(&tdv, dv, p->d, sk, nkv, 128)))
         return rc;
     ac::BwdArgs a{};
     a.c = common_args(p);

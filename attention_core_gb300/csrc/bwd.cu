@@ -443,7 +443,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int bh = (int)(blockIdx.x % n_bh);
     const int group = a.h_q / a.h_kv;
     const int bkv = (bh / a.h_q) * a.h_kv + (bh % a.h_q) / group;
-    const int n_kblk = (a.s + BN - 1) / BN;
+    const int n_kblk = (a.s_k + BN - 1) / BN;
     const int nk = a.causal ? min((qb + 1) * (128 / BN), n_kblk) : n_kblk;
     const uint32_t warp = warp_id(), lane = lane_id();
 
@@ -655,9 +655,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     if (key0 + 2 * e > i) lo = 0.f;
                     if (key0 + 2 * e + 1 > i) hi = 0.f;
                 }
-                if (!a.causal && key0 + HK > a.s) {
-                    if (key0 + 2 * e >= a.s) lo = 0.f;
-                    if (key0 + 2 * e + 1 >= a.s) hi = 0.f;
+                if (!a.causal && key0 + HK > a.s_k) {
+                    if (key0 + 2 * e >= a.s_k) lo = 0.f;
+                    if (key0 + 2 * e + 1 >= a.s_k) hi = 0.f;
                 }
                 pp[e] = f2_pack(lo, hi);
             }
@@ -766,7 +766,7 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
-    const unsigned grid = (unsigned)a.c.n_blk * n_bkv;
+    const unsigned grid = (unsigned)a.c.n_blk_k * n_bkv;
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return (int)cudaGetLastError();
 }

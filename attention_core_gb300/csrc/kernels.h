@@ -17,9 +17,11 @@ constexpr int kThreads = 384;
 constexpr int kRowThreads = 256;
 
 struct CommonArgs {
-    int32_t s;            // sequence length (queries == keys)
+    int32_t s;            // queries per head
+    int32_t s_k;          // keys (and value rows) per KV head; == s when causal
     int32_t h_q, h_kv;    // query / key-value heads
-    int32_t n_blk;        // ceil(s / 128)
+    int32_t n_blk;        // ceil(s / 128): query blocks
+    int32_t n_blk_k;      // ceil(s_k / 128): key blocks
     int32_t n_bh;         // b * h_q
     int32_t causal;
     float scale_log2;     // score scale * log2(e)

@@ -18,11 +18,13 @@
  * accounting exactly.
  *
  * Tensors (all device pointers, 16-byte aligned, contiguous, row-major):
- *   Q, O, dO, dQ : bf16 [b, h_q,  s, d]
- *   K, V, dK, dV : bf16 [b, h_kv, s, d]
+ *   Q, O, dO, dQ : bf16 [b, h_q,  s,    d]
+ *   K, V, dK, dV : bf16 [b, h_kv, s_kv, d]   (s_kv = s unless set)
  *   LSE          : fp32 [b, h_q, s]   natural-log log-sum-exp of each row
  * Query head h uses KV head h / (h_q / h_kv) (grouped-query attention).
- * Causal masking is top-left aligned: query i sees keys 0..i.
+ * Causal masking is top-left aligned: query i sees keys 0..i; it needs
+ * s_kv == s.  Without it, s queries attend to all s_kv keys
+ * (cross-attention when s_kv != s).
  *
  * Readings the pages leave open (the CPU oracle in the tests follows the
  * same ones):
@@ -55,7 +57,8 @@ extern "C" {
  * output has been written, except ATTN_CORE_ERR_CUDA from a launch, which
  * reports the CUDA error of that launch. */
 #define ATTN_CORE_OK 0
-#define ATTN_CORE_ERR_INVALID_ARG 1         /* null pointer, bad shape, p outside [0,1), offset >= 2^32 */
+#define ATTN_CORE_ERR_INVALID_ARG 1         /* null pointer, bad shape, p outside [0,1), offset >= 2^32,
+                                               causal with s_kv != s */
 #define ATTN_CORE_ERR_UNSUPPORTED 2         /* head dimension or device not supported */
 #define ATTN_CORE_ERR_MISALIGNED 3          /* a pointer is not 16-byte aligned (workspace: 256) */
 #define ATTN_CORE_ERR_WORKSPACE_TOO_SMALL 4 /* bwd workspace smaller than attn_core_bwd_workspace_bytes */
@@ -68,7 +71,7 @@ extern "C" {
                                                   ATTN_CORE_ERR_DEVICE_TIMEOUT to dev_status and exits */
 
 typedef struct {
-    int32_t b, h_q, h_kv, s, d; /* s queries == s keys; h_q % h_kv == 0; d in {64, 96, 128, 160} */
+    int32_t b, h_q, h_kv, s, d; /* s queries per head; h_q % h_kv == 0; d in {64, 96, 128, 160} */
     int32_t causal;             /* 0 or 1 */
     float p_drop;               /* softmax-dropout probability in [0, 1) */
     float scale;                /* score scale; <= 0 selects 1/sqrtf(d) */
@@ -85,6 +88,10 @@ typedef struct {
      * dQ, dK/dV), recorded on `stream` immediately before and
      * after each launch.  May be NULL. */
     void** timing_events;
+    /* Keys (and value rows) per KV head; 0 selects s.  s_kv != s requires
+     * causal == 0.  The dropout mask of (query i, key j) does not depend on
+     * s or s_kv. */
+    int32_t s_kv;
 } attn_core_params;
 
 typedef struct {
@@ -94,8 +101,8 @@ typedef struct {
     int64_t layer_none;           /* 34 s b h + 5 h_q s^2 b : nothing recomputed */
     int64_t layer_selective;      /* 34 s b h               : attention core recomputed */
     int64_t layer_full;           /* 2 s b h                : only the layer input kept */
-    int64_t core_scores_avoided;  /* 5 h_q s^2 b            : what this library never stores */
-    int64_t core_kept;            /* 2 s d b (2 h_q + 2 h_kv): Q, K, V, O in bf16 */
+    int64_t core_scores_avoided;  /* 5 h_q s s_kv b         : what this library never stores */
+    int64_t core_kept;            /* 2 d b (2 h_q s + 2 h_kv s_kv): Q, K, V, O in bf16 */
     int64_t core_recompute_state; /* 4 b h_q s + 16         : LSE and seed/offset */
 } attn_core_bytes;
 

@@ -68,6 +68,9 @@ FAKE = 0x7f0000000000  # 16-byte aligned, never dereferenced: validation fails f
     (dict(p_drop=float("nan")), ac.ERR_INVALID_ARG),
     (dict(offset=2**32), ac.ERR_INVALID_ARG),
     (dict(causal=2), ac.ERR_INVALID_ARG),
+    (dict(s_kv=-1), ac.ERR_INVALID_ARG),
+    (dict(s_kv=200), ac.ERR_INVALID_ARG),            # causal needs s_kv == s
+    (dict(s_kv=200, causal=False, d=80), ac.ERR_UNSUPPORTED),
     (dict(d=80), ac.ERR_UNSUPPORTED),
     (dict(d=256), ac.ERR_UNSUPPORTED),
 ])
@@ -79,6 +82,17 @@ def test_fwd_rejects_null_and_misaligned(lib):
     assert ac.attn_core_fwd(_p(), 0, FAKE, FAKE, FAKE, FAKE, 0) == ac.ERR_INVALID_ARG
     assert ac.attn_core_fwd(_p(), FAKE + 8, FAKE, FAKE, FAKE, FAKE, 0) == ac.ERR_MISALIGNED
     assert ac.attn_core_fwd(_p(), FAKE, FAKE, FAKE, FAKE, FAKE + 4, 0) == ac.ERR_MISALIGNED
+
+
+def test_cross_attention_params(lib):
+    # s_kv == s is self-attention, causal or not; the workspace follows the queries only
+    assert ac.attn_core_bwd_workspace_bytes(_p(s_kv=128)) == ac.attn_core_bwd_workspace_bytes(_p())
+    assert (ac.attn_core_bwd_workspace_bytes(_p(s=200, s_kv=1000, causal=False))
+            == ac.attn_core_bwd_workspace_bytes(_p(s=200)))
+    assert ac.attn_core_bwd_workspace_bytes(_p(s=200, s_kv=1000)) == 0     # causal, s_kv != s
+    args = [FAKE] * 10
+    ws = ac.attn_core_bwd_workspace_bytes(_p())
+    assert ac.attn_core_bwd_recompute(_p(s_kv=64), *args, ws, 0) == ac.ERR_INVALID_ARG
 
 
 def test_bwd_workspace_and_validation(lib):
@@ -105,6 +119,15 @@ def test_stored_bytes_match_oracle(lib, shape):
     got = ac.stored_bytes(b, hq, hkv, s, d)
     ref = oracle.stored_bytes(oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d))
     assert got == ref
+
+
+@pytest.mark.parametrize("shape", [(2, 8, 2, 512, 1536, 64), (1, 4, 4, 300, 77, 128)])
+def test_stored_bytes_cross_attention_match_oracle(lib, shape):
+    b, hq, hkv, s, skv, d = shape
+    got = ac.stored_bytes(b, hq, hkv, s, d, s_kv=skv)
+    ref = oracle.stored_bytes(oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, s_kv=skv))
+    assert got == ref
+    assert got["core_scores_avoided"] == 5 * hq * s * skv * b
 
 
 def test_stored_bytes_llama_worked_example(lib):

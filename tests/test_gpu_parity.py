@@ -75,6 +75,38 @@ def test_custom_scale_and_offset():
         assert row_rel_err(to_np(out[name]), ref) <= TOL, name
 
 
+# Cross-attention (not causal): (b, h_q, h_kv, s queries, s_kv keys, d, p_drop); ragged on
+# either side, more keys than queries and fewer, one-block and multi-block, GQA.
+CROSS = [
+    (1, 2, 2, 300, 77, 64, 0.1),
+    (1, 2, 2, 77, 300, 128, 0.1),
+    (2, 4, 2, 200, 513, 96, 0.2),
+    (1, 2, 1, 130, 260, 160, 0.1),
+    (1, 2, 2, 256, 128, 128, 0.0),
+    (1, 1, 1, 1, 200, 64, 0.1),
+    (1, 2, 2, 129, 1, 128, 0.1),
+]
+
+
+@pytest.mark.parametrize("case", CROSS,
+                         ids=lambda c: f"b{c[0]}_h{c[1]}x{c[2]}_s{c[3]}_kv{c[4]}_d{c[5]}_p{c[6]}")
+def test_cross_attention_matches_oracle(case):
+    b, hq, hkv, s, skv, d, p = case
+    seed = 4242 + s + skv
+    t = random_inputs(b, hq, hkv, s, d, seed=s * 7 + skv, s_kv=skv)
+    out = run_gpu(t, False, p, seed)
+    assert tuple(out["dk"].shape) == (b, hkv, skv, d)
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=False, p_drop=p, seed=seed,
+                        s_kv=skv)
+    ro, rlse = oracle.fwd(pr, t.q, t.k, t.v)
+    rdq, rdk, rdv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    errs = {"o": row_rel_err(to_np(out["o"]), ro), "dq": row_rel_err(to_np(out["dq"]), rdq),
+            "dk": row_rel_err(to_np(out["dk"]), rdk), "dv": row_rel_err(to_np(out["dv"]), rdv)}
+    lse_err = float(np.abs(to_np(out["lse"]) - rlse).max())
+    assert lse_err <= LSE_TOL, lse_err
+    assert all(e <= TOL for e in errs.values()), errs
+
+
 @pytest.mark.parametrize("shape", [(1, 2, 128, 64), (1, 2, 300, 128), (2, 1, 260, 96),
                                    (1, 2, 200, 160)])
 @pytest.mark.parametrize("causal", [True, False])
