@@ -145,6 +145,17 @@ size_t padded_rows(const attn_core_params* p)
     return (size_t)p->b * p->h_q * n_blk * kBlockRows;
 }
 
+// Bytes of the keep bits the dQ kernel hands to the dK/dV kernel (p > 0,
+// d <= 128).  For d = 160 the dK/dV kernel is bound by its products, not by
+// its row threads, so drawing the mask there again costs no time, while
+// writing the bits would cost the dQ kernel some: that case draws twice.
+size_t mask_bytes(const attn_core_params* p)
+{
+    if (drop_threshold(p->p_drop) == 0 || p->d > 128) return 0;
+    const ac::CommonArgs c = common_args(p);
+    return sizeof(uint32_t) * ac::mask_ws_words(c);
+}
+
 int record(void** ev, int idx, cudaStream_t st)
 {
     if (!ev) return ATTN_CORE_OK;
@@ -189,7 +200,7 @@ int attn_core_stored_bytes(const attn_core_params* p, attn_core_bytes* out)
 size_t attn_core_bwd_workspace_bytes(const attn_core_params* p)
 {
     if (check_params(p)) return 0;
-    return 2 * sizeof(float) * padded_rows(p);
+    return 2 * sizeof(float) * padded_rows(p) + mask_bytes(p);
 }
 
 int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -220,9 +231,16 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
     return record(p->timing_events, 1, st);
 }
 
-int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void* k, const void* v, const void* o,
-                            const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
-                            size_t workspace_bytes, void* stream)
+}  // extern "C"
+
+namespace {
+
+// The backward.  share_mask: the workspace also holds the keep bits, which the
+// dQ kernel writes and the dK/dV kernel reads; otherwise the dK/dV kernel draws
+// the mask again from Philox.
+int bwd_impl(const attn_core_params* p, const void* q, const void* k, const void* v, const void* o,
+             const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, bool share_mask, void* stream)
 {
     int rc = check_params(p);
     if (rc) return rc;
@@ -231,7 +249,8 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return ATTN_CORE_ERR_MISALIGNED;
-    if (workspace_bytes < attn_core_bwd_workspace_bytes(p)) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    const size_t need = 2 * sizeof(float) * padded_rows(p) + (share_mask ? mask_bytes(p) : 0);
+    if (workspace_bytes < need) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
     if ((rc = check_device())) return rc;
     if ((rc = get_encoder())) return rc;
     const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
@@ -255,6 +274,9 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     a.lse = lse;
     a.lse2_ws = static_cast<float*>(workspace);
     a.delta_ws = static_cast<float*>(workspace) + padded_rows(p);
+    a.mask_ws = (share_mask && mask_bytes(p) != 0)
+                    ? reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) + 2 * padded_rows(p))
+                    : nullptr;
     a.d = p->d;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool drop = a.c.thr != 0;
@@ -263,6 +285,17 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
     if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
     return record(p->timing_events, 3, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, void* stream)
+{
+    return bwd_impl(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, true, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -291,8 +324,10 @@ int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, co
             return ATTN_CORE_ERR_CUDA;
         g_noalloc_addr[dev] = addr;
     }
-    return attn_core_bwd_recompute(p, q, k, v, o, lse, dout, dq, dk, dv, g_noalloc_addr[dev],
-                                   sizeof(float) * 2 * kNoAllocMaxRows, stream);
+    // The fixed array holds the two row statistics only; the dK/dV kernel draws
+    // its own mask.
+    return bwd_impl(p, q, k, v, o, lse, dout, dq, dk, dv, g_noalloc_addr[dev], sizeof(float) * 2 * kNoAllocMaxRows,
+                    false, stream);
 }
 
 }  // extern "C"

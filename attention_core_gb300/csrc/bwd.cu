@@ -57,7 +57,11 @@ struct DkdvCfg {
     static constexpr uint32_t OFF_DO = OFF_Q + ST * Q_TILE;
     static constexpr uint32_t OFF_LSE = OFF_DO + ST * Q_TILE;
     static constexpr uint32_t OFF_DEL = OFF_LSE + ST * BQ * 4;
-    static constexpr uint32_t OFF_BAR = OFF_DEL + ST * BQ * 4;
+    // keep bits of a query tile, when the dQ kernel handed them over: 4 key
+    // quarters x BQ query rows (in 64-row units) of 32-bit words
+    static constexpr uint32_t MSK_BYTES = BQ * 16;
+    static constexpr uint32_t OFF_MSK = OFF_DEL + ST * BQ * 4;
+    static constexpr uint32_t OFF_BAR = OFF_MSK + ST * MSK_BYTES;
     static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM columns
@@ -76,7 +80,7 @@ struct DkdvBars {
 
 }  // namespace
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool MWS>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -157,7 +161,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 if (!wait_bounded(wc, bar(bars->q_empty[st]), ((it / ST) & 1) ^ 1, timeout_code(kSiteQEmpty)))
                     break;
                 const uint32_t fb = bar(bars->q_full[st]);
-                mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 2 * BQ * 4);
+                mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 2 * BQ * 4 + (MWS ? C::MSK_BYTES : 0u));
                 for (int ch = 0; ch < G::NCH; ++ch) {
                     tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, qt * BQ, bh, fb);
                     tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, qt * BQ, bh,
@@ -166,6 +170,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 const size_t srow = (size_t)bh * args.s_pad + (size_t)qt * BQ;
                 bulk_load_1d(sb + C::OFF_LSE + st * BQ * 4, args.lse2_ws + srow, BQ * 4, fb);
                 bulk_load_1d(sb + C::OFF_DEL + st * BQ * 4, args.delta_ws + srow, BQ * 4, fb);
+                if constexpr (MWS) {
+                    // this tile's rows of the (qb, kb) keep bits: both 64-row units, or one
+                    const size_t w0 = mask_pair_word(a, bh, (qt * BQ) >> 7, kb) + (size_t)(((qt * BQ) & 127) >> 6) * 256;
+                    bulk_load_1d(sb + C::OFF_MSK + st * C::MSK_BYTES, args.mask_ws + w0, C::MSK_BYTES, fb);
+                }
             }
         }
     } else if (alive && warp == 1) {
@@ -248,7 +257,15 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
             keep_bytes_col<HQ>(pk, ks, warp_key0 / 8u + lane / 8u, (uint32_t)q0, klo, khi);
         };
-        if (DROP && n_it > 0) draw_mask(0);
+        // With the dQ kernel's keep bits (MWS): this key's bits over the half's
+        // queries, transposed from the staged rows and spread to byte sign bits
+        // (byte t of word n: query 4n + t of the half).
+        uint32_t kbyte[HQ / 4] = {};
+        auto pair_mask = [&](int e) -> uint32_t {
+            if constexpr (MWS) return keep_pair_mask_nat(kbyte, e);
+            else return keep_pair_mask<HQ>(klo, khi, e);
+        };
+        if (DROP && !MWS && n_it > 0) draw_mask(0);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int st = it % ST;
@@ -259,6 +276,16 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), it & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
+            if constexpr (DROP && MWS) {
+                const uint32_t* msk = reinterpret_cast<const uint32_t*>(smem + C::OFF_MSK + st * C::MSK_BYTES);
+#pragma unroll
+                for (int c = 0; c < HQ / 32; ++c) {
+                    const int row = HQ * h + 32 * c + (int)lane;    // query row of the tile
+                    const uint32_t col = transpose32(msk[(row >> 6) * 256 + (int)(warp & 3u) * 64 + (row & 63)]);
+#pragma unroll
+                    for (int n = 0; n < 8; ++n) kbyte[8 * c + n] = keep_nibble_bytes((col >> (4 * n)) & 0xFu);
+                }
+            }
             const float2* nl2 = reinterpret_cast<const float2*>(lse2_s + st * BQ + HQ * h);
             const float2* dl2 = reinterpret_cast<const float2*>(del_s + st * BQ + HQ * h);
             const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
@@ -292,7 +319,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 uint32_t pw[HQ / 2];
 #pragma unroll
                 for (int e = 0; e < HQ / 2; ++e)
-                    pw[e] = DROP ? pack_bf16x2(pp[e]) & keep_pair_mask<HQ>(klo, khi, e) : pack_bf16x2(pp[e]);
+                    pw[e] = DROP ? pack_bf16x2(pp[e]) & pair_mask(e) : pack_bf16x2(pp[e]);
                 if constexpr (HQ / 2 == 32) {
                     tmem_st32(tmem + C::T_S + lane_off + HQ * h, pw);
                 } else {
@@ -317,7 +344,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
                     if (DROP) {
                         // dP = dP_d * Z: factor 1/(1-p) where kept, 0 where dropped
-                        const uint32_t m = keep_pair_mask<HQ>(klo, khi, ep);
+                        const uint32_t m = pair_mask(ep);
                         dp = f2_mul(dp, f2_pack(__uint_as_float(prmt(m, 0u, 0x9999u) & zs_bits),
                                                 __uint_as_float(prmt(m, 0u, 0xBBBBu) & zs_bits)));
                     }
@@ -329,7 +356,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->ds_full));
-            if (DROP && it + 1 < n_it) draw_mask(it + 1);
+            if (DROP && !MWS && it + 1 < n_it) draw_mask(it + 1);
         }
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
         if (ok) {
@@ -418,7 +445,7 @@ struct DqBars {
 
 }  // namespace
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool MWS>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -683,6 +710,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
                 uint32_t w[16];
+                uint32_t kbits = 0u;                       // keep bits of these 32 keys
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {          // 8 keys per Philox call
                     uint32_t wv[4] = {0u, 0u, 0u, 0u};
@@ -697,11 +725,23 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         const int ep = c32 * 16 + e;
                         uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
                         if (DROP) dp = f2_mul(dp, keep_factor2(wv[t], t16, a.keep_scale));
+                        if (DROP && MWS) {
+                            kbits |= (((wv[t] << 16) >= t16) ? 1u : 0u) << (2 * e);
+                            kbits |= ((wv[t] >= t16) ? 1u : 0u) << (2 * e + 1);
+                        }
                         dacc2 = f2_fma(pp[ep], dp, dacc2);
                         w[e] = pack_bf16x2(f2_mul(pp[ep], f2_sub(dp, dt2)));
                     }
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
+                if constexpr (DROP && MWS) {
+                    // hand the bits to the dK/dV kernel: key quarter of the 128-key block,
+                    // query unit (rows 0-63 / 64-127) and row within it
+                    const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
+                    const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
+                                        (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
+                    args.mask_ws[word] = kbits;
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -756,13 +796,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 // ========================================================== launchers ====
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool MWS>
 static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
                          cudaStream_t stream)
 {
     constexpr uint32_t smem = DkdvCfg<D>::SMEM;
-    auto kern = attn_bwd_dkdv_kernel<D, DROP>;
+    auto kern = attn_bwd_dkdv_kernel<D, DROP, MWS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
@@ -771,12 +811,12 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return (int)cudaGetLastError();
 }
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool MWS>
 static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& to, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
 {
     constexpr uint32_t smem = DqCfg<D>::SMEM;
-    auto kern = attn_bwd_dq_kernel<D, DROP>;
+    auto kern = attn_bwd_dq_kernel<D, DROP, MWS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned grid = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
@@ -790,8 +830,9 @@ int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMa
 {
 #define AC_DKDV_CASE(DD)                                                                            \
     case DD:                                                                                        \
-        return dropout ? launch_dkdv_t<DD, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)              \
-                       : launch_dkdv_t<DD, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+        return !dropout     ? launch_dkdv_t<DD, false, false>(tq, tk, tv, tdo, tdk, tdv, a, stream)   \
+               : a.mask_ws ? launch_dkdv_t<DD, true, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)    \
+                           : launch_dkdv_t<DD, true, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
     switch (d) {
         AC_DKDV_CASE(64)
         AC_DKDV_CASE(96)
@@ -808,8 +849,9 @@ int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap&
 {
 #define AC_DQ_CASE(DD)                                                                              \
     case DD:                                                                                        \
-        return dropout ? launch_dq_t<DD, true>(tq, tk, tv, tdo, to, tdq, a, stream)                 \
-                       : launch_dq_t<DD, false>(tq, tk, tv, tdo, to, tdq, a, stream);
+        return !dropout     ? launch_dq_t<DD, false, false>(tq, tk, tv, tdo, to, tdq, a, stream)        \
+               : a.mask_ws ? launch_dq_t<DD, true, true>(tq, tk, tv, tdo, to, tdq, a, stream)         \
+                           : launch_dq_t<DD, true, false>(tq, tk, tv, tdo, to, tdq, a, stream);
     switch (d) {
         AC_DQ_CASE(64)
         AC_DQ_CASE(96)

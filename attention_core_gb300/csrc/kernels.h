@@ -50,8 +50,23 @@ struct BwdArgs {
     float* lse2_ws;       // [b*h_q*s_pad]  -LSE * log2(e); -inf past s
     float* delta_ws;      // [b*h_q*s_pad]  exact row statistic D = sum_j P_ij dP_ij
                           // (written by the dQ kernel, read by the dK/dV kernel)
+    uint32_t* mask_ws;    // dropout keep bits, written by the dQ kernel and read by the
+                          // dK/dV kernel (layout: mask_pair_word); null: dK/dV draws its own
     int32_t d;
 };
+
+// Keep bits handed from the dQ kernel to the dK/dV kernel.  For every
+// (query head, 128-query block qb, 128-key block kb) that the causal mask does
+// not hide, two 1 KB units (query rows 0-63 and 64-127 of the block); unit
+// word [g * 64 + row] holds, in bit k, whether the pair (query row, key
+// 32 g + k of the block) is kept.  Returns the index of the pair's first word.
+__host__ __device__ inline size_t mask_pair_word(const CommonArgs& a, int bh, int qb, int kb)
+{
+    const size_t per_head = a.causal ? (size_t)a.n_blk * (a.n_blk + 1) / 2 : (size_t)a.n_blk * a.n_blk_k;
+    const size_t pair = a.causal ? (size_t)qb * (qb + 1) / 2 + kb : (size_t)qb * a.n_blk_k + kb;
+    return ((size_t)bh * per_head + pair) * 512;
+}
+inline size_t mask_ws_words(const CommonArgs& a) { return mask_pair_word(a, a.n_bh, 0, 0); }
 
 // Host launchers; return a cudaError_t value.
 int launch_fwd(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -144,4 +144,38 @@ __device__ __forceinline__ uint32_t keep_pair_mask(const uint32_t (&lo)[HQ / 8],
     return t < 4 ? prmt(lo[2 * a], lo[2 * a + 1], sel) : prmt(hi[2 * a], hi[2 * a + 1], sel);
 }
 
+// Keep bits of four consecutive queries (bit t = query t) as the sign bits of
+// four bytes (bit t -> bit 8t + 7).  Multiplying by 2^7 + 2^14 + 2^21 + 2^28
+// moves bit t up by 7t + 7; a cross term t + 7u + 7 (u != t) never lands on a
+// position 8k + 7 and no two terms share a position, so nothing carries.
+__device__ __forceinline__ uint32_t keep_nibble_bytes(uint32_t nibble)
+{
+    return (nibble * 0x10204080u) & 0x80808080u;
+}
+
+// The 16-bit lane mask of the query pair (2e, 2e+1) from such words (byte t
+// of word n: query 4n + t): low half from query 2e's byte, high half from
+// query 2e + 1's.
+__device__ __forceinline__ uint32_t keep_pair_mask_nat(const uint32_t* kbyte, int e)
+{
+    return prmt(kbyte[e >> 1], 0u, (e & 1) ? 0xBBAAu : 0x9988u);
+}
+
+// 32 x 32 bit transpose across a warp: on entry lane L holds row L (bit k =
+// element (L, k)); on return lane L holds column L (bit i = element (i, L)).
+// Five exchange stages; at stage j lanes L and L ^ j swap the j-wide blocks
+// that lie on the wrong side of the diagonal.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const uint32_t j = 16u >> s, m = kMask[s];
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        x = (lane & j) ? (((y >> j) & m) | (x & ~m)) : ((x & m) | ((y << j) & ~m));
+    }
+    return x;
+}
+
 }  // namespace ac

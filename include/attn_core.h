@@ -112,14 +112,22 @@ typedef struct {
 int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const void* v, void* o,
                   float* lse, void* stream);
 
-/* Bytes of device workspace attn_core_bwd_recompute needs:
- * 8 * b * h_q * ceil(s / 128) * 128 (two fp32 row statistics per padded
- * query row), 0 if p is invalid. */
+/* Bytes of device workspace attn_core_bwd_recompute needs, 0 if p is invalid:
+ *   8 * b * h_q * ceil(s / 128) * 128   two fp32 row statistics per padded
+ *                                       query row, and, when p_drop > 0 and
+ *                                       d <= 128,
+ *   2048 * b * h_q * N                  the dropout keep bits, one bit per
+ *                                       (query, key) of each 128 x 128 block,
+ * with N = n (n + 1) / 2 blocks per head if causal (n = ceil(s / 128)), else
+ * ceil(s / 128) * ceil(s_kv / 128). */
 size_t attn_core_bwd_workspace_bytes(const attn_core_params* p);
 
 /* Backward with recomputation: dQ, dK, dV from Q, K, V, O, LSE and dO.  The
  * scores, probabilities and dropout mask are rebuilt on chip from Q, K, LSE
- * and (seed, offset); the mask is bit-identical to the forward's.  The
+ * and (seed, offset); the mask is bit-identical to the forward's.  For
+ * d <= 128 it is drawn once, by the first kernel, which hands it to the
+ * second as bits in the workspace (nothing of it outlives the call); for
+ * d = 160 each kernel draws it.  The
  * softmax row statistic sum_j P_ij dP_ij is formed exactly from the
  * recomputed P and dP (a first estimate from the stored bf16 O is corrected
  * in fp32), not rounded through the stored output.  Launches two kernels
@@ -142,7 +150,8 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
  * has no counterpart to this entry point.
  *
  * Same arguments and results as attn_core_bwd_recompute without the
- * workspace.  Limit: b * h_q * ceil(s / 128) * 128 <= 1048576 padded query
+ * workspace.  The array holds the row statistics only, so here the second
+ * kernel draws the dropout mask again from Philox (the same bits).  Limit: b * h_q * ceil(s / 128) * 128 <= 1048576 padded query
  * rows (the array holds 8 MiB on every GPU that loads the library, until the
  * process exits); larger shapes return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL
  * without launching anything.  The first call on a device looks up the

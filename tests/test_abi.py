@@ -85,10 +85,13 @@ def test_fwd_rejects_null_and_misaligned(lib):
 
 
 def test_cross_attention_params(lib):
-    # s_kv == s is self-attention, causal or not; the workspace follows the queries only
+    # s_kv == s is self-attention; without dropout the workspace follows the queries only
     assert ac.attn_core_bwd_workspace_bytes(_p(s_kv=128)) == ac.attn_core_bwd_workspace_bytes(_p())
+    assert (ac.attn_core_bwd_workspace_bytes(_p(s=200, s_kv=1000, causal=False, p_drop=0.0))
+            == ac.attn_core_bwd_workspace_bytes(_p(s=200, p_drop=0.0)) == 2 * 4 * 2 * 256)
+    # with dropout it adds 2 KB of keep bits per 128 x 128 block: 2 heads x 2 x 8 blocks
     assert (ac.attn_core_bwd_workspace_bytes(_p(s=200, s_kv=1000, causal=False))
-            == ac.attn_core_bwd_workspace_bytes(_p(s=200)))
+            == 2 * 4 * 2 * 256 + 2048 * 2 * 2 * 8)
     assert ac.attn_core_bwd_workspace_bytes(_p(s=200, s_kv=1000)) == 0     # causal, s_kv != s
     args = [FAKE] * 10
     ws = ac.attn_core_bwd_workspace_bytes(_p())
@@ -98,7 +101,12 @@ def test_cross_attention_params(lib):
 def test_bwd_workspace_and_validation(lib):
     p = _p(s=200)
     ws = ac.attn_core_bwd_workspace_bytes(p)
-    assert ws == 2 * 4 * 1 * 2 * 256   # two fp32 statistics per padded query row
+    # two fp32 statistics per padded query row, and (p > 0) 2 KB of keep bits for
+    # each of the 3 causal 128 x 128 blocks of the 2 heads
+    assert ws == 2 * 4 * 1 * 2 * 256 + 2048 * 2 * 3
+    assert ac.attn_core_bwd_workspace_bytes(_p(s=200, p_drop=0.0)) == 2 * 4 * 1 * 2 * 256
+    assert ac.attn_core_bwd_workspace_bytes(_p(s=200, causal=False)) == 2 * 4 * 1 * 2 * 256 + 2048 * 2 * 4
+    assert ac.attn_core_bwd_workspace_bytes(_p(s=200, d=160)) == 2 * 4 * 1 * 2 * 256    # d = 160 draws twice
     assert ac.attn_core_bwd_workspace_bytes(_p(b=0)) == 0
     args = [FAKE] * 10
     assert ac.attn_core_bwd_recompute(p, *args, ws - 1, 0) == ac.ERR_WORKSPACE_TOO_SMALL
