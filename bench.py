@@ -43,8 +43,10 @@ def _flops(w) -> dict:
     pairs = w["s"] * (w["s"] + 1) // 2
     u = w["d"] * pairs * w["b"] * w["h_q"]
     return {"fwd": 4 * u, "bwd": 10 * u, "total": 14 * u, "model": 12 * u,
-            # algorithmic FLOPs of each kernel's launch
-            "k_fwd": 4 * u, "k_dkdv": 8 * u, "k_dq": 2 * u}
+            # algorithmic FLOPs of each kernel's launch: the backward's 10 d per pair
+            # (recomputed S, dP, dV, dQ, dK) split between its two kernels, the
+            # recomputed S and dP that both need counted half to each
+            "k_fwd": 4 * u, "k_dkdv": 6 * u, "k_dq": 4 * u}
 
 
 def _peaks():
