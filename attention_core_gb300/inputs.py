@@ -105,3 +105,40 @@ def dq_mask_probe(b: int, h_q: int, h_kv: int, s: int, d: int, w0: int) -> Tenso
         if j < s:
             k[:, :, j, c] = 1.0
     return Tensors(q, k, v, dout)
+
+
+# Dropout + residual add + layer norm on either side of the core: the rows are
+# tokens (s * b of them), the columns the hidden size h of the layer.
+DAL_WORKLOADS = {
+    "tiny": dict(n_rows=64, hidden=1024, p_drop=0.1),
+    "gpt175b": dict(n_rows=4096, hidden=12288, p_drop=0.1),
+}
+
+
+@dataclass
+class DalTensors:
+    x: torch.Tensor          # sub-layer output entering the dropout, bf16 [n_rows, hidden]
+    residual: torch.Tensor   # residual stream, bf16 [n_rows, hidden]
+    gamma: torch.Tensor      # fp32 [hidden]
+    beta: torch.Tensor       # fp32 [hidden]
+    dy: torch.Tensor         # gradient of the layer-norm output, bf16 [n_rows, hidden]
+    dz_next: torch.Tensor    # gradient reaching z through the residual path, bf16
+
+
+def dal_inputs(n_rows: int, hidden: int, seed: int) -> DalTensors:
+    """x, residual, dy, dz_next ~ N(0, 1) in bf16 (drawn in that order after
+    gamma = 1 + 0.1 N(0, 1) and beta = 0.1 N(0, 1), fp32), on the CPU."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    gamma = 1.0 + 0.1 * torch.randn((hidden,), generator=g, dtype=torch.float32)
+    beta = 0.1 * torch.randn((hidden,), generator=g, dtype=torch.float32)
+    x, r, dy, dzn = (torch.randn((n_rows, hidden), generator=g, dtype=torch.float32).to(torch.bfloat16)
+                     for _ in range(4))
+    return DalTensors(x, r, gamma, beta, dy, dzn)
+
+
+def dal_mask_probe(n_rows: int, hidden: int) -> DalTensors:
+    """x = 1, residual = 0, gamma = 1, beta = 0: z is the keep factor of each
+    element (0 where dropped), so z exposes the dropout mask."""
+    ones = torch.ones((n_rows, hidden), dtype=torch.bfloat16)
+    zeros = torch.zeros((n_rows, hidden), dtype=torch.bfloat16)
+    return DalTensors(ones, zeros, torch.ones(hidden), torch.zeros(hidden), zeros.clone(), zeros.clone())

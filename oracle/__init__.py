@@ -4,10 +4,12 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` import this package.  The product library never does: it shares
 no code with this package, and this package imports nothing from the product.
 
-The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows or
-heads).  This module compiles it with gcc and exposes it through ctypes with
-numpy float64 arrays.  See the header of ``attn_oracle.c`` for what each
-function computes and which passage of the pages it follows.
+The arithmetic lives in ``attn_oracle.c`` (the attention core) and
+``dropout_add_ln_oracle.c`` (the dropout, residual add and layer norm on
+either side of it): plain C, fp64, OpenMP over rows or heads.  This module
+compiles them with gcc and exposes them through ctypes with numpy float64
+arrays.  See the headers of the C files for what each function computes and
+which passage of the pages it follows.
 """
 from __future__ import annotations
 
@@ -19,7 +21,7 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = [os.path.join(_HERE, "attn_oracle.c"), os.path.join(_HERE, "dropout_add_ln_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lib = None
@@ -29,11 +31,11 @@ def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, OpenMP)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(src) for src in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall",
-           "-o", tmp, _SRC, "-lm"]
+           "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -45,6 +47,11 @@ class _Params(ctypes.Structure):
                 ("p_drop", ctypes.c_float), ("scale", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
                 ("stored_o_bf16", ctypes.c_int32), ("s_kv", ctypes.c_int32)]
+
+
+class _DalParams(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("hidden", ctypes.c_int32), ("p_drop", ctypes.c_float),
+                ("eps", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
 
 
 class _Bytes(ctypes.Structure):
@@ -81,6 +88,11 @@ def _load():
         lib.oracle_dq_rows.argtypes = [_PP, _D, _D, _D, _D, ctypes.c_int64, _I64, _I64, _D]
         lib.oracle_dkdv_rows.argtypes = [_PP, _D, _D, _D, _D, ctypes.c_int64, _I64, _I64, _D, _D]
         lib.oracle_stored_bytes.argtypes = [_PP, ctypes.POINTER(_Bytes)]
+        DP = ctypes.POINTER(_DalParams)
+        lib.oracle_dal_keep.argtypes = [DP, ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_dal_keep.restype = ctypes.c_int
+        lib.oracle_dal_fwd.argtypes = [DP, _D, _D, _D, _D, _D, _D, _D, _D]
+        lib.oracle_dal_bwd.argtypes = [DP, _D, _D, _D, _D, _D, _D, _D, _D, _D]
         _lib = lib
     return _lib
 
@@ -241,3 +253,58 @@ def stored_bytes(pr: Problem) -> dict:
     out = _Bytes()
     _load().oracle_stored_bytes(ctypes.byref(pr._c()), ctypes.byref(out))
     return {n: int(getattr(out, n)) for n, _ in _Bytes._fields_}
+
+
+# ------------------------------------------- dropout + residual + layer norm
+
+@dataclass
+class DalProblem:
+    """z = residual + dropout(x), y = LayerNorm(z) over rows of ``hidden`` values."""
+    n_rows: int
+    hidden: int
+    p_drop: float = 0.0
+    eps: float = 1e-5
+    seed: int = 0
+    offset: int = 0
+
+    def _c(self) -> _DalParams:
+        return _DalParams(self.n_rows, self.hidden, float(self.p_drop), float(self.eps),
+                          int(self.seed) & (2**64 - 1), int(self.offset) & (2**64 - 1))
+
+
+def dal_keep(pr: DalProblem, row: int, col: int) -> int:
+    return int(_load().oracle_dal_keep(ctypes.byref(pr._c()), row, col))
+
+
+def dal_mask(pr: DalProblem) -> np.ndarray:
+    """Keep mask (uint8, n_rows x hidden)."""
+    return np.array([[dal_keep(pr, i, c) for c in range(pr.hidden)] for i in range(pr.n_rows)],
+                    dtype=np.uint8)
+
+
+def dal_fwd(pr: DalProblem, x, r, gamma, beta):
+    """(z, y) [n_rows, hidden] and (mean, rstd) [n_rows], fp64."""
+    lib = _load()
+    x, r, gamma, beta = _f64(x), _f64(r), _f64(gamma), _f64(beta)
+    z = np.zeros((pr.n_rows, pr.hidden))
+    y = np.zeros((pr.n_rows, pr.hidden))
+    mean = np.zeros(pr.n_rows)
+    rstd = np.zeros(pr.n_rows)
+    lib.oracle_dal_fwd(ctypes.byref(pr._c()), _dp(x), _dp(r), _dp(gamma), _dp(beta), _dp(z), _dp(y),
+                       _dp(mean), _dp(rstd))
+    return z, y, mean, rstd
+
+
+def dal_bwd(pr: DalProblem, x, r, gamma, dy, dz_next=None):
+    """(dx, d_residual) [n_rows, hidden] and (dgamma, dbeta) [hidden], fp64."""
+    lib = _load()
+    x, r, gamma, dy = _f64(x), _f64(r), _f64(gamma), _f64(dy)
+    dzn = _f64(dz_next) if dz_next is not None else None
+    dx = np.zeros((pr.n_rows, pr.hidden))
+    dres = np.zeros((pr.n_rows, pr.hidden))
+    dgamma = np.zeros(pr.hidden)
+    dbeta = np.zeros(pr.hidden)
+    lib.oracle_dal_bwd(ctypes.byref(pr._c()), _dp(x), _dp(r), _dp(gamma), _dp(dy),
+                       _dp(dzn) if dzn is not None else None, _dp(dx), _dp(dres), _dp(dgamma),
+                       _dp(dbeta))
+    return dx, dres, dgamma, dbeta
