@@ -25,6 +25,8 @@ __all__ = [
     "fwd", "bwd_recompute", "stored_bytes", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED",
     "ERR_MISALIGNED", "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
     "FLAG_TEST_WAIT_TIMEOUT", "SUPPORTED_HEAD_DIMS",
+    "DalParams", "attn_core_dropout_add_ln_fwd", "attn_core_dropout_add_ln_bwd",
+    "attn_core_dropout_add_ln_bwd_workspace_bytes", "dropout_add_ln_fwd", "dropout_add_ln_bwd",
 ]
 
 OK = 0
@@ -55,6 +57,12 @@ class _CParams(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p), ("flags", ctypes.c_int32),
                 ("wait_timeout_ms", ctypes.c_uint32), ("timing_events", ctypes.c_void_p),
                 ("s_kv", ctypes.c_int32)]
+
+
+class _CDalParams(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("hidden", ctypes.c_int32), ("p_drop", ctypes.c_float),
+                ("eps", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+                ("dev_status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32)]
 
 
 class _CBytes(ctypes.Structure):
@@ -93,6 +101,24 @@ class Params:
                         int(self.wait_timeout_ms), self.timing_events or None, int(self.s_kv))
 
 
+@dataclass
+class DalParams:
+    """Mirror of ``attn_core_dal_params`` (dropout + residual add + layer norm)."""
+    n_rows: int
+    hidden: int
+    p_drop: float = 0.0
+    eps: float = 1e-5
+    seed: int = 0
+    offset: int = 0
+    dev_status: int = 0          # device address of an int32, or 0
+    wait_timeout_ms: int = 0
+
+    def to_c(self) -> _CDalParams:
+        return _CDalParams(int(self.n_rows), int(self.hidden), float(self.p_drop), float(self.eps),
+                           int(self.seed) & (2**64 - 1), int(self.offset) & (2**64 - 1),
+                           self.dev_status or None, int(self.wait_timeout_ms))
+
+
 _lib = None
 
 
@@ -120,6 +146,14 @@ def load_library(path: str = LIB_PATH):
     lib.attn_core_stored_bytes.restype = ctypes.c_int
     lib.attn_core_strerror.argtypes = [ctypes.c_int]
     lib.attn_core_strerror.restype = ctypes.c_char_p
+    DP = ctypes.POINTER(_CDalParams)
+    lib.attn_core_dropout_add_ln_fwd.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.attn_core_dropout_add_ln_fwd.restype = ctypes.c_int
+    lib.attn_core_dropout_add_ln_bwd_workspace_bytes.argtypes = [DP]
+    lib.attn_core_dropout_add_ln_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_core_dropout_add_ln_bwd.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 ctypes.c_size_t, vp]
+    lib.attn_core_dropout_add_ln_bwd.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -164,6 +198,27 @@ def attn_core_stored_bytes(p: Params) -> tuple[int, dict]:
     out = _CBytes()
     rc = load_library().attn_core_stored_bytes(ctypes.byref(cp), ctypes.byref(out))
     return rc, {n: int(getattr(out, n)) for n, _ in _CBytes._fields_}
+
+
+def attn_core_dropout_add_ln_fwd(p: DalParams, x: int, residual: int, gamma: int, beta: int, z: int,
+                                 y: int, mean: int, rstd: int, stream: int) -> int:
+    cp = p.to_c()
+    return load_library().attn_core_dropout_add_ln_fwd(ctypes.byref(cp), x, residual, gamma, beta, z, y,
+                                                       mean, rstd, stream or None)
+
+
+def attn_core_dropout_add_ln_bwd_workspace_bytes(p: DalParams) -> int:
+    cp = p.to_c()
+    return int(load_library().attn_core_dropout_add_ln_bwd_workspace_bytes(ctypes.byref(cp)))
+
+
+def attn_core_dropout_add_ln_bwd(p: DalParams, dy: int, dz_next: int, z: int, mean: int, rstd: int,
+                                 gamma: int, dx: int, d_residual: int, dgamma: int, dbeta: int,
+                                 workspace: int, workspace_bytes: int, stream: int) -> int:
+    cp = p.to_c()
+    return load_library().attn_core_dropout_add_ln_bwd(ctypes.byref(cp), dy, dz_next or None, z, mean,
+                                                       rstd, gamma, dx, d_residual, dgamma, dbeta,
+                                                       workspace, workspace_bytes, stream or None)
 
 
 # --------------------------------------------------- torch conveniences ---
@@ -252,3 +307,53 @@ def stored_bytes(b: int, h_q: int, h_kv: int, s: int, d: int, s_kv: int = 0) -> 
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_stored_bytes")
     return out
+
+
+def dropout_add_ln_fwd(x, residual, gamma, beta, *, p_drop: float = 0.0, seed: int = 0, offset: int = 0,
+                       eps: float = 1e-5, **kw):
+    """z = residual + dropout(x), y = LayerNorm(z).  Returns (z, y, mean, rstd)."""
+    import torch
+    n, h = x.shape
+    p = DalParams(n_rows=n, hidden=h, p_drop=p_drop, eps=eps, seed=seed, offset=offset, **kw)
+    _check(x, "x", torch.bfloat16, (n, h))
+    _check(residual, "residual", torch.bfloat16, (n, h))
+    _check(gamma, "gamma", torch.float32, (h,))
+    _check(beta, "beta", torch.float32, (h,))
+    z, y = torch.empty_like(x), torch.empty_like(x)
+    mean = torch.empty(n, dtype=torch.float32, device=x.device)
+    rstd = torch.empty(n, dtype=torch.float32, device=x.device)
+    rc = attn_core_dropout_add_ln_fwd(p, x.data_ptr(), residual.data_ptr(), gamma.data_ptr(),
+                                      beta.data_ptr(), z.data_ptr(), y.data_ptr(), mean.data_ptr(),
+                                      rstd.data_ptr(), _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_dropout_add_ln_fwd")
+    return z, y, mean, rstd
+
+
+def dropout_add_ln_bwd(dy, z, mean, rstd, gamma, *, dz_next=None, p_drop: float = 0.0, seed: int = 0,
+                       offset: int = 0, eps: float = 1e-5, workspace=None, **kw):
+    """Gradients of dropout_add_ln_fwd.  Returns (dx, d_residual, dgamma, dbeta)."""
+    import torch
+    n, h = dy.shape
+    p = DalParams(n_rows=n, hidden=h, p_drop=p_drop, eps=eps, seed=seed, offset=offset, **kw)
+    _check(dy, "dy", torch.bfloat16, (n, h))
+    _check(z, "z", torch.bfloat16, (n, h))
+    _check(mean, "mean", torch.float32, (n,))
+    _check(rstd, "rstd", torch.float32, (n,))
+    _check(gamma, "gamma", torch.float32, (h,))
+    if dz_next is not None:
+        _check(dz_next, "dz_next", torch.bfloat16, (n, h))
+    dx, dres = torch.empty_like(dy), torch.empty_like(dy)
+    dgamma = torch.empty(h, dtype=torch.float32, device=dy.device)
+    dbeta = torch.empty(h, dtype=torch.float32, device=dy.device)
+    ws_bytes = attn_core_dropout_add_ln_bwd_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dy.device)
+    rc = attn_core_dropout_add_ln_bwd(p, dy.data_ptr(), dz_next.data_ptr() if dz_next is not None else 0,
+                                      z.data_ptr(), mean.data_ptr(), rstd.data_ptr(), gamma.data_ptr(),
+                                      dx.data_ptr(), dres.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(),
+                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                      _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_dropout_add_ln_bwd")
+    return dx, dres, dgamma, dbeta

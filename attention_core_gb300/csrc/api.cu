@@ -299,6 +299,109 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
 }
 
 // ---------------------------------------------------------------------------
+// Dropout + residual add + layer norm.
+namespace {
+
+int check_dal(const attn_core_dal_params* p)
+{
+    if (p == nullptr) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->n_rows <= 0 || p->hidden <= 0 || p->hidden % 8 != 0) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->hidden > ac::kDalMaxHidden) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (!(p->p_drop >= 0.0f && p->p_drop < 1.0f)) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!(p->eps > 0.0f) || isinf(p->eps)) return ATTN_CORE_ERR_INVALID_ARG;
+    if (p->offset >> 32) return ATTN_CORE_ERR_INVALID_ARG;
+    return ATTN_CORE_OK;
+}
+
+ac::DalArgs dal_args(const attn_core_dal_params* p)
+{
+    ac::DalArgs a{};
+    a.n_rows = p->n_rows;
+    a.hidden = p->hidden;
+    a.eps = p->eps;
+    a.thr = drop_threshold(p->p_drop);
+    a.keep_scale = 1.0f / (1.0f - (float)a.thr / 65536.0f);
+    a.seed_lo = (uint32_t)(p->seed & 0xffffffffu);
+    a.seed_hi = (uint32_t)(p->seed >> 32);
+    a.offset = (uint32_t)p->offset;
+    a.status = p->dev_status;
+    a.timeout_ns = (uint64_t)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
+    return a;
+}
+
+int dal_partial_rows(const attn_core_dal_params* p)
+{
+    return p->n_rows < ac::kDalMaxPartial ? p->n_rows : ac::kDalMaxPartial;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_core_dropout_add_ln_fwd(const attn_core_dal_params* p, const void* x, const void* residual,
+                                 const float* gamma, const float* beta, void* z, void* y, float* mean,
+                                 float* rstd, void* stream)
+{
+    int rc = check_dal(p);
+    if (rc) return rc;
+    if (!x || !residual || !gamma || !beta || !z || !y || !mean || !rstd) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(gamma) || !aligned16(beta) || !aligned16(z) ||
+        !aligned16(y))
+        return ATTN_CORE_ERR_MISALIGNED;
+    if ((rc = check_device())) return rc;
+    int sms = 0;
+    if ((rc = device_sms(&sms))) return rc;
+    ac::DalArgs a = dal_args(p);
+    a.x = static_cast<const uint16_t*>(x);
+    a.residual = static_cast<const uint16_t*>(residual);
+    a.gamma = gamma;
+    a.beta = beta;
+    a.z = static_cast<uint16_t*>(z);
+    a.y = static_cast<uint16_t*>(y);
+    a.mean = mean;
+    a.rstd = rstd;
+    return ac::launch_dal_fwd(a, sms, reinterpret_cast<cudaStream_t>(stream)) ? ATTN_CORE_ERR_CUDA : ATTN_CORE_OK;
+}
+
+size_t attn_core_dropout_add_ln_bwd_workspace_bytes(const attn_core_dal_params* p)
+{
+    if (check_dal(p)) return 0;
+    return 2 * sizeof(float) * (size_t)p->hidden * (size_t)dal_partial_rows(p);
+}
+
+int attn_core_dropout_add_ln_bwd(const attn_core_dal_params* p, const void* dy, const void* dz_next,
+                                 const void* z, const float* mean, const float* rstd, const float* gamma,
+                                 void* dx, void* d_residual, float* dgamma, float* dbeta, void* workspace,
+                                 size_t workspace_bytes, void* stream)
+{
+    int rc = check_dal(p);
+    if (rc) return rc;
+    if (!dy || !z || !mean || !rstd || !gamma || !dx || !d_residual || !dgamma || !dbeta || !workspace)
+        return ATTN_CORE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || (dz_next && !aligned16(dz_next)) || !aligned16(z) || !aligned16(gamma) ||
+        !aligned16(dx) || !aligned16(d_residual) || !aligned16(workspace))
+        return ATTN_CORE_ERR_MISALIGNED;
+    if (workspace_bytes < attn_core_dropout_add_ln_bwd_workspace_bytes(p)) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    if ((rc = check_device())) return rc;
+    int sms = 0;
+    if ((rc = device_sms(&sms))) return rc;
+    ac::DalArgs a = dal_args(p);
+    a.gamma = gamma;
+    a.z = static_cast<uint16_t*>(const_cast<void*>(z));
+    a.mean = const_cast<float*>(mean);
+    a.rstd = const_cast<float*>(rstd);
+    a.dy = static_cast<const uint16_t*>(dy);
+    a.dz_next = static_cast<const uint16_t*>(dz_next);
+    a.dx = static_cast<uint16_t*>(dx);
+    a.d_residual = static_cast<uint16_t*>(d_residual);
+    a.dgamma = dgamma;
+    a.dbeta = dbeta;
+    a.partial = static_cast<float*>(workspace);
+    return ac::launch_dal_bwd(a, sms, reinterpret_cast<cudaStream_t>(stream)) ? ATTN_CORE_ERR_CUDA : ATTN_CORE_OK;
+}
+
+}  // extern "C"
+
 // Backward for callers that cannot allocate device memory.  Its workspace is a
 // fixed array of this library's own, 2 * kNoAllocMaxRows fp32 values (8 MiB),
 // which every GPU that loads the library holds until the process exits.  The

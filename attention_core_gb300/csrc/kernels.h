@@ -78,6 +78,38 @@ int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap&
                   const CUtensorMap& tdo, const CUtensorMap& to, const CUtensorMap& tdq, const BwdArgs& a,
                   cudaStream_t stream);
 
+// Dropout + residual add + layer norm (dropout_add_ln.cu).  Rows are tokens,
+// `hidden` (a multiple of 8) the row length; bf16 tensors are row-major.
+struct DalArgs {
+    int32_t n_rows, hidden;
+    float eps;
+    float keep_scale;     // 1 / (1 - thr / 65536)
+    uint32_t thr;         // dropout threshold on a 16-bit draw (0: no dropout)
+    uint32_t seed_lo, seed_hi, offset;
+    const uint16_t* x;           // fwd: sub-layer output entering the dropout
+    const uint16_t* residual;    // fwd
+    const float* gamma;          // fwd, bwd
+    const float* beta;           // fwd
+    uint16_t* z;                 // fwd: written; bwd: read
+    uint16_t* y;                 // fwd
+    float* mean;                 // fwd: written; bwd: read
+    float* rstd;                 // fwd: written; bwd: read
+    const uint16_t* dy;          // bwd
+    const uint16_t* dz_next;     // bwd, may be null
+    uint16_t* dx;                // bwd
+    uint16_t* d_residual;        // bwd
+    float* dgamma;               // bwd
+    float* dbeta;                // bwd
+    float* partial;              // bwd workspace: [2][grid][hidden] per-CTA column sums
+    int32_t* status;             // caller-owned device status word (may be null)
+    uint64_t timeout_ns;         // limit of every in-kernel wait
+};
+constexpr int kDalMaxHidden = 28672;   // backward keeps 8 * hidden bytes of column sums in shared memory
+constexpr int kDalMaxPartial = 320;   // backward CTAs (rows of the partial-sum workspace)
+// Grids are sized from the device's SM count and each kernel's occupancy.
+int launch_dal_fwd(const DalArgs& a, int sms, cudaStream_t stream);
+int launch_dal_bwd(const DalArgs& a, int sms, cudaStream_t stream);
+
 // Query-tile height of the dK/dV kernel for head dimension d (TMEM budget).
 constexpr int dkdv_query_tile(int d) { return (2 * d + 2 * 128 <= 512) ? 128 : 64; }
 // Key-block width of the dQ kernel for head dimension d (TMEM budget:

@@ -354,6 +354,11 @@ def run_ours(args, w):
     if not args.no_graph:
         graph = _graph_replay(args, sets, step, n_sets, dev, fl, world, dist, status)
 
+    # the dropout + residual add + layer norm block of the same layer (its own field)
+    dal = None
+    if not args.no_dal and rank == 0:
+        dal = _dal_measure(dev, stream)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -388,6 +393,7 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "cuda_graph": graph,
+            "dropout_add_ln": dal,
             "gpu_launches": 3 * K,
             "kernel_ms_sampled": f"per-kernel events on every {EVERY}th timed step ({len(kt['fwd'])} samples)",
             "clocks": clocks,
@@ -396,6 +402,55 @@ def run_ours(args, w):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def _dal_measure(dev, stream, iters: int = 30):
+    """Dropout + residual add + layer norm at the 175B layer's residual boundary
+    (s * b = 4096 tokens of h = 12288, p = 0.1): forward and backward, each timed
+    alone with CUDA events on its stream, inputs (100 MB per tensor) larger than
+    L2.  Algorithmic bytes: forward reads x and the residual and writes z and y
+    (8 n h) plus mean, rstd, gamma and beta; backward reads dy, z and dz_next and
+    writes dx and d_residual (10 n h) plus mean, rstd, gamma, dgamma and dbeta."""
+    import secrets
+
+    import torch
+
+    import attention_core_gb300 as ac
+    from attention_core_gb300.inputs import DAL_WORKLOADS, dal_inputs
+    w = DAL_WORKLOADS["gpt175b"]
+    n, h, p = w["n_rows"], w["hidden"], w["p_drop"]
+    t = dal_inputs(n, h, seed=11)
+    x, r, dy, dzn = (v.to(dev) for v in (t.x, t.residual, t.dy, t.dz_next))
+    g, b = t.gamma.to(dev), t.beta.to(dev)
+    kw = dict(p_drop=p, seed=secrets.randbits(63), offset=0)
+    z, y, mean, rstd = ac.dropout_add_ln_fwd(x, r, g, b, **kw)
+    ws = torch.empty(ac.attn_core_dropout_add_ln_bwd_workspace_bytes(ac.DalParams(n, h, p)),
+                     dtype=torch.uint8, device=dev)
+    fwd_bytes = 8 * n * h + 8 * n + 8 * h
+    bwd_bytes = 10 * n * h + 8 * n + 12 * h
+    pk = _peaks()
+    out = {"workload": f"{n} tokens x hidden {h} (175B layer, s=2048, b=2), p={p}"}
+    for name, fn, nbytes in (
+            ("fwd", lambda: ac.dropout_add_ln_fwd(x, r, g, b, **kw), fwd_bytes),
+            ("bwd", lambda: ac.dropout_add_ln_bwd(dy, z, mean, rstd, g, dz_next=dzn, workspace=ws, **kw),
+             bwd_bytes)):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = sorted(e0.elapsed_time(e1) for e0, e1 in evs)[iters // 2]
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"us": ms * 1e3, "roofline": {
+            "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"], "bytes": nbytes,
+            "traffic": _traffic("dal_" + name + "_kernel", "gpt175b_dal")}}
+    return out
 
 
 def _graph_replay(args, sets, step, n_sets, dev, fl, world, dist, status):
@@ -534,6 +589,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay figure")
+    ap.add_argument("--no-dal", action="store_true",
+                    help="skip the dropout + residual add + layer norm measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the CPU-oracle baseline sample")
     args = ap.parse_args()

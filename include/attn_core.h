@@ -172,6 +172,65 @@ int attn_core_stored_bytes(const attn_core_params* p, attn_core_bytes* out);
 /* Static description of a return code. */
 const char* attn_core_strerror(int code);
 
+/* ------------------------------------------------------------------------
+ * Dropout + residual add + layer norm at a residual sub-layer boundary, on
+ * either side of the attention core.  These are the layer norms and the
+ * dropouts after the attention block and the MLP that tensor parallelism
+ * leaves replicated and that act on each sequence position independently
+ * ("Reducing Activation Recomputation in Large Transformer Models", dmarx
+ * anthology LIT-736, Key takeaways, first and second bullets).  Reading of
+ * the block (the pages give no formula), per row (token) of `hidden` values:
+ *     z = residual + dropout(x)                            stored, bf16
+ *     y = gamma * (z - mean) * rstd + beta                 bf16
+ *     rstd = 1 / sqrt(var + eps), var the biased variance of the stored z.
+ * Dropout follows the attention core's reading with counter (col / 8, row,
+ * 0xFFFFFFFF, offset): word 2 is a value no attention head index takes.  As
+ * in the core, the backward redraws the mask from (seed, offset); the block
+ * keeps z, mean and rstd only.
+ *
+ * Tensors (device pointers, 16-byte aligned, contiguous, row-major):
+ *   x, residual, z, y, dy, dz_next, dx, d_residual : bf16 [n_rows, hidden]
+ *   gamma, beta, dgamma, dbeta                      : fp32 [hidden]
+ *   mean, rstd                                      : fp32 [n_rows]
+ * Asynchronous on `stream`; nothing is allocated.  Return codes as above. */
+typedef struct {
+    int32_t n_rows;   /* tokens, >= 1 */
+    int32_t hidden;   /* multiple of 8, 8 .. 28672 */
+    float p_drop;     /* [0, 1) */
+    float eps;        /* layer-norm epsilon, > 0 */
+    uint64_t seed;    /* Philox key */
+    uint64_t offset;  /* Philox counter word 3; must be < 2^32 */
+    /* Optional caller-owned device int32, zero before the call: a forward
+     * wait that runs out writes ATTN_CORE_ERR_DEVICE_TIMEOUT | 1 << 8 there.
+     * May be NULL. */
+    int32_t* dev_status;
+    uint32_t wait_timeout_ms;   /* limit of each in-kernel wait; 0 selects 2000 ms */
+} attn_core_dal_params;
+
+/* Forward: writes z, y, mean and rstd.  Launches one kernel. */
+int attn_core_dropout_add_ln_fwd(const attn_core_dal_params* p, const void* x, const void* residual,
+                                 const float* gamma, const float* beta, void* z, void* y, float* mean,
+                                 float* rstd, void* stream);
+
+/* Bytes of device workspace the backward needs: 8 * hidden * min(n_rows, 320)
+ * (per-CTA column sums for dgamma and dbeta), 0 if p is invalid. */
+size_t attn_core_dropout_add_ln_bwd_workspace_bytes(const attn_core_dal_params* p);
+
+/* Backward from dy (gradient of y) and, optionally, dz_next (the gradient
+ * reaching z through the residual path; NULL for none):
+ *     dz = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dz_next,
+ *          g = dy * gamma, xhat = (z - mean) * rstd,
+ *     d_residual = dz,  dx = dz * keep / (1 - p_eff),
+ *     dgamma = sum over rows of dy * xhat,  dbeta = sum over rows of dy.
+ * Needs z, mean and rstd from the forward, not x or residual.  dgamma and
+ * dbeta are summed in a fixed order (bit-reproducible).  Launches two
+ * kernels; `workspace` is caller-owned device memory of at least
+ * attn_core_dropout_add_ln_bwd_workspace_bytes(p) bytes, 16-byte aligned. */
+int attn_core_dropout_add_ln_bwd(const attn_core_dal_params* p, const void* dy, const void* dz_next,
+                                 const void* z, const float* mean, const float* rstd, const float* gamma,
+                                 void* dx, void* d_residual, float* dgamma, float* dbeta, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

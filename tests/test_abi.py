@@ -155,3 +155,46 @@ def test_binding_fails_loudly_without_library(tmp_path):
             ac.load_library(str(tmp_path / "missing.so"))
     finally:
         ac._lib = saved
+
+
+# ------------------------------------------- dropout + residual + layer norm
+
+def _dp(**kw):
+    base = dict(n_rows=64, hidden=1024, p_drop=0.1, eps=1e-5, seed=1, offset=0)
+    base.update(kw)
+    return ac.DalParams(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_rows=0), ac.ERR_INVALID_ARG),
+    (dict(hidden=1020), ac.ERR_INVALID_ARG),          # not a multiple of 8
+    (dict(hidden=0), ac.ERR_INVALID_ARG),
+    (dict(hidden=28680), ac.ERR_UNSUPPORTED),          # above the column-sum buffer
+    (dict(p_drop=1.0), ac.ERR_INVALID_ARG),
+    (dict(eps=0.0), ac.ERR_INVALID_ARG),
+    (dict(eps=float("nan")), ac.ERR_INVALID_ARG),
+    (dict(offset=2**32), ac.ERR_INVALID_ARG),
+])
+def test_dal_rejects_bad_params(lib, kw, code):
+    assert ac.attn_core_dropout_add_ln_fwd(_dp(**kw), *([FAKE] * 8), 0) == code
+    assert ac.attn_core_dropout_add_ln_bwd_workspace_bytes(_dp(**kw)) == 0
+
+
+def test_dal_workspace_and_validation(lib):
+    # per-CTA column sums of dgamma and dbeta: 2 x 4 bytes x hidden x min(n_rows, 320)
+    assert ac.attn_core_dropout_add_ln_bwd_workspace_bytes(_dp()) == 8 * 1024 * 64
+    assert ac.attn_core_dropout_add_ln_bwd_workspace_bytes(_dp(n_rows=4096, hidden=12288)) == 8 * 12288 * 320
+    p = _dp()
+    ws = ac.attn_core_dropout_add_ln_bwd_workspace_bytes(p)
+    args = [FAKE] * 11                                 # dy, dz_next, z, ..., dbeta, workspace
+    assert ac.attn_core_dropout_add_ln_bwd(p, *args, ws - 1, 0) == ac.ERR_WORKSPACE_TOO_SMALL
+    a1 = list(args)
+    a1[1] = FAKE + 8                                   # dz_next is optional, but aligned if given
+    assert ac.attn_core_dropout_add_ln_bwd(p, *a1, ws, 0) == ac.ERR_MISALIGNED
+    a2 = list(args)
+    a2[0] = FAKE + 8                                   # dy misaligned
+    assert ac.attn_core_dropout_add_ln_bwd(p, *a2, ws, 0) == ac.ERR_MISALIGNED
+    a3 = list(args)
+    a3[2] = 0                                          # z missing
+    assert ac.attn_core_dropout_add_ln_bwd(p, *a3, ws, 0) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_dropout_add_ln_fwd(p, 0, *([FAKE] * 7), 0) == ac.ERR_INVALID_ARG
