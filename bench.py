@@ -49,6 +49,22 @@ def _flops(w) -> dict:
             "k_fwd": 4 * u, "k_dkdv": 6 * u, "k_dq": 4 * u}
 
 
+def job_ms(ms: float, dist, device) -> float:
+    """The job's time: the slowest rank's (max over ranks; one rank: its own)."""
+    if dist is None:
+        return ms
+    import torch
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tflops(units_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed (each rank runs the
+    same workload on its own inputs) over the job's time."""
+    return units_per_rank_step * steps * world / (ms / 1e3) / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -325,11 +341,7 @@ def run_ours(args, w):
     clocks = sampler.stop()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x} during the timed region")
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = job_ms(t_start.elapsed_time(t_end), dist, dev)
 
     names = ["fwd", "dq", "dkdv"]
     kt = {n: [] for n in names}
@@ -341,8 +353,7 @@ def run_ours(args, w):
     bwd_ms = kavg["dkdv"] + kavg["dq"]
 
     pk = _peaks()
-    total_units = fl["total"] * K * world
-    value = total_units / (elapsed_ms / 1e3) / 1e12
+    value = job_tflops(fl["total"], K, world, elapsed_ms)
     dom = max(("fwd", "dkdv", "dq"), key=lambda n: kavg[n])
     dom_flops = fl["k_" + dom]
     achieved = dom_flops / (kavg[dom] / 1e3) / 1e12
@@ -483,13 +494,9 @@ def _graph_replay(args, sets, step, n_sets, dev, fl, world, dist, status):
         side.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x} during the graph replays")
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = job_ms(e0.elapsed_time(e1), dist, dev)
     steps = reps * n_sets
-    return {"value": fl["total"] * steps * world / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+    return {"value": job_tflops(fl["total"], steps, world, ms), "unit": "TFLOP/s",
             "steps": steps, "ms_per_step": ms / steps, "gpu_launches": 3 * steps}
 
 
@@ -569,12 +576,8 @@ def _e2e(args, w, pr, base, dev, stream, ws_bytes, fl, world, dist):
     stream.wait_stream(s_up)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": fl["total"] * k2 * world / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+    ms = job_ms(e0.elapsed_time(e1), dist, dev)
+    return {"value": job_tflops(fl["total"], k2, world, ms), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k2,
             "ms_per_step": ms / k2, "pipelined": "uploads, compute and downloads of adjacent steps overlap"}
 
