@@ -27,6 +27,7 @@ __all__ = [
     "FLAG_TEST_WAIT_TIMEOUT", "SUPPORTED_HEAD_DIMS",
     "DalParams", "attn_core_dropout_add_ln_fwd", "attn_core_dropout_add_ln_bwd",
     "attn_core_dropout_add_ln_bwd_workspace_bytes", "dropout_add_ln_fwd", "dropout_add_ln_bwd",
+    "attn_core_gelu_fwd", "attn_core_gelu_bwd", "gelu_fwd", "gelu_bwd",
 ]
 
 OK = 0
@@ -154,6 +155,10 @@ def load_library(path: str = LIB_PATH):
     lib.attn_core_dropout_add_ln_bwd.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  ctypes.c_size_t, vp]
     lib.attn_core_dropout_add_ln_bwd.restype = ctypes.c_int
+    lib.attn_core_gelu_fwd.argtypes = [ctypes.c_int64, vp, vp, vp]
+    lib.attn_core_gelu_fwd.restype = ctypes.c_int
+    lib.attn_core_gelu_bwd.argtypes = [ctypes.c_int64, vp, vp, vp, vp]
+    lib.attn_core_gelu_bwd.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -219,6 +224,14 @@ def attn_core_dropout_add_ln_bwd(p: DalParams, dy: int, dz_next: int, z: int, me
     return load_library().attn_core_dropout_add_ln_bwd(ctypes.byref(cp), dy, dz_next or None, z, mean,
                                                        rstd, gamma, dx, d_residual, dgamma, dbeta,
                                                        workspace, workspace_bytes, stream or None)
+
+
+def attn_core_gelu_fwd(n: int, x: int, y: int, stream: int) -> int:
+    return load_library().attn_core_gelu_fwd(int(n), x, y, stream or None)
+
+
+def attn_core_gelu_bwd(n: int, x: int, dy: int, dx: int, stream: int) -> int:
+    return load_library().attn_core_gelu_bwd(int(n), x, dy, dx, stream or None)
 
 
 # --------------------------------------------------- torch conveniences ---
@@ -357,3 +370,26 @@ def dropout_add_ln_bwd(dy, z, mean, rstd, gamma, *, dz_next=None, p_drop: float 
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_dropout_add_ln_bwd")
     return dx, dres, dgamma, dbeta
+
+
+def gelu_fwd(x, out=None):
+    """GeLU (tanh form) of a contiguous bf16 CUDA tensor (numel a multiple of 8)."""
+    import torch
+    _check(x, "x", torch.bfloat16, tuple(x.shape))
+    out = torch.empty_like(x) if out is None else out
+    rc = attn_core_gelu_fwd(x.numel(), x.data_ptr(), out.data_ptr(), _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_gelu_fwd")
+    return out
+
+
+def gelu_bwd(x, dy, out=None):
+    """dy * GeLU'(x) for contiguous bf16 CUDA tensors of one shape."""
+    import torch
+    _check(x, "x", torch.bfloat16, tuple(x.shape))
+    _check(dy, "dy", torch.bfloat16, tuple(x.shape))
+    out = torch.empty_like(x) if out is None else out
+    rc = attn_core_gelu_bwd(x.numel(), x.data_ptr(), dy.data_ptr(), out.data_ptr(), _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_gelu_bwd")
+    return out

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libattn_core.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "dropout_add_ln.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "dropout_add_ln.cu", "gelu.cu"]
 HEADERS = ["ptx.cuh", "philox.cuh", "tile.cuh", "sched.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -402,6 +402,39 @@ int attn_core_dropout_add_ln_bwd(const attn_core_dal_params* p, const void* dy, 
 
 }  // extern "C"
 
+// GeLU of the layer's MLP.
+extern "C" {
+
+int attn_core_gelu_fwd(int64_t n, const void* x, void* y, void* stream)
+{
+    if (n <= 0 || n % 8 != 0 || !x || !y) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return ATTN_CORE_ERR_MISALIGNED;
+    int rc = check_device();
+    if (rc) return rc;
+    int sms = 0;
+    if ((rc = device_sms(&sms))) return rc;
+    return ac::launch_gelu_fwd(static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), n, sms,
+                               reinterpret_cast<cudaStream_t>(stream))
+               ? ATTN_CORE_ERR_CUDA
+               : ATTN_CORE_OK;
+}
+
+int attn_core_gelu_bwd(int64_t n, const void* x, const void* dy, void* dx, void* stream)
+{
+    if (n <= 0 || n % 8 != 0 || !x || !dy || !dx) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return ATTN_CORE_ERR_MISALIGNED;
+    int rc = check_device();
+    if (rc) return rc;
+    int sms = 0;
+    if ((rc = device_sms(&sms))) return rc;
+    return ac::launch_gelu_bwd(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dy),
+                               static_cast<uint16_t*>(dx), n, sms, reinterpret_cast<cudaStream_t>(stream))
+               ? ATTN_CORE_ERR_CUDA
+               : ATTN_CORE_OK;
+}
+
+}  // extern "C"
+
 // Backward for callers that cannot allocate device memory.  Its workspace is a
 // fixed array of this library's own, 2 * kNoAllocMaxRows fp32 values (8 MiB),
 // which every GPU that loads the library holds until the process exits.  The

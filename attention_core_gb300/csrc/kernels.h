@@ -110,6 +110,10 @@ constexpr int kDalMaxPartial = 320;   // backward CTAs (rows of the partial-sum 
 int launch_dal_fwd(const DalArgs& a, int sms, cudaStream_t stream);
 int launch_dal_bwd(const DalArgs& a, int sms, cudaStream_t stream);
 
+// GeLU (tanh form) of the layer's MLP, elementwise on n bf16 values (n % 8 == 0).
+int launch_gelu_fwd(const uint16_t* x, uint16_t* y, int64_t n, int sms, cudaStream_t stream);
+int launch_gelu_bwd(const uint16_t* x, const uint16_t* dy, uint16_t* dx, int64_t n, int sms, cudaStream_t stream);
+
 // Query-tile height of the dK/dV kernel for head dimension d (TMEM budget).
 constexpr int dkdv_query_tile(int d) { return (2 * d + 2 * 128 <= 512) ? 128 : 64; }
 // Key-block width of the dQ kernel for head dimension d (TMEM budget:

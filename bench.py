@@ -370,6 +370,11 @@ def run_ours(args, w):
     if not args.no_dal and rank == 0:
         dal = _dal_measure(dev, stream)
 
+    # the layer around the core: recompute overhead of the core against the whole layer
+    layer_study = None
+    if not args.no_layer and rank == 0:
+        layer_study = _layer_study(dev, stream)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -405,6 +410,7 @@ def run_ours(args, w):
             "e2e": e2e,
             "cuda_graph": graph,
             "dropout_add_ln": dal,
+            "layer_study": layer_study,
             "gpu_launches": 3 * K,
             "kernel_ms_sampled": f"per-kernel events on every {EVERY}th timed step ({len(kt['fwd'])} samples)",
             "clocks": clocks,
@@ -462,6 +468,54 @@ def _dal_measure(dev, stream, iters: int = 30):
             "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"], "bytes": nbytes,
             "traffic": _traffic("dal_" + name + "_kernel", "gpt175b_dal")}}
     return out
+
+
+def _layer_study(dev, stream, iters: int = 10):
+    """One 175B-shaped layer shard (b=2, s=2048, h=12288, 12 local heads of 128,
+    MLP width 6144, p=0.1) through attention_core_gb300.layer: the layer's
+    forward, its backward (which recomputes the attention core) and the core's
+    forward alone, each the median of `iters` CUDA-event timings on the stream.
+    Overheads are relative to a step without recomputation, taken as the step
+    minus the core's forward time (an upper bound of what the backward spends
+    rebuilding the core): recomputing the core costs that core forward,
+    recomputing the whole layer (full recomputation) a whole layer forward."""
+    import torch
+
+    import attention_core_gb300 as ac
+    from attention_core_gb300 import layer
+    sh = layer.LayerShape(b=2, s=2048, h=12288, a=12, d=128, ffn=6144, p_drop=0.1)
+    w = layer.init_weights(sh, seed=3, device=dev)
+    gen = torch.Generator(device="cpu").manual_seed(4)
+    y_in, r_in, dy2, dz2 = (torch.randn((sh.n, sh.h), generator=gen).to(torch.bfloat16).to(dev)
+                            for _ in range(4))
+    seed = 12345
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return sorted(e0.elapsed_time(e1) for e0, e1 in evs)[iters // 2]
+
+    _, _, ctx = layer.forward(sh, w, y_in, r_in, seed=seed)
+    fwd_ms = timed(lambda: layer.forward(sh, w, y_in, r_in, seed=seed))
+    bwd_ms = timed(lambda: layer.backward(sh, w, ctx, dy2, dz2))
+    core_ms = timed(lambda: ac.fwd(ctx["q"], ctx["k"], ctx["v"], **ctx["core"]))
+    step = fwd_ms + bwd_ms
+    base = step - core_ms
+    sb = ac.stored_bytes(sh.b, sh.a, sh.a, sh.s, sh.d)
+    return {"workload": "175B layer shard: b=2, s=2048, h=12288, 12 local heads of 128, MLP 6144, "
+                        "p=0.1; GEMMs by cuBLAS (torch.matmul), the rest by this library",
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms": step, "core_fwd_ms": core_ms,
+            "overhead_selective": core_ms / base, "overhead_full": fwd_ms / base,
+            "gemm_fwd_tflops": sh.gemm_flops_fwd() / (fwd_ms / 1e3) / 1e12,
+            "activation_bytes_per_layer": {k: sb[k] for k in ("layer_none", "layer_selective", "layer_full")}}
 
 
 def _graph_replay(args, sets, step, n_sets, dev, fl, world, dist, status):
@@ -594,6 +648,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay figure")
     ap.add_argument("--no-dal", action="store_true",
                     help="skip the dropout + residual add + layer norm measurement")
+    ap.add_argument("--no-layer", action="store_true",
+                    help="skip the layer-level recompute-overhead measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the CPU-oracle baseline sample")
     args = ap.parse_args()

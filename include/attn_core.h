@@ -231,6 +231,17 @@ int attn_core_dropout_add_ln_bwd(const attn_core_dal_params* p, const void* dy, 
                                  void* dx, void* d_residual, float* dgamma, float* dbeta, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * GeLU of the layer's MLP, for the layer-level measurement of selective
+ * recomputation (the anthology page's Key takeaways, fourth bullet: recompute
+ * the whole layer, or only the attention core).  Tanh form:
+ *     y = x / 2 * (1 + tanh(sqrt(2 / pi) * (x + 0.044715 x^3))),
+ * elementwise on n bf16 values (n a multiple of 8, pointers 16-byte aligned),
+ * fp32 arithmetic.  The backward writes dx = dy * dy/dx at x.  One kernel
+ * each, asynchronous on `stream`. */
+int attn_core_gelu_fwd(int64_t n, const void* x, void* y, void* stream);
+int attn_core_gelu_bwd(int64_t n, const void* x, const void* dy, void* dx, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

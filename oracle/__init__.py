@@ -14,6 +14,7 @@ which passage of the pages it follows.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 from dataclasses import dataclass
@@ -308,3 +309,23 @@ def dal_bwd(pr: DalProblem, x, r, gamma, dy, dz_next=None):
                        _dp(dzn) if dzn is not None else None, _dp(dx), _dp(dres), _dp(dgamma),
                        _dp(dbeta))
     return dx, dres, dgamma, dbeta
+
+
+# ------------------------------------------------------------------ GeLU ---
+# The MLP activation of the layer around the core, tanh form (Hendrycks and
+# Gimpel): y = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), fp64.
+
+_GELU_C = math.sqrt(2.0 / math.pi)
+_GELU_A = 0.044715
+
+
+def gelu(x) -> np.ndarray:
+    x = _f64(x)
+    return 0.5 * x * (1.0 + np.tanh(_GELU_C * (x + _GELU_A * x ** 3)))
+
+
+def gelu_grad(x) -> np.ndarray:
+    """d gelu / dx."""
+    x = _f64(x)
+    t = np.tanh(_GELU_C * (x + _GELU_A * x ** 3))
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * _GELU_C * (1.0 + 3.0 * _GELU_A * x * x)
