@@ -28,6 +28,8 @@ __all__ = [
     "DalParams", "attn_core_dropout_add_ln_fwd", "attn_core_dropout_add_ln_bwd",
     "attn_core_dropout_add_ln_bwd_workspace_bytes", "dropout_add_ln_fwd", "dropout_add_ln_bwd",
     "attn_core_gelu_fwd", "attn_core_gelu_bwd", "gelu_fwd", "gelu_bwd",
+    "attn_core_fwd_varlen", "attn_core_bwd_varlen", "attn_core_bwd_varlen_workspace_bytes",
+    "fwd_varlen", "bwd_varlen",
 ]
 
 OK = 0
@@ -58,6 +60,12 @@ class _CParams(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p), ("flags", ctypes.c_int32),
                 ("wait_timeout_ms", ctypes.c_uint32), ("timing_events", ctypes.c_void_p),
                 ("s_kv", ctypes.c_int32)]
+
+
+class _CVarlenParams(ctypes.Structure):
+    _fields_ = [("base", _CParams), ("n_seq", ctypes.c_int32),
+                ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)),
+                ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32))]
 
 
 class _CDalParams(ctypes.Structure):
@@ -155,6 +163,13 @@ def load_library(path: str = LIB_PATH):
     lib.attn_core_dropout_add_ln_bwd.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  ctypes.c_size_t, vp]
     lib.attn_core_dropout_add_ln_bwd.restype = ctypes.c_int
+    VP = ctypes.POINTER(_CVarlenParams)
+    lib.attn_core_fwd_varlen.argtypes = [VP, vp, vp, vp, vp, vp, vp]
+    lib.attn_core_fwd_varlen.restype = ctypes.c_int
+    lib.attn_core_bwd_varlen_workspace_bytes.argtypes = [VP]
+    lib.attn_core_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_core_bwd_varlen.argtypes = [VP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.attn_core_bwd_varlen.restype = ctypes.c_int
     lib.attn_core_gelu_fwd.argtypes = [ctypes.c_int64, vp, vp, vp]
     lib.attn_core_gelu_fwd.restype = ctypes.c_int
     lib.attn_core_gelu_bwd.argtypes = [ctypes.c_int64, vp, vp, vp, vp]
@@ -224,6 +239,34 @@ def attn_core_dropout_add_ln_bwd(p: DalParams, dy: int, dz_next: int, z: int, me
     return load_library().attn_core_dropout_add_ln_bwd(ctypes.byref(cp), dy, dz_next or None, z, mean,
                                                        rstd, gamma, dx, d_residual, dgamma, dbeta,
                                                        workspace, workspace_bytes, stream or None)
+
+
+def _varlen_c(p: Params, cu_q, cu_k):
+    """(_CVarlenParams, keep-alive arrays) for host sequence tables."""
+    aq = (ctypes.c_int32 * len(cu_q))(*[int(x) for x in cu_q])
+    ak = (ctypes.c_int32 * len(cu_k))(*[int(x) for x in cu_k]) if cu_k is not None else None
+    vp = _CVarlenParams(p.to_c(), len(cu_q) - 1, ctypes.cast(aq, ctypes.POINTER(ctypes.c_int32)),
+                        ctypes.cast(ak, ctypes.POINTER(ctypes.c_int32)) if ak is not None else None)
+    return vp, (aq, ak)
+
+
+def attn_core_fwd_varlen(p: Params, cu_q, cu_k, q: int, k: int, v: int, o: int, lse: int, stream: int) -> int:
+    """p supplies h_q, h_kv, d, causal, p_drop, scale, seed, offset, dev_status,
+    flags and wait_timeout_ms; cu_q / cu_k are host sequence tables."""
+    vp, keep = _varlen_c(p, cu_q, cu_k)
+    return load_library().attn_core_fwd_varlen(ctypes.byref(vp), q, k, v, o, lse, stream or None)
+
+
+def attn_core_bwd_varlen_workspace_bytes(p: Params, cu_q, cu_k) -> int:
+    vp, keep = _varlen_c(p, cu_q, cu_k)
+    return int(load_library().attn_core_bwd_varlen_workspace_bytes(ctypes.byref(vp)))
+
+
+def attn_core_bwd_varlen(p: Params, cu_q, cu_k, q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int,
+                         dk: int, dv: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    vp, keep = _varlen_c(p, cu_q, cu_k)
+    return load_library().attn_core_bwd_varlen(ctypes.byref(vp), q, k, v, o, lse, dout, dq, dk, dv, workspace,
+                                               workspace_bytes, stream or None)
 
 
 def attn_core_gelu_fwd(n: int, x: int, y: int, stream: int) -> int:
@@ -393,3 +436,51 @@ def gelu_bwd(x, dy, out=None):
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_gelu_bwd")
     return out
+
+
+def _varlen_params(q, k, causal, p_drop, seed, offset, scale, **kw) -> Params:
+    _, h_q, d = q.shape
+    return Params(b=1, h_q=h_q, h_kv=k.shape[1], s=1, d=d, causal=causal, p_drop=p_drop, scale=scale,
+                  seed=seed, offset=offset, **kw)
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k=None, *, causal: bool = True, p_drop: float = 0.0,
+               seed: int = 0, offset: int = 0, scale: float = 0.0, **kw):
+    """Forward over a packed batch: q [total_q, h_q, d], k/v [total_k, h_kv, d];
+    cu_seqlens_* host sequence tables (lists or CPU tensors).  Returns (O, LSE
+    [h_q, total_q])."""
+    import torch
+    p = _varlen_params(q, k, causal, p_drop, seed, offset, scale, **kw)
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k] if cu_seqlens_k is not None else None
+    _check(q, "q", torch.bfloat16, (cq[-1], p.h_q, p.d))
+    _check(k, "k", torch.bfloat16, ((ck or cq)[-1], p.h_kv, p.d))
+    _check(v, "v", torch.bfloat16, ((ck or cq)[-1], p.h_kv, p.d))
+    o = torch.empty_like(q)
+    lse = torch.empty((p.h_q, cq[-1]), dtype=torch.float32, device=q.device)
+    rc = attn_core_fwd_varlen(p, cq, ck, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_fwd_varlen")
+    return o, lse
+
+
+def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k=None, *, causal: bool = True,
+               p_drop: float = 0.0, seed: int = 0, offset: int = 0, scale: float = 0.0, **kw):
+    """Recompute-backward over a packed batch.  Returns (dQ, dK, dV)."""
+    import torch
+    p = _varlen_params(q, k, causal, p_drop, seed, offset, scale, **kw)
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k] if cu_seqlens_k is not None else None
+    _check(o, "o", torch.bfloat16, tuple(q.shape))
+    _check(dout, "dout", torch.bfloat16, tuple(q.shape))
+    _check(lse, "lse", torch.float32, (p.h_q, cq[-1]))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = attn_core_bwd_varlen_workspace_bytes(p, cq, ck)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    rc = attn_core_bwd_varlen(p, cq, ck, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                              ws.data_ptr(), ws.numel(), _stream())
+    if rc != OK:
+        raise AttnCoreError(rc, "attn_core_bwd_varlen")
+    return dq, dk, dv

@@ -120,23 +120,52 @@ ac::CommonArgs common_args(const attn_core_params* p)
     c.status = p->dev_status;
     c.timeout_ns = (uint64_t)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
     c.inject_timeout = (p->flags & ATTN_CORE_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
+    c.bh0 = 0;
+    c.lse_stride = p->s;
     return c;
 }
 
-// 3-D map over a [heads, s, d] bf16 tensor: box = one column chunk of
+// 3-D map over `heads` x `s` rows of d bf16 values, row r of head h at
+// ptr + h * head_stride + r * row_stride elements: box = one column chunk of
 // `rows` rows of one head, swizzled to match the shared-memory tile layout.
-int encode_map(CUtensorMap* m, const void* ptr, int d, int s, int64_t heads, int rows)
+// [heads, s, d] tensors have row_stride d and head_stride s * d; one sequence
+// of a packed [tokens, heads, d] batch has row_stride heads * d and
+// head_stride d.
+int encode_map_strided(CUtensorMap* m, const void* ptr, int d, int s, int64_t heads, int64_t row_stride,
+                       int64_t head_stride, int rows)
 {
     const int cw = (d % 64 == 0) ? 64 : 32;
     const CUtensorMapSwizzle sw = (cw == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)s, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)s * (cuuint64_t)d * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)head_stride * 2};
     cuuint32_t box[3] = {(cuuint32_t)cw, (cuuint32_t)rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_CORE_OK : ATTN_CORE_ERR_CUDA;
+}
+
+// Where the query-side (Q, O, dO, dQ) and key-side (K, V, dK, dV) rows of one
+// launch live, and where its LSE rows go.
+struct Geometry {
+    int64_t q_heads, kv_heads;              // map heads: b * h_q and b * h_kv, or h_q and h_kv
+    int64_t q_row, q_head, kv_row, kv_head; // strides in elements
+    int64_t lse_stride;                     // LSE elements from one query head to the next
+    uint32_t bh0;                           // Philox head-index offset
+};
+
+Geometry padded_geometry(const attn_core_params* p, int sk)
+{
+    Geometry g;
+    g.q_heads = (int64_t)p->b * p->h_q;
+    g.kv_heads = (int64_t)p->b * p->h_kv;
+    g.q_row = g.kv_row = p->d;
+    g.q_head = (int64_t)p->s * p->d;
+    g.kv_head = (int64_t)sk * p->d;
+    g.lse_stride = p->s;
+    g.bh0 = 0;
+    return g;
 }
 
 size_t padded_rows(const attn_core_params* p)
@@ -203,6 +232,40 @@ size_t attn_core_bwd_workspace_bytes(const attn_core_params* p)
     return 2 * sizeof(float) * padded_rows(p) + mask_bytes(p);
 }
 
+}  // extern "C"
+
+namespace {
+
+// One forward launch over the geometry g (pointers at the launch's first row).
+int fwd_launch(const attn_core_params* p, const Geometry& g, const void* q, const void* k, const void* v, void* o,
+               float* lse, cudaStream_t st)
+{
+    int rc;
+    const int sk = keys_of(p);
+    CUtensorMap tq, tk, tv, to;
+    if ((rc = encode_map_strided(&tq, q, p->d, p->s, g.q_heads, g.q_row, g.q_head, 128)) ||
+        (rc = encode_map_strided(&tk, k, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, 128)) ||
+        (rc = encode_map_strided(&tv, v, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, 128)) ||
+        (rc = encode_map_strided(&to, o, p->d, p->s, g.q_heads, g.q_row, g.q_head, 128)))
+        return rc;
+    ac::FwdArgs a{};
+    a.c = common_args(p);
+    a.c.bh0 = g.bh0;
+    a.c.lse_stride = g.lse_stride;
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.o_head_stride = g.q_head;
+    a.o_row_stride = g.q_row;
+    if ((rc = device_sms(&a.num_sms))) return rc;
+    if ((rc = record(p->timing_events, 0, st))) return rc;
+    if (ac::launch_fwd(p->d, a.c.thr != 0, tq, tk, tv, to, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    return record(p->timing_events, 1, st);
+}
+
+}  // namespace
+
+extern "C" {
+
 int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const void* v, void* o, float* lse,
                   void* stream)
 {
@@ -214,30 +277,68 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
         return ATTN_CORE_ERR_MISALIGNED;
     if ((rc = check_device())) return rc;
     if ((rc = get_encoder())) return rc;
-    const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
-    CUtensorMap tq, tk, tv, to;
-    const int sk = keys_of(p);
-    if ((rc = encode_map(&tq, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tk, k, p->d, sk, nkv, 128)) ||
-        (rc = encode_map(&tv, v, p->d, sk, nkv, 128)) || (rc = encode_map(&to, o, p->d, p->s, nq, 128)))
-        return rc;
-    ac::FwdArgs a{};
-    a.c = common_args(p);
-    a.o = static_cast<uint16_t*>(o);
-    a.lse = lse;
-    if ((rc = device_sms(&a.num_sms))) return rc;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((rc = record(p->timing_events, 0, st))) return rc;
-    if (ac::launch_fwd(p->d, a.c.thr != 0, tq, tk, tv, to, a, st) != 0) return ATTN_CORE_ERR_CUDA;
-    return record(p->timing_events, 1, st);
+    return fwd_launch(p, padded_geometry(p, keys_of(p)), q, k, v, o, lse, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
 
 namespace {
 
-// The backward.  share_mask: the workspace also holds the keep bits, which the
-// dQ kernel writes and the dK/dV kernel reads; otherwise the dK/dV kernel draws
-// the mask again from Philox.
+// Workspace bytes of one backward launch: the two row statistics and (when
+// shared) the keep bits, rounded up to 256 bytes.
+size_t launch_ws_bytes(const attn_core_params* p, bool share_mask)
+{
+    const size_t b = 2 * sizeof(float) * padded_rows(p) + (share_mask ? mask_bytes(p) : 0);
+    return (b + 255) & ~(size_t)255;
+}
+
+// One backward launch (dQ, then dK/dV) over the geometry g; `workspace` holds
+// launch_ws_bytes(p, share_mask) bytes.  share_mask: the workspace also holds
+// the keep bits, which the dQ kernel writes and the dK/dV kernel reads;
+// otherwise the dK/dV kernel draws the mask again from Philox.
+int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, const void* k, const void* v,
+               const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+               bool share_mask, cudaStream_t st)
+{
+    int rc;
+    const int bq = ac::dkdv_query_tile(p->d);
+    const int bn = ac::dq_key_tile(p->d);
+    const int sk = keys_of(p);
+    auto qmap = [&](CUtensorMap* m, const void* ptr, int rows) {
+        return encode_map_strided(m, ptr, p->d, p->s, g.q_heads, g.q_row, g.q_head, rows);
+    };
+    auto kmap = [&](CUtensorMap* m, const void* ptr, int rows) {
+        return encode_map_strided(m, ptr, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, rows);
+    };
+    CUtensorMap tq128, tdo128, to128, tqb, tdob, tk, tv, tkb, tvb, tdq, tdk, tdv;
+    if ((rc = qmap(&tq128, q, 128)) || (rc = qmap(&tdo128, dout, 128)) || (rc = qmap(&to128, o, 128)) ||
+        (rc = qmap(&tqb, q, bq)) || (rc = qmap(&tdob, dout, bq)) || (rc = kmap(&tk, k, 128)) ||
+        (rc = kmap(&tv, v, 128)) || (rc = kmap(&tkb, k, bn)) || (rc = kmap(&tvb, v, bn)) ||
+        (rc = qmap(&tdq, dq, 128)) || (rc = kmap(&tdk, dk, 128)) || (rc = kmap(&tdv, dv, 128)))
+        return rc;
+    ac::BwdArgs a{};
+    a.c = common_args(p);
+    a.c.bh0 = g.bh0;
+    a.c.lse_stride = g.lse_stride;
+    a.s_pad = a.c.n_blk * kBlockRows;
+    a.o = static_cast<const uint16_t*>(o);
+    a.dout = static_cast<const uint16_t*>(dout);
+    a.lse = lse;
+    a.lse2_ws = static_cast<float*>(workspace);
+    a.delta_ws = static_cast<float*>(workspace) + padded_rows(p);
+    a.mask_ws = (share_mask && mask_bytes(p) != 0)
+                    ? reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) + 2 * padded_rows(p))
+                    : nullptr;
+    a.d = p->d;
+    const bool drop = a.c.thr != 0;
+    if ((rc = record(p->timing_events, 0, st))) return rc;
+    if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, to128, tdq, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
+    if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    return record(p->timing_events, 3, st);
+}
+
+// The backward of the padded layout.
 int bwd_impl(const attn_core_params* p, const void* q, const void* k, const void* v, const void* o,
              const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
              size_t workspace_bytes, bool share_mask, void* stream)
@@ -253,38 +354,8 @@ int bwd_impl(const attn_core_params* p, const void* q, const void* k, const void
     if (workspace_bytes < need) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
     if ((rc = check_device())) return rc;
     if ((rc = get_encoder())) return rc;
-    const int64_t nq = (int64_t)p->b * p->h_q, nkv = (int64_t)p->b * p->h_kv;
-    const int bq = ac::dkdv_query_tile(p->d);
-    const int bn = ac::dq_key_tile(p->d);
-    const int sk = keys_of(p);
-    CUtensorMap tq128, tdo128, to128, tqb, tdob, tk, tv, tkb, tvb, tdq, tdk, tdv;
-    if ((rc = encode_map(&tq128, q, p->d, p->s, nq, 128)) || (rc = encode_map(&tdo128, dout, p->d, p->s, nq, 128)) ||
-        (rc = encode_map(&to128, o, p->d, p->s, nq, 128)) ||
-        (rc = encode_map(&tqb, q, p->d, p->s, nq, bq)) || (rc = encode_map(&tdob, dout, p->d, p->s, nq, bq)) ||
-        (rc = encode_map(&tk, k, p->d, sk, nkv, 128)) || (rc = encode_map(&tv, v, p->d, sk, nkv, 128)) ||
-        (rc = encode_map(&tkb, k, p->d, sk, nkv, bn)) || (rc = encode_map(&tvb, v, p->d, sk, nkv, bn)) ||
-        (rc = encode_map(&tdq, dq, p->d, p->s, nq, 128)) || (rc = encode_map(&tdk, dk, p->d, sk, nkv, 128)) ||
-        (rc = encode_map(&tdv, dv, p->d, sk, nkv, 128)))
-        return rc;
-    ac::BwdArgs a{};
-    a.c = common_args(p);
-    a.s_pad = a.c.n_blk * kBlockRows;
-    a.o = static_cast<const uint16_t*>(o);
-    a.dout = static_cast<const uint16_t*>(dout);
-    a.lse = lse;
-    a.lse2_ws = static_cast<float*>(workspace);
-    a.delta_ws = static_cast<float*>(workspace) + padded_rows(p);
-    a.mask_ws = (share_mask && mask_bytes(p) != 0)
-                    ? reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) + 2 * padded_rows(p))
-                    : nullptr;
-    a.d = p->d;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const bool drop = a.c.thr != 0;
-    if ((rc = record(p->timing_events, 0, st))) return rc;
-    if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, to128, tdq, a, st) != 0) return ATTN_CORE_ERR_CUDA;
-    if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
-    if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
-    return record(p->timing_events, 3, st);
+    return bwd_launch(p, padded_geometry(p, keys_of(p)), q, k, v, o, lse, dout, dq, dk, dv, workspace, share_mask,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -297,6 +368,140 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
 {
     return bwd_impl(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, true, stream);
 }
+
+// ---------------------------------------------------------------------------
+// Variable-length (packed) batches: one launch per sequence, each over that
+// sequence's rows of the packed tensors.
+namespace {
+
+// Checks the sequence table and fills the per-sequence parameters' shared part.
+int check_varlen(const attn_core_varlen_params* vp, int64_t* total_q, int64_t* total_k)
+{
+    if (vp == nullptr || vp->n_seq <= 0 || vp->cu_seqlens_q == nullptr) return ATTN_CORE_ERR_INVALID_ARG;
+    if (vp->base.timing_events != nullptr) return ATTN_CORE_ERR_INVALID_ARG;
+    if ((int64_t)vp->n_seq * vp->base.h_q >= (int64_t)INT32_MAX) return ATTN_CORE_ERR_INVALID_ARG;
+    const int32_t* cq = vp->cu_seqlens_q;
+    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
+    if (cq[0] != 0 || ck[0] != 0) return ATTN_CORE_ERR_INVALID_ARG;
+    for (int i = 0; i < vp->n_seq; ++i) {
+        const int32_t lq = cq[i + 1] - cq[i], lk = ck[i + 1] - ck[i];
+        if (lq < 0 || lk < 0 || (lq > 0 && lk == 0)) return ATTN_CORE_ERR_INVALID_ARG;
+        if (vp->base.causal && lq != lk) return ATTN_CORE_ERR_INVALID_ARG;
+        if (lq == 0) continue;
+        attn_core_params ps = vp->base;
+        ps.b = 1;
+        ps.s = lq;
+        ps.s_kv = lk;
+        if (int rc = check_params(&ps)) return rc;
+    }
+    *total_q = cq[vp->n_seq];
+    *total_k = ck[vp->n_seq];
+    return ATTN_CORE_OK;
+}
+
+// Sequence i as a one-batch launch: its parameters and geometry.
+attn_core_params seq_params(const attn_core_varlen_params* vp, int i)
+{
+    const int32_t* cq = vp->cu_seqlens_q;
+    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
+    attn_core_params ps = vp->base;
+    ps.b = 1;
+    ps.s = cq[i + 1] - cq[i];
+    ps.s_kv = ck[i + 1] - ck[i];
+    return ps;
+}
+
+Geometry seq_geometry(const attn_core_varlen_params* vp, int i, int64_t total_q)
+{
+    Geometry g;
+    g.q_heads = vp->base.h_q;
+    g.kv_heads = vp->base.h_kv;
+    g.q_row = (int64_t)vp->base.h_q * vp->base.d;
+    g.kv_row = (int64_t)vp->base.h_kv * vp->base.d;
+    g.q_head = g.kv_head = vp->base.d;
+    g.lse_stride = total_q;
+    g.bh0 = (uint32_t)i * (uint32_t)vp->base.h_q;
+    return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_core_bwd_varlen_workspace_bytes(const attn_core_varlen_params* vp)
+{
+    int64_t tq = 0, tk = 0;
+    if (check_varlen(vp, &tq, &tk)) return 0;
+    size_t total = 0;
+    for (int i = 0; i < vp->n_seq; ++i) {
+        const attn_core_params ps = seq_params(vp, i);
+        if (ps.s > 0) total += launch_ws_bytes(&ps, true);
+    }
+    return total;
+}
+
+int attn_core_fwd_varlen(const attn_core_varlen_params* vp, const void* q, const void* k, const void* v, void* o,
+                         float* lse, void* stream)
+{
+    int64_t tq = 0, tk = 0;
+    int rc = check_varlen(vp, &tq, &tk);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!supported_d(vp->base.d)) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_CORE_ERR_MISALIGNED;
+    if ((rc = check_device())) return rc;
+    if ((rc = get_encoder())) return rc;
+    const int d = vp->base.d, hq = vp->base.h_q, hkv = vp->base.h_kv;
+    const int32_t* cq = vp->cu_seqlens_q;
+    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
+    for (int i = 0; i < vp->n_seq; ++i) {
+        const attn_core_params ps = seq_params(vp, i);
+        if (ps.s == 0) continue;
+        const size_t qo = (size_t)cq[i] * hq * d, ko = (size_t)ck[i] * hkv * d;
+        rc = fwd_launch(&ps, seq_geometry(vp, i, tq), static_cast<const uint16_t*>(q) + qo,
+                        static_cast<const uint16_t*>(k) + ko, static_cast<const uint16_t*>(v) + ko,
+                        static_cast<uint16_t*>(o) + qo, lse + cq[i], reinterpret_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
+    return ATTN_CORE_OK;
+}
+
+int attn_core_bwd_varlen(const attn_core_varlen_params* vp, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, void* stream)
+{
+    int64_t tq = 0, tk = 0;
+    int rc = check_varlen(vp, &tq, &tk);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return ATTN_CORE_ERR_INVALID_ARG;
+    if (!supported_d(vp->base.d)) return ATTN_CORE_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return ATTN_CORE_ERR_MISALIGNED;
+    if (workspace_bytes < attn_core_bwd_varlen_workspace_bytes(vp)) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    if ((rc = check_device())) return rc;
+    if ((rc = get_encoder())) return rc;
+    const int d = vp->base.d, hq = vp->base.h_q, hkv = vp->base.h_kv;
+    const int32_t* cq = vp->cu_seqlens_q;
+    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    for (int i = 0; i < vp->n_seq; ++i) {
+        const attn_core_params ps = seq_params(vp, i);
+        if (ps.s == 0) continue;
+        const size_t qo = (size_t)cq[i] * hq * d, ko = (size_t)ck[i] * hkv * d;
+        rc = bwd_launch(&ps, seq_geometry(vp, i, tq), static_cast<const uint16_t*>(q) + qo,
+                        static_cast<const uint16_t*>(k) + ko, static_cast<const uint16_t*>(v) + ko,
+                        static_cast<const uint16_t*>(o) + qo, lse + cq[i], static_cast<const uint16_t*>(dout) + qo,
+                        static_cast<uint16_t*>(dq) + qo, static_cast<uint16_t*>(dk) + ko,
+                        static_cast<uint16_t*>(dv) + ko, ws, true, reinterpret_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+        ws += launch_ws_bytes(&ps, true);
+    }
+    return ATTN_CORE_OK;
+}
+
+}  // extern "C"
 
 // ---------------------------------------------------------------------------
 // Dropout + residual add + layer norm.

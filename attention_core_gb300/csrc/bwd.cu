@@ -254,7 +254,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         auto draw_mask = [&](int it) {
             const int bh = bh0 + it / per_head;
             const int q0 = (qt0 + it % per_head) * BQ + HQ * h;
-            const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh, a.offset, a.thr};
+            const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh + a.bh0, a.offset, a.thr};
             keep_bytes_col<HQ>(pk, ks, warp_key0 / 8u + lane / 8u, (uint32_t)q0, klo, khi);
         };
         // With the dQ kernel's keep bits (MWS): this key's bits over the half's
@@ -627,7 +627,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // D~ = rowsum(dO * O) from the staged bf16 O and dO tiles (rows past s
         // were filled with zeros by TMA).  Each half sums its D/2 columns; the
         // halves meet in shared memory.
-        const float nl2 = i < a.s ? -args.lse[(size_t)bh * a.s + i] * 1.44269504088896340736f : -INFINITY;
+        const float nl2 = i < a.s ? -args.lse[(size_t)bh * a.lse_stride + i] * 1.44269504088896340736f : -INFINITY;
         if (h == 0) args.lse2_ws[srow] = nl2;
         bool ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_full), 0, timeout_code(kSiteOFull)));
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->qdo_full), 0, timeout_code(kSiteQFull)));
@@ -715,7 +715,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int g = 0; g < 4; ++g) {          // 8 keys per Philox call
                     uint32_t wv[4] = {0u, 0u, 0u, 0u};
                     if (DROP) {
-                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + c32 * 4 + g, (uint32_t)i, (uint32_t)bh,
+                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + c32 * 4 + g, (uint32_t)i,
+                                                       (uint32_t)bh + a.bh0,
                                                        a.offset, a.seed_lo, a.seed_hi);
                         wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
                     }

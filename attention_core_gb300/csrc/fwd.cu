@@ -397,7 +397,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int g8 = 0; g8 < 8; ++g8) {
                     uint32_t wv[4] = {0u, 0u, 0u, 0u};
                     if (DROP) {
-                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g8, (uint32_t)i, (uint32_t)bh,
+                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g8, (uint32_t)i, (uint32_t)bh + a.bh0,
                                                        a.offset, a.seed_lo, a.seed_hi);
                         wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
                     }
@@ -456,7 +456,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     stage_row32<D, 128>(sb + C::OFF_OST, r, c32 * 32, rr, inv);
                 }
                 if (i < a.s && h == 0)
-                    args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+                    args.lse[(size_t)bh * a.lse_stride + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
                 fence_proxy_async_smem();
                 ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_full), u & 1, timeout_code(kSiteStage)));
                 if (!ok) break;
@@ -470,7 +470,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // 32-column chunks.  The TMEM loads are warp-collective, so every
                 // lane takes them; only the stores are guarded (rows past s).
                 const bool live = i < a.s;
-                uint4* orow = reinterpret_cast<uint4*>(args.o + ((size_t)bh * a.s + (live ? i : 0)) * D);
+                uint4* orow = reinterpret_cast<uint4*>(args.o + (size_t)bh * args.o_head_stride +
+                                                       (size_t)(live ? i : 0) * args.o_row_stride);
 #pragma unroll 1
                 for (int c32 = h; c32 < D / 32; c32 += 2) {
                     uint32_t rr[32];
@@ -486,7 +487,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 }
                 if (live && h == 0)
-                    args.lse[(size_t)bh * a.s + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+                    args.lse[(size_t)bh * a.lse_stride + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
             }
             tc_fence_before();
             mbar_arrive(bar(bars->o_free));

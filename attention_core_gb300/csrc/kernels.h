@@ -32,12 +32,17 @@ struct CommonArgs {
     int32_t* status;      // caller-owned device status word (may be null)
     uint64_t timeout_ns;  // limit of every in-kernel wait
     int32_t inject_timeout;  // test hook: every thread waits on a barrier nothing completes
+    uint32_t bh0;         // added to the flattened head index in the Philox counter (a
+                          // sequence of a packed batch draws as batch element bh0 / h_q)
+    int64_t lse_stride;   // LSE elements from one query head to the next (s, or the
+                          // packed batch's total query count)
 };
 
 struct FwdArgs {
     CommonArgs c;
-    uint16_t* o;          // bf16 [b*h_q*s*d]
-    float* lse;           // [b*h_q*s]
+    uint16_t* o;          // bf16 [b*h_q*s*d], or one sequence of a packed [tokens, h_q, d]
+    float* lse;           // query head bh, row i at lse[bh * c.lse_stride + i]
+    int64_t o_head_stride, o_row_stride;   // elements, for O stored row by row (d = 160)
     int32_t num_sms;      // persistent grid size
 };
 

@@ -164,6 +164,41 @@ int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, co
                                     const void* o, const float* lse, const void* dout, void* dq, void* dk,
                                     void* dv, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Variable-length (packed) batches.  n_seq sequences of different lengths in
+ * one token-major tensor; the tokens of sequence i are rows cu_seqlens_q[i]
+ * .. cu_seqlens_q[i + 1] - 1 (keys: cu_seqlens_k, NULL for the same table):
+ *   Q, O, dO, dQ : bf16 [total_q, h_q, d]     total_q = cu_seqlens_q[n_seq]
+ *   K, V, dK, dV : bf16 [total_k, h_kv, d]
+ *   LSE          : fp32 [h_q, total_q]
+ * Each sequence attends only within itself, as batch element i of the
+ * padded layout would: the same causal rule (causal needs equal query and
+ * key counts per sequence), and the same dropout mask (Philox counter word 2
+ * = i * h_q + head).  The sequence tables are HOST arrays of n_seq + 1 int32
+ * starting at 0 and nondecreasing; an empty sequence is skipped, one with
+ * queries but no keys is invalid.  `base` supplies h_q, h_kv, d, causal,
+ * p_drop, scale, seed, offset, dev_status, flags and wait_timeout_ms; its b,
+ * s and s_kv are ignored and its timing_events must be NULL.  The kernels
+ * run one sequence after another on `stream` (the same kernels as the
+ * padded entry points, each over one sequence's rows). */
+typedef struct {
+    attn_core_params base;
+    int32_t n_seq;
+    const int32_t* cu_seqlens_q;   /* host, n_seq + 1 */
+    const int32_t* cu_seqlens_k;   /* host, n_seq + 1, or NULL: as cu_seqlens_q */
+} attn_core_varlen_params;
+
+int attn_core_fwd_varlen(const attn_core_varlen_params* p, const void* q, const void* k, const void* v, void* o,
+                         float* lse, void* stream);
+
+/* Workspace of attn_core_bwd_varlen: each sequence's share of
+ * attn_core_bwd_workspace_bytes, rounded up to 256 bytes. */
+size_t attn_core_bwd_varlen_workspace_bytes(const attn_core_varlen_params* p);
+
+int attn_core_bwd_varlen(const attn_core_varlen_params* p, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* Activation-byte accounting (pure host, integer, exact).  Worked example of
  * the activation-checkpointing page: Llama 3 70B, s = 8192, b = 1, h_q = 64,
  * d = 128, 80 layers -> 1.9 TB none, 182.5 GB selective, 10.7 GB full. */

@@ -198,3 +198,27 @@ def test_dal_workspace_and_validation(lib):
     a3[2] = 0                                          # z missing
     assert ac.attn_core_dropout_add_ln_bwd(p, *a3, ws, 0) == ac.ERR_INVALID_ARG
     assert ac.attn_core_dropout_add_ln_fwd(p, 0, *([FAKE] * 7), 0) == ac.ERR_INVALID_ARG
+
+
+# ------------------------------------------------ variable-length batches
+
+@pytest.mark.parametrize("cu_q,cu_k,causal", [
+    ([1, 5], None, True),              # table must start at 0
+    ([0, 5, 3], None, True),           # nondecreasing
+    ([0, 5], [0, 4], True),            # causal needs equal counts per sequence
+    ([0, 5, 9], [0, 0, 3], False),     # queries without keys
+])
+def test_varlen_rejects_bad_tables(lib, cu_q, cu_k, causal):
+    p = _p(causal=causal)
+    assert ac.attn_core_fwd_varlen(p, cu_q, cu_k, *([FAKE] * 5), 0) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_bwd_varlen_workspace_bytes(p, cu_q, cu_k) == 0
+
+
+def test_varlen_workspace_is_the_sum_of_the_sequences(lib):
+    p = _p(p_drop=0.1)
+    cu = [0, 200, 200, 300]            # lengths 200, 0 (skipped), 100
+    per = [ac.attn_core_bwd_workspace_bytes(_p(s=n, p_drop=0.1)) for n in (200, 100)]
+    assert ac.attn_core_bwd_varlen_workspace_bytes(p, cu, None) == sum((x + 255) // 256 * 256 for x in per)
+    pt = _p(p_drop=0.1)
+    pt.timing_events = FAKE           # per-kernel events are not offered for packed batches
+    assert ac.attn_core_fwd_varlen(pt, cu, None, *([FAKE] * 5), 0) == ac.ERR_INVALID_ARG
