@@ -307,20 +307,38 @@ dal_bwd_kernel(const DalArgs a)
     }
 }
 
-// dgamma and dbeta: column sums of the partial rows, in CTA order (deterministic).
+// dgamma and dbeta: column sums of the partial rows, in a fixed order
+// (bit-reproducible).  A CTA of 256 threads owns 32 columns: warp w sums the
+// partial rows w, w + 8, ... (lane = column; coalesced 128-byte loads), then
+// the eight warp sums are added in warp order.
 __global__ void __launch_bounds__(256)
 dal_reduce_kernel(const DalArgs a, int n_part)
 {
+    __shared__ float sg[8][32], sb[8][32];
     const int H = a.hidden;
-    const int c = blockIdx.x * 256 + threadIdx.x;
-    if (c >= H) return;
-    float sg = 0.f, sb = 0.f;
-    for (int p = 0; p < n_part; ++p) {
-        sg += a.partial[(size_t)p * H + c];
-        sb += a.partial[(size_t)(n_part + p) * H + c];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
+    float g = 0.f, b = 0.f;
+    if (c < H) {
+#pragma unroll 4
+        for (int p = w; p < n_part; p += 8) {
+            g += a.partial[(size_t)p * H + c];
+            b += a.partial[(size_t)(n_part + p) * H + c];
+        }
     }
-    a.dgamma[c] = sg;
-    a.dbeta[c] = sb;
+    sg[w][lane] = g;
+    sb[w][lane] = b;
+    __syncthreads();
+    if (w == 0 && c < H) {
+        float tg = 0.f, tb = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            tg += sg[k][lane];
+            tb += sb[k][lane];
+        }
+        a.dgamma[c] = tg;
+        a.dbeta[c] = tb;
+    }
 }
 
 namespace {
@@ -363,7 +381,7 @@ int launch_bwd_nv(bool drop, const DalArgs& a, int sms, cudaStream_t st)
     if (int rc = resident_grid(kern, NT, smem, sms, cap, &grid)) return rc;
     kern<<<grid, NT, smem, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return (int)cudaErrorLaunchFailure;
-    dal_reduce_kernel<<<(a.hidden + 255) / 256, 256, 0, st>>>(a, grid);
+    dal_reduce_kernel<<<(a.hidden + 31) / 32, 256, 0, st>>>(a, grid);
     return (int)cudaGetLastError();
 }
 
