@@ -20,6 +20,11 @@
 //   bwd_dkdv  one (KV head, 128-key block) per CTA; keys on TMEM lanes; loops
 //             over the query heads of the GQA group and their query tiles;
 //             recomputes S^T and dP^T, accumulates dV and dK in TMEM
+// The dropout mask is drawn once per backward where the workspace has room
+// for it (d <= 128): bwd_dq stores its keep decisions as bits (one 32-bit
+// word per query row and 32 keys), and bwd_dkdv loads them with its query
+// tiles and transposes them to its key-major lanes (mask_pair_word gives the
+// layout).  Otherwise bwd_dkdv draws the mask again, transposed.
 // Neither gradient kernel writes a partial sum to global memory: each output
 // tile is finished in TMEM and stored once.
 #include "kernels.h"

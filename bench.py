@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -75,13 +76,23 @@ def _peaks():
     return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (the kernel sources
+    hold no string literal with a comment marker in it)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+
+
 def _csrc_hash() -> str:
+    """Hash of the kernel sources, comments aside: a profile taken on them stays
+    valid until their code changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_core_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as f:
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
             h.update(fn.encode())
-            h.update(f.read())
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:12]
 
 

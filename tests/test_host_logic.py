@@ -59,3 +59,11 @@ def test_traffic_lookup_reads_only_matching_hash(tmp_path, monkeypatch):
     assert bench._traffic("attn_bwd_dq_kernel", "gpt175b") is None      # taken on other sources
     assert bench._traffic("attn_fwd_kernel", "tiny") is None
     assert os.path.isdir(real_root)
+
+
+def test_source_hash_ignores_comments_only():
+    a = "// header\nint f() { return 1; }  // trailing\n/* block\n comment */\nint g;\n"
+    b = "int f() { return 1; }\n\nint g;\n"
+    c = "int f() { return 2; }\nint g;\n"
+    assert bench._strip_comments(a) == bench._strip_comments(b)
+    assert bench._strip_comments(a) != bench._strip_comments(c)
