@@ -222,3 +222,25 @@ def test_varlen_workspace_is_the_sum_of_the_sequences(lib):
     pt = _p(p_drop=0.1)
     pt.timing_events = FAKE           # per-kernel events are not offered for packed batches
     assert ac.attn_core_fwd_varlen(pt, cu, None, *([FAKE] * 5), 0) == ac.ERR_INVALID_ARG
+
+
+def test_bwd_workspace_formula_of_the_header(lib):
+    """8 b h_q ceil(s/128) 128 bytes of row statistics, plus (p > 0, d <= 128)
+    2048 b h_q N bytes of keep bits, N = n(n+1)/2 causal blocks per head or
+    ceil(s/128) ceil(s_kv/128), as the public header states."""
+    rng = __import__("random").Random(7)
+    for _ in range(200):
+        b, hkv = rng.randint(1, 4), rng.randint(1, 3)
+        hq = hkv * rng.randint(1, 4)
+        s = rng.randint(1, 3000)
+        d = rng.choice([64, 96, 128, 160])
+        causal = rng.random() < 0.5
+        skv = s if causal else rng.choice([0, rng.randint(1, 3000)])
+        p_drop = rng.choice([0.0, 0.1])
+        kv = skv or s
+        n, nk = -(-s // 128), -(-kv // 128)
+        stats = 8 * b * hq * n * 128
+        blocks = n * (n + 1) // 2 if causal else n * nk
+        bits = 2048 * b * hq * blocks if (p_drop > 0 and d <= 128) else 0
+        p = ac.Params(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=causal, p_drop=p_drop, s_kv=skv)
+        assert ac.attn_core_bwd_workspace_bytes(p) == stats + bits, (b, hq, hkv, s, skv, d, causal, p_drop)
