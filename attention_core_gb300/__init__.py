@@ -24,7 +24,7 @@ __all__ = [
     "attn_core_bwd_recompute_noalloc",
     "fwd", "bwd_recompute", "stored_bytes", "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED",
     "ERR_MISALIGNED", "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
-    "FLAG_TEST_WAIT_TIMEOUT", "SUPPORTED_HEAD_DIMS",
+    "FLAG_TEST_WAIT_TIMEOUT", "FLAG_REDRAW_MASK", "SUPPORTED_HEAD_DIMS",
     "DalParams", "attn_core_dropout_add_ln_fwd", "attn_core_dropout_add_ln_bwd",
     "attn_core_dropout_add_ln_bwd_workspace_bytes", "dropout_add_ln_fwd", "dropout_add_ln_bwd",
     "attn_core_gelu_fwd", "attn_core_gelu_bwd", "gelu_fwd", "gelu_bwd",
@@ -39,6 +39,7 @@ ERR_MISALIGNED = 3
 ERR_WORKSPACE_TOO_SMALL = 4
 ERR_CUDA = 5
 ERR_DEVICE_TIMEOUT = 6
+FLAG_REDRAW_MASK = 0x1
 FLAG_TEST_WAIT_TIMEOUT = 0x100
 SUPPORTED_HEAD_DIMS = (64, 96, 128, 160)
 

@@ -180,7 +180,7 @@ size_t padded_rows(const attn_core_params* p)
 // writing the bits would cost the dQ kernel some: that case draws twice.
 size_t mask_bytes(const attn_core_params* p)
 {
-    if (drop_threshold(p->p_drop) == 0 || p->d > 128) return 0;
+    if (drop_threshold(p->p_drop) == 0 || p->d > 128 || (p->flags & ATTN_CORE_FLAG_REDRAW_MASK)) return 0;
     const ac::CommonArgs c = common_args(p);
     return sizeof(uint32_t) * ac::mask_ws_words(c);
 }
@@ -369,6 +369,8 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
     return bwd_impl(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, true, stream);
 }
 
+}  // extern "C"
+
 // ---------------------------------------------------------------------------
 // Variable-length (packed) batches: one launch per sequence, each over that
 // sequence's rows of the packed tensors.
@@ -488,8 +490,17 @@ int attn_core_bwd_varlen(const attn_core_varlen_params* vp, const void* q, const
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     for (int i = 0; i < vp->n_seq; ++i) {
         const attn_core_params ps = seq_params(vp, i);
-        if (ps.s == 0) continue;
         const size_t qo = (size_t)cq[i] * hq * d, ko = (size_t)ck[i] * hkv * d;
+        if (ps.s == 0) {
+            // No query sees these keys: their gradients are zero.
+            const size_t nb = (size_t)ps.s_kv * hkv * d * sizeof(uint16_t);
+            if (nb && (cudaMemsetAsync(static_cast<uint16_t*>(dk) + ko, 0, nb, reinterpret_cast<cudaStream_t>(stream)) !=
+                           cudaSuccess ||
+                       cudaMemsetAsync(static_cast<uint16_t*>(dv) + ko, 0, nb, reinterpret_cast<cudaStream_t>(stream)) !=
+                           cudaSuccess))
+                return ATTN_CORE_ERR_CUDA;
+            continue;
+        }
         rc = bwd_launch(&ps, seq_geometry(vp, i, tq), static_cast<const uint16_t*>(q) + qo,
                         static_cast<const uint16_t*>(k) + ko, static_cast<const uint16_t*>(v) + ko,
                         static_cast<const uint16_t*>(o) + qo, lse + cq[i], static_cast<const uint16_t*>(dout) + qo,
@@ -642,12 +653,15 @@ int attn_core_gelu_bwd(int64_t n, const void* x, const void* dy, void* dx, void*
 
 // Backward for callers that cannot allocate device memory.  Its workspace is a
 // fixed array of this library's own, 2 * kNoAllocMaxRows fp32 values (8 MiB),
-// which every GPU that loads the library holds until the process exits.  The
-// array's name is only a host-side stand-in in host code; the device address
-// is looked up once per device with cudaGetSymbolAddress and then reused.
+// which every GPU that loads the library holds until the process exits.  In
+// host code the array's name is only a host-side stand-in: every call looks up
+// its device address for the current device with cudaGetSymbolAddress (which
+// allocates nothing) and passes that address to the kernels, so the address is
+// never stale, not even after the device's context has been reset.
 static constexpr size_t kNoAllocMaxRows = (size_t)1 << 20;
 static __device__ __align__(256) float g_noalloc_scratch[2 * kNoAllocMaxRows];
-static void* g_noalloc_addr[128];
+
+extern "C" {
 
 int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, const void* k, const void* v,
                                     const void* o, const float* lse, const void* dout, void* dq, void* dk,
@@ -656,19 +670,12 @@ int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, co
     int rc = check_params(p);
     if (rc) return rc;
     if (padded_rows(p) > kNoAllocMaxRows) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_CORE_ERR_CUDA;
-    if (dev < 0 || dev >= 128) return ATTN_CORE_ERR_UNSUPPORTED;
-    if (g_noalloc_addr[dev] == nullptr) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
-            return ATTN_CORE_ERR_CUDA;
-        g_noalloc_addr[dev] = addr;
-    }
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) return ATTN_CORE_ERR_CUDA;
     // The fixed array holds the two row statistics only; the dK/dV kernel draws
     // its own mask.
-    return bwd_impl(p, q, k, v, o, lse, dout, dq, dk, dv, g_noalloc_addr[dev], sizeof(float) * 2 * kNoAllocMaxRows,
-                    false, stream);
+    return bwd_impl(p, q, k, v, o, lse, dout, dq, dk, dv, addr, sizeof(float) * 2 * kNoAllocMaxRows, false,
+                    stream);
 }
 
 }  // extern "C"

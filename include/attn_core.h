@@ -66,6 +66,11 @@ extern "C" {
 #define ATTN_CORE_ERR_DEVICE_TIMEOUT 6      /* a kernel wait ran past its limit (reported via dev_status) */
 
 /* flags */
+#define ATTN_CORE_FLAG_REDRAW_MASK 0x1         /* backward: the dK/dV kernel draws the dropout mask again
+                                                  instead of reading keep bits the dQ kernel wrote to the
+                                                  workspace; the workspace then holds only the row
+                                                  statistics (smaller, see attn_core_bwd_workspace_bytes)
+                                                  at the cost of a second Philox pass */
 #define ATTN_CORE_FLAG_TEST_WAIT_TIMEOUT 0x100 /* test hook: every kernel waits on a barrier that nothing
                                                   completes; it gives up after wait_timeout_ms, writes
                                                   ATTN_CORE_ERR_DEVICE_TIMEOUT to dev_status and exits */
@@ -119,7 +124,10 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
  *   2048 * b * h_q * N                  the dropout keep bits, one bit per
  *                                       (query, key) of each 128 x 128 block,
  * with N = n (n + 1) / 2 blocks per head if causal (n = ceil(s / 128)), else
- * ceil(s / 128) * ceil(s_kv / 128). */
+ * ceil(s / 128) * ceil(s_kv / 128).  The keep bits are transient (written and
+ * read within one backward call) but scale with s^2: 6.7 MB for b = 2,
+ * h_q = 12, s = 2048, and 272 MB for h_q = 64, s = 8192.  Callers short of
+ * memory set ATTN_CORE_FLAG_REDRAW_MASK to leave them out. */
 size_t attn_core_bwd_workspace_bytes(const attn_core_params* p);
 
 /* Backward with recomputation: dQ, dK, dV from Q, K, V, O, LSE and dO.  The
@@ -154,9 +162,11 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
  * kernel draws the dropout mask again from Philox (the same bits).  Limit: b * h_q * ceil(s / 128) * 128 <= 1048576 padded query
  * rows (the array holds 8 MiB on every GPU that loads the library, until the
  * process exits); larger shapes return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL
- * without launching anything.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  All calls on a device
+ * without launching anything.  Every call looks up the array's device
+ * address for the current device (cudaGetSymbolAddress, which allocates
+ * nothing); the first call on a device may make the runtime load this
+ * library's device code there, so make that first call before any stream
+ * capture.  All calls on a device
  * share the one array and it keeps the last call's contents (nothing in it
  * needs to start at zero), so calls whose kernels overlap on the GPU --
  * concurrent streams, or several host threads -- race on it: order them. */
@@ -176,7 +186,8 @@ int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, co
  * key counts per sequence), and the same dropout mask (Philox counter word 2
  * = i * h_q + head).  The sequence tables are HOST arrays of n_seq + 1 int32
  * starting at 0 and nondecreasing; an empty sequence is skipped, one with
- * queries but no keys is invalid.  `base` supplies h_q, h_kv, d, causal,
+ * queries but no keys is invalid; one with keys but no queries gets zero
+ * dK and dV rows.  `base` supplies h_q, h_kv, d, causal,
  * p_drop, scale, seed, offset, dev_status, flags and wait_timeout_ms; its b,
  * s and s_kv are ignored and its timing_events must be NULL.  The kernels
  * run one sequence after another on `stream` (the same kernels as the

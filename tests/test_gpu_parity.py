@@ -158,6 +158,39 @@ def test_backward_mask_through_dq(causal):
         assert row_rel_err(dq, rdq) <= TOL
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_redraw_flag_matches_oracle_and_mask(d):
+    """ATTN_CORE_FLAG_REDRAW_MASK: the dK/dV kernel draws the mask itself
+    instead of reading the dQ kernel's keep bits; the workspace shrinks to the
+    row statistics, the gradients match the oracle, and the transposed draw
+    is bit-exact through the dV probe."""
+    b, h, s, p, seed = 1, 2, 300, 0.1, 606 + d
+    flags = ac.FLAG_REDRAW_MASK
+    full = ac.attn_core_bwd_workspace_bytes(ac.Params(b=b, h_q=h, h_kv=h, s=s, d=d, p_drop=p))
+    small = ac.attn_core_bwd_workspace_bytes(ac.Params(b=b, h_q=h, h_kv=h, s=s, d=d, p_drop=p, flags=flags))
+    assert small == 8 * b * h * 384 and full > small
+    t = random_inputs(b, h, h, s, d, seed=d + 1)
+    dev = torch.device("cuda:0")
+    q, k, v, g = (x.to(dev) for x in (t.q, t.k, t.v, t.dout))
+    kw = dict(causal=True, p_drop=p, seed=seed, flags=flags)
+    o, lse = ac.fwd(q, k, v, **kw)
+    dq, dk, dv = ac.bwd_recompute(q, k, v, o, lse, g, **kw)
+    pr = oracle.Problem(b=b, h_q=h, h_kv=h, s=s, d=d, causal=True, p_drop=p, seed=seed)
+    rdq, rdk, rdv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    for name, got, ref in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv)):
+        assert row_rel_err(to_np(got), ref) <= TOL, name
+    masks = [oracle.mask_rows(pr, bh, 0, s) for bh in range(b * h)]
+    for w0 in range(0, s, d):
+        tp = dv_mask_probe(b, h, h, s, d, w0)
+        qp, kp, vp, gp = (x.to(dev) for x in (tp.q, tp.k, tp.v, tp.dout))
+        op, lp = ac.fwd(qp, kp, vp, **kw)
+        dvp = to_np(ac.bwd_recompute(qp, kp, vp, op, lp, gp, **kw)[2]).reshape(b * h, s, d)
+        width = min(d, s - w0)
+        for bh in range(b * h):
+            got = (dvp[bh, :, :width] != 0).astype(np.uint8)
+            assert np.array_equal(got, masks[bh][w0:w0 + width, :].T), (bh, w0)
+
+
 def test_deterministic():
     """No atomics anywhere: two runs give identical bits."""
     t = random_inputs(1, 4, 2, 384, 128, seed=3)

@@ -115,3 +115,43 @@ def test_equal_lengths_match_padded_layout_bit_for_bit(d):
     assert torch.equal(lse2, lse.permute(1, 0, 2).reshape(h, b * s))
     for x, y in ((dq2, dq), (dk2, dk), (dv2, dv)):
         assert torch.equal(x, pack(y))
+
+
+def test_sequence_without_queries_gets_zero_key_gradients():
+    """A cross-attention sequence with keys but no queries: no query sees its
+    keys, so their dK and dV rows are zero -- written as zeros, whatever the
+    output buffers held before the call.  The other sequence still matches
+    the oracle."""
+    lq, lk, hq, hkv, d, p = [0, 100], [50, 80], 2, 2, 64, 0.1
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    q, do = _packed(lq, hq, d, gen), _packed(lq, hq, d, gen)
+    k, v = _packed(lk, hkv, d, gen), _packed(lk, hkv, d, gen)
+    cq, ck = _cu(lq), _cu(lk)
+    seed = 31337
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    pr_c = ac.Params(b=1, h_q=hq, h_kv=hkv, s=1, d=d, causal=False, p_drop=p, seed=seed)
+    o, lse = ac.fwd_varlen(qd, kd, vd, cq, ck, causal=False, p_drop=p, seed=seed)
+    dq = torch.empty_like(qd)
+    dk = torch.full_like(kd, 1.0)
+    dv = torch.full_like(vd, -2.0)
+    ws_bytes = ac.attn_core_bwd_varlen_workspace_bytes(pr_c, cq, ck)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    rc = ac.attn_core_bwd_varlen(pr_c, cq, ck, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), dod.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert rc == ac.OK, ac.attn_core_strerror(rc)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk[:50]).item() == 0
+    assert torch.count_nonzero(dv[:50]).item() == 0
+    i = 1
+    pr = _seq_problem(i, lq[i], lk[i], hq, hkv, d, False, p, seed)
+    qb, dob = _as_batch(q, cq[i], cq[i + 1], i, hq), _as_batch(do, cq[i], cq[i + 1], i, hq)
+    kb, vb = _as_batch(k, ck[i], ck[i + 1], i, hkv), _as_batch(v, ck[i], ck[i + 1], i, hkv)
+    bkv = np.repeat(np.arange(i * hkv, (i + 1) * hkv), lk[i])
+    krows = np.tile(np.arange(lk[i]), hkv)
+    rdk, rdv = oracle.dkdv_rows(pr, qb, kb, vb, dob, bkv, krows)
+    gdk = to_np(dk)[ck[i]:ck[i + 1]].transpose(1, 0, 2).reshape(-1, d)
+    gdv = to_np(dv)[ck[i]:ck[i + 1]].transpose(1, 0, 2).reshape(-1, d)
+    assert row_rel_err(gdk, rdk) <= TOL
+    assert row_rel_err(gdv, rdv) <= TOL
