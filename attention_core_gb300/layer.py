@@ -84,15 +84,69 @@ def _tokens(x4d, shape: LayerShape):
     return x4d.permute(0, 2, 1, 3).reshape(shape.n, shape.a * shape.d).contiguous()
 
 
-def forward(shape: LayerShape, wts: dict, y_in, r_in, seed: int, offset: int = 0):
+class StoredCore:
+    """The attention core without recomputation, for the measurement only: the
+    forward materialises and keeps what the backward needs -- the softmax
+    output P (bf16), the dropout mask (one byte per element) and the dropout
+    output (bf16), the 5 a s^2 b bytes of the per-layer activation formula --
+    and the backward reads them instead of rebuilding them.  Built from
+    cuBLAS products and PyTorch's softmax and dropout; its mask comes from
+    PyTorch's generator, not this library's Philox stream, so it computes the
+    same function as the library's core only in distribution when p > 0 (and
+    exactly, up to rounding, at p = 0).  It is the baseline against which
+    recomputation is an overhead, not part of the library's path."""
+
+    def __init__(self, shape: "LayerShape"):
+        import torch
+        self.shape = shape
+        self.scale = 1.0 / float(shape.d) ** 0.5
+        self._above = None
+        self.torch = torch
+
+    def _causal(self, dev):
+        if self._above is None:
+            s = self.shape.s
+            self._above = self.torch.ones((s, s), dtype=self.torch.bool, device=dev).triu(1)
+        return self._above
+
+    def fwd(self, q, k, v):
+        torch = self.torch
+        s_ = torch.matmul(q, k.transpose(-1, -2))
+        s_ = s_.float().mul_(self.scale).masked_fill_(self._causal(q.device), float("-inf"))
+        p = torch.softmax(s_, dim=-1).to(torch.bfloat16)
+        pd, mask = torch.ops.aten.native_dropout(p, self.shape.p_drop, True)
+        o = torch.matmul(pd, v)
+        return o, (q, k, v, p, mask, pd)
+
+    def bwd(self, saved, do):
+        torch = self.torch
+        q, k, v, p, mask, pd = saved
+        dv = torch.matmul(pd.transpose(-1, -2), do)
+        dpd = torch.matmul(do, v.transpose(-1, -2))
+        keep = 1.0 / (1.0 - self.shape.p_drop)
+        dp = torch.ops.aten.native_dropout_backward(dpd, mask, keep)
+        ds = torch.ops.aten._softmax_backward_data(dp, p, -1, torch.bfloat16)
+        dq = torch.matmul(ds, k) * self.scale
+        dk = torch.matmul(ds.transpose(-1, -2), q) * self.scale
+        return dq, dk, dv
+
+
+def forward(shape: LayerShape, wts: dict, y_in, r_in, seed: int, offset: int = 0, stored: "StoredCore" = None):
     """Returns (y2, z2, ctx); ctx holds what the backward needs.  The three
-    dropouts use Philox counter offsets offset, offset + 1 and offset + 2."""
+    dropouts use Philox counter offsets offset, offset + 1 and offset + 2.
+    With `stored`, the core is that no-recomputation baseline instead of this
+    library's recomputing core."""
     import torch
     ad = shape.a * shape.d
     qkv = torch.matmul(y_in, wts["wqkv"])
     q, k, v = (_heads(qkv[:, i * ad:(i + 1) * ad], shape) for i in range(3))
     core = dict(causal=True, p_drop=shape.p_drop, seed=seed, offset=offset)
-    o, lse = ac.fwd(q, k, v, **core)
+    if stored is not None:
+        o, saved = stored.fwd(q, k, v)
+        lse = None
+        core = dict(core, stored=stored, saved=saved)
+    else:
+        o, lse = ac.fwd(q, k, v, **core)
     o2 = _tokens(o, shape)
     attn = torch.matmul(o2, wts["wo"])
     d1 = dict(p_drop=shape.p_drop, seed=seed, offset=offset + 1, eps=shape.eps)
@@ -122,9 +176,21 @@ def backward(shape: LayerShape, wts: dict, ctx: dict, dy2, dz2):
                                                           dz_next=dz1, **c["d1"])
     do2 = torch.matmul(dattn, wts["wo"].t())
     dwo = torch.matmul(c["o2"].t(), dattn)
-    dq, dk, dv = ac.bwd_recompute(c["q"], c["k"], c["v"], c["o"], c["lse"], _heads(do2, shape), **c["core"])
+    if "stored" in c["core"]:
+        dq, dk, dv = c["core"]["stored"].bwd(c["core"]["saved"], _heads(do2, shape))
+    else:
+        dq, dk, dv = ac.bwd_recompute(c["q"], c["k"], c["v"], c["o"], c["lse"], _heads(do2, shape), **c["core"])
     dqkv = torch.cat([_tokens(t, shape) for t in (dq, dk, dv)], dim=1)
     dy_in = torch.matmul(dqkv, wts["wqkv"].t())
     dwqkv = torch.matmul(c["y_in"].t(), dqkv)
     return {"y_in": dy_in, "r_in": dr_in, "wqkv": dwqkv, "wo": dwo, "w1": dw1, "w2": dw2,
             "gamma1": dgamma1, "beta1": dbeta1, "gamma2": dgamma2, "beta2": dbeta2}
+
+
+def backward_full(shape: LayerShape, wts: dict, y_in, r_in, dy2, dz2, seed: int, offset: int = 0):
+    """Full activation recomputation: the forward kept only the layer's inputs
+    (y_in, r_in), so the backward first reruns the whole layer forward from
+    them (the same seed and offsets, so the same masks) and then runs the
+    backward on what that rerun produced."""
+    _, _, ctx = forward(shape, wts, y_in, r_in, seed=seed, offset=offset)
+    return backward(shape, wts, ctx, dy2, dz2)

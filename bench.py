@@ -386,6 +386,11 @@ def run_ours(args, w):
     if not args.no_layer and rank == 0:
         layer_study = _layer_study(dev, stream)
 
+    # every workload configuration, timed in this run
+    per_config = None
+    if not args.no_per_config and rank == 0:
+        per_config = _per_config(dev, stream)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -422,6 +427,8 @@ def run_ours(args, w):
             "cuda_graph": graph,
             "dropout_add_ln": dal,
             "layer_study": layer_study,
+            "per_config": per_config,
+            "bwd_workspace_bytes": ws_bytes,
             "gpu_launches": 3 * K,
             "kernel_ms_sampled": f"per-kernel events on every {EVERY}th timed step ({len(kt['fwd'])} samples)",
             "clocks": clocks,
@@ -430,6 +437,107 @@ def run_ours(args, w):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+PER_CONFIG = ["tiny", "gpt22b", "gpt175b", "gpt530b", "llama70b_p0", "llama70b_p01"]
+
+
+def _core_bytes(w) -> dict:
+    """Algorithmic HBM bytes of one step: the forward reads Q, K, V and writes
+    O and the LSE; the backward reads Q, K, V, O, dO and the LSE and writes dQ,
+    dK, dV (bf16 tensors, fp32 LSE)."""
+    q = 2 * w["b"] * w["h_q"] * w["s"] * w["d"]
+    kv = 2 * w["b"] * w["h_kv"] * w["s"] * w["d"]
+    lse = 4 * w["b"] * w["h_q"] * w["s"]
+    return {"fwd": q + 2 * kv + q + lse, "bwd": 3 * q + 2 * kv + lse + q + 2 * kv}
+
+
+def _per_config(dev, stream, steps: int = 20, warmup: int = 3):
+    """Every workload configuration, timed in this run: the whole step with
+    events around `steps` back-to-back steps, and each kernel with the ABI's
+    timing events on a second pass of `steps` steps.  Inputs rotate over sets
+    larger than L2 in total.  TFLOP/s are algorithmic (fwd 4 d, bwd 10 d per
+    visible pair); the tiny configuration is latency-bound and also reports
+    its algorithmic bytes over the step time."""
+    import torch
+
+    import attention_core_gb300 as ac
+    from attention_core_gb300.inputs import random_inputs
+    pk = _peaks()
+    out = {}
+    for name in PER_CONFIG:
+        w = _workload(name)
+        b, hq, hkv, s, d, p = w["b"], w["h_q"], w["h_kv"], w["s"], w["d"], w["p_drop"]
+        fl = _flops(w)
+        pr = ac.Params(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=True, p_drop=p, seed=0x5EED + len(out))
+        ws_bytes = ac.attn_core_bwd_workspace_bytes(pr)
+        base = random_inputs(b, hq, hkv, s, d, seed=PER_CONFIG.index(name))
+        per_set = 2 * (4 * b * hq * s * d + 4 * b * hkv * s * d) + 4 * b * hq * s + ws_bytes
+        n_sets = max(1, math.ceil(3 * L2_BYTES / per_set))
+        sets = []
+        for _ in range(n_sets):
+            q, k, v, g = (x.to(dev) for x in (base.q, base.k, base.v, base.dout))
+            sets.append(dict(q=q, k=k, v=v, g=g, o=torch.empty_like(q),
+                             lse=torch.empty((b, hq, s), dtype=torch.float32, device=dev),
+                             dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                             ws=torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)))
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        pr.dev_status = status.data_ptr()
+        sh = stream.cuda_stream
+
+        def step(t, ev=0):
+            pr.timing_events = ev
+            rc = ac.attn_core_fwd(pr, t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(), t["o"].data_ptr(),
+                                  t["lse"].data_ptr(), sh)
+            if rc:
+                raise ac.AttnCoreError(rc, "attn_core_fwd")
+            pr.timing_events = ev + 2 * ctypes.sizeof(ctypes.c_void_p) if ev else 0
+            rc = ac.attn_core_bwd_recompute(pr, t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(),
+                                            t["o"].data_ptr(), t["lse"].data_ptr(), t["g"].data_ptr(),
+                                            t["dq"].data_ptr(), t["dk"].data_ptr(), t["dv"].data_ptr(),
+                                            t["ws"].data_ptr(), ws_bytes, sh)
+            if rc:
+                raise ac.AttnCoreError(rc, "attn_core_bwd_recompute")
+
+        for i in range(warmup):
+            step(sets[i % n_sets])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(steps):
+            step(sets[i % n_sets])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6 * steps)]
+        for e in evs:
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        arr = (ctypes.c_void_p * len(evs))(*[e.cuda_event for e in evs])
+        for i in range(steps):
+            step(sets[i % n_sets], ctypes.addressof(arr) + 6 * i * ctypes.sizeof(ctypes.c_void_p))
+        torch.cuda.synchronize(dev)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item()):#x} in configuration {name}")
+        kms = {}
+        for j, kn in enumerate(("fwd", "dq", "dkdv")):
+            kms[kn] = sum(evs[6 * i + 2 * j].elapsed_time(evs[6 * i + 2 * j + 1]) for i in range(steps)) / steps
+        fwd_ms, bwd_ms = kms["fwd"], kms["dq"] + kms["dkdv"]
+        tf = fl["total"] / (ms / 1e3) / 1e12
+        entry = {"b": b, "h_q": hq, "h_kv": hkv, "s": s, "d_head": d, "p_drop": p,
+                 "ms_per_step": ms, "kernel_ms": {k: round(v, 4) for k, v in kms.items()},
+                 "fwd_tflops": fl["fwd"] / (fwd_ms / 1e3) / 1e12,
+                 "bwd_tflops": fl["bwd"] / (bwd_ms / 1e3) / 1e12,
+                 "combined_tflops": tf, "pct_of_bf16_peak": 100.0 * tf / pk["bf16_tflops"],
+                 "bwd_workspace_bytes": ws_bytes, "steps": steps, "input_sets": n_sets}
+        if name == "tiny":
+            cb = _core_bytes(w)
+            entry["gbs"] = (cb["fwd"] + cb["bwd"]) / (ms / 1e3) / 1e9
+            entry["pct_of_hbm"] = 100.0 * entry["gbs"] / pk["hbm_gbs"]
+        out[name] = entry
+        del sets
+        torch.cuda.empty_cache()
+    return out
 
 
 def _dal_measure(dev, stream, iters: int = 30):
@@ -483,13 +591,18 @@ def _dal_measure(dev, stream, iters: int = 30):
 
 def _layer_study(dev, stream, iters: int = 10):
     """One 175B-shaped layer shard (b=2, s=2048, h=12288, 12 local heads of 128,
-    MLP width 6144, p=0.1) through attention_core_gb300.layer: the layer's
-    forward, its backward (which recomputes the attention core) and the core's
-    forward alone, each the median of `iters` CUDA-event timings on the stream.
-    Overheads are relative to a step without recomputation, taken as the step
-    minus the core's forward time (an upper bound of what the backward spends
-    rebuilding the core): recomputing the core costs that core forward,
-    recomputing the whole layer (full recomputation) a whole layer forward."""
+    MLP width 6144, p=0.1) through attention_core_gb300.layer, three training
+    steps each timed (median of `iters` CUDA-event timings on the stream):
+      none       -- no recomputation: the core keeps its probabilities, mask and
+                    dropout output (layer.StoredCore, 5 a s^2 b bytes) and the
+                    backward reads them;
+      selective  -- this library's core: the forward keeps Q, K, V, O and the
+                    LSE, and the backward recomputes scores, probabilities and
+                    mask on chip;
+      full       -- only the layer input is kept: the backward reruns the whole
+                    layer forward first (layer.backward_full).
+    The overheads are ratios of these measured step times to the step without
+    recomputation."""
     import torch
 
     import attention_core_gb300 as ac
@@ -514,17 +627,31 @@ def _layer_study(dev, stream, iters: int = 10):
         torch.cuda.synchronize()
         return sorted(e0.elapsed_time(e1) for e0, e1 in evs)[iters // 2]
 
+    stored = layer.StoredCore(sh)
     _, _, ctx = layer.forward(sh, w, y_in, r_in, seed=seed)
     fwd_ms = timed(lambda: layer.forward(sh, w, y_in, r_in, seed=seed))
     bwd_ms = timed(lambda: layer.backward(sh, w, ctx, dy2, dz2))
     core_ms = timed(lambda: ac.fwd(ctx["q"], ctx["k"], ctx["v"], **ctx["core"]))
-    step = fwd_ms + bwd_ms
-    base = step - core_ms
+    del ctx
+    _, _, ctx_n = layer.forward(sh, w, y_in, r_in, seed=seed, stored=stored)
+    fwd_none_ms = timed(lambda: layer.forward(sh, w, y_in, r_in, seed=seed, stored=stored))
+    bwd_none_ms = timed(lambda: layer.backward(sh, w, ctx_n, dy2, dz2))
+    del ctx_n
+    bwd_full_ms = timed(lambda: layer.backward_full(sh, w, y_in, r_in, dy2, dz2, seed=seed))
+    step_none = fwd_none_ms + bwd_none_ms
+    step_sel = fwd_ms + bwd_ms
+    step_full = fwd_ms + bwd_full_ms
     sb = ac.stored_bytes(sh.b, sh.a, sh.a, sh.s, sh.d)
     return {"workload": "175B layer shard: b=2, s=2048, h=12288, 12 local heads of 128, MLP 6144, "
-                        "p=0.1; GEMMs by cuBLAS (torch.matmul), the rest by this library",
-            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms": step, "core_fwd_ms": core_ms,
-            "overhead_selective": core_ms / base, "overhead_full": fwd_ms / base,
+                        "p=0.1; GEMMs by cuBLAS (torch.matmul), the rest by this library; the "
+                        "no-recomputation core materialised with cuBLAS and PyTorch softmax/dropout",
+            "step_ms": {"none": step_none, "selective": step_sel, "full": step_full},
+            "fwd_ms": {"none": fwd_none_ms, "selective": fwd_ms, "full": fwd_ms},
+            "bwd_ms": {"none": bwd_none_ms, "selective": bwd_ms, "full": bwd_full_ms},
+            "core_fwd_ms": core_ms,
+            "overhead_selective": step_sel / step_none - 1.0,
+            "overhead_full": step_full / step_none - 1.0,
+            "full_over_selective": step_full / step_sel - 1.0,
             "gemm_fwd_tflops": sh.gemm_flops_fwd() / (fwd_ms / 1e3) / 1e12,
             "activation_bytes_per_layer": {k: sb[k] for k in ("layer_none", "layer_selective", "layer_full")}}
 
@@ -661,6 +788,8 @@ def main():
                     help="skip the dropout + residual add + layer norm measurement")
     ap.add_argument("--no-layer", action="store_true",
                     help="skip the layer-level recompute-overhead measurement")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other workload configurations")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the CPU-oracle baseline sample")
     args = ap.parse_args()

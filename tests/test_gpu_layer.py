@@ -97,3 +97,31 @@ def test_layer_matches_composed_oracles(dims):
         g = to_np(got[name])
         errs[name] = row_rel_err(g[None] if g.ndim == 1 else g, r[None] if r.ndim == 1 else r)
     assert all(e <= LAYER_TOL for e in errs.values()), errs
+
+
+def test_stored_core_baseline_computes_the_same_layer():
+    """The no-recomputation baseline core of the layer study (it keeps the
+    dense probabilities) computes the same layer as this library's core: at
+    p = 0 (where its own dropout mask plays no part) both match the composed
+    oracles."""
+    b, s, h, a, d, f = 1, 256, 512, 4, 64, 1024
+    sh = layer.LayerShape(b=b, s=s, h=h, a=a, d=d, ffn=f, p_drop=0.0)
+    dev = torch.device("cuda:0")
+    w = layer.init_weights(sh, seed=5, device=dev)
+    gen = torch.Generator(device="cpu").manual_seed(10)
+    y_in, r_in, dy2, dz2 = (torch.randn((sh.n, h), generator=gen).to(torch.bfloat16) for _ in range(4))
+    seed = 99
+    stored = layer.StoredCore(sh)
+    y2, z2, ctx = layer.forward(sh, w, y_in.to(dev), r_in.to(dev), seed=seed, stored=stored)
+    grads = layer.backward(sh, w, ctx, dy2.to(dev), dz2.to(dev))
+    full = layer.backward_full(sh, w, y_in.to(dev), r_in.to(dev), dy2.to(dev), dz2.to(dev), seed=seed)
+    torch.cuda.synchronize()
+    ref = _reference(sh, w, *(t.double().numpy() for t in (y_in, r_in, dy2, dz2)), seed=seed)
+    for got in ({"y2": y2, "z2": z2, **grads}, full):
+        errs = {}
+        for name, r in ref.items():
+            if name not in got:
+                continue
+            g = to_np(got[name])
+            errs[name] = row_rel_err(g[None] if g.ndim == 1 else g, r[None] if r.ndim == 1 else r)
+        assert all(e <= LAYER_TOL for e in errs.values()), errs
