@@ -7,6 +7,7 @@
 
 #include "../../include/attn_core.h"
 #include "kernels.h"
+#include "philox.cuh"
 #include "tile.cuh"
 
 namespace {
@@ -89,7 +90,20 @@ int check_params(const attn_core_params* p)
     return ATTN_CORE_OK;
 }
 
+// Dropout threshold of the attention core on an 8-bit draw: round(p * 256), at
+// most 255; an element is dropped iff its draw is below it.
 uint32_t drop_threshold(float p)
+{
+    if (!(p > 0.0f)) return 0u;
+    long long t = llround((double)p * 256.0);
+    if (t > 255) t = 255;
+    if (t < 0) t = 0;
+    return (uint32_t)t;
+}
+
+// The dropout + layer norm block's threshold on a 16-bit draw: round(p * 65536),
+// at most 65535.
+uint32_t drop_threshold16(float p)
 {
     if (!(p > 0.0f)) return 0u;
     long long t = llround((double)p * 65536.0);
@@ -113,9 +127,10 @@ ac::CommonArgs common_args(const attn_core_params* p)
     c.scale = scale;
     c.scale_log2 = scale * 1.44269504088896340736f;
     c.thr = drop_threshold(p->p_drop);
-    c.keep_scale = 1.0f / (1.0f - (float)c.thr / 65536.0f);
+    c.keep_scale = 1.0f / (1.0f - (float)c.thr / 256.0f);
     c.seed_lo = (uint32_t)(p->seed & 0xffffffffu);
     c.seed_hi = (uint32_t)(p->seed >> 32);
+    ac::philox_round_keys(c.seed_lo, c.seed_hi, c.rk);
     c.offset = (uint32_t)p->offset;
     c.status = p->dev_status;
     c.timeout_ns = (uint64_t)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;
@@ -535,10 +550,11 @@ ac::DalArgs dal_args(const attn_core_dal_params* p)
     a.n_rows = p->n_rows;
     a.hidden = p->hidden;
     a.eps = p->eps;
-    a.thr = drop_threshold(p->p_drop);
+    a.thr = drop_threshold16(p->p_drop);
     a.keep_scale = 1.0f / (1.0f - (float)a.thr / 65536.0f);
     a.seed_lo = (uint32_t)(p->seed & 0xffffffffu);
     a.seed_hi = (uint32_t)(p->seed >> 32);
+    ac::philox_round_keys(a.seed_lo, a.seed_hi, a.rk);
     a.offset = (uint32_t)p->offset;
     a.status = p->dev_status;
     a.timeout_ns = (uint64_t)(p->wait_timeout_ms ? p->wait_timeout_ms : 2000u) * 1000000ull;

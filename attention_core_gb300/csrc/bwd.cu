@@ -249,18 +249,18 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int key = kb * 128 + r;
         const uint32_t warp_key0 = (uint32_t)(kb * 128 + (int)(warp & 3u) * 32);
         const float* lse2_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
-        const KeepSwar ks(a.thr);
+        const KeepSwar8 ks(a.thr);
         const uint32_t zs_bits = __float_as_uint(a.keep_scale);
         const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DEL);
         // Keep bytes of this lane's key over the half's queries (transposed draw).  Those
         // of tile it + 1 are drawn right after tile it's dS, while the tensor core forms
         // S_{it+1}: the draw needs no score.
-        uint32_t klo[HQ / 8], khi[HQ / 8];
+        uint32_t kw[HQ / 16][4];
         auto draw_mask = [&](int it) {
             const int bh = bh0 + it / per_head;
             const int q0 = (qt0 + it % per_head) * BQ + HQ * h;
-            const PhiloxKey pk{a.seed_lo, a.seed_hi, (uint32_t)bh + a.bh0, a.offset, a.thr};
-            keep_bytes_col<HQ>(pk, ks, warp_key0 / 8u + lane / 8u, (uint32_t)q0, klo, khi);
+            const PhiloxKey pk{a.rk, (uint32_t)bh + a.bh0, a.offset};
+            keep_bytes_col16<HQ>(pk, ks, warp_key0 / 16u + lane / 16u, (uint32_t)q0, kw);
         };
         // With the dQ kernel's keep bits (MWS): this key's bits over the half's
         // queries, transposed from the staged rows and spread to byte sign bits
@@ -268,8 +268,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         uint32_t kbyte[HQ / 4] = {};
         auto pair_mask = [&](int e) -> uint32_t {
             if constexpr (MWS) return keep_pair_mask_nat(kbyte, e);
-            else return keep_pair_mask<HQ>(klo, khi, e);
+            else return keep_pair_mask_col<HQ>(kw, e);
         };
+        // The dQ kernel's words hold key 4k + b of a warp's 32 keys at bit 8b + 7 - k;
+        // after the transpose, lane p holds the queries of bit position p, so the lane
+        // of key L reads it from lane keep_bit_position(L).
+        const int src_lane = (int)keep_bit_position(lane);
         if (DROP && !MWS && n_it > 0) draw_mask(0);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
@@ -286,7 +290,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
                 for (int c = 0; c < HQ / 32; ++c) {
                     const int row = HQ * h + 32 * c + (int)lane;    // query row of the tile
-                    const uint32_t col = transpose32(msk[(row >> 6) * 256 + (int)(warp & 3u) * 64 + (row & 63)]);
+                    const uint32_t col = __shfl_sync(
+                        0xffffffffu, transpose32(msk[(row >> 6) * 256 + (int)(warp & 3u) * 64 + (row & 63)]), src_lane);
 #pragma unroll
                     for (int n = 0; n < 8; ++n) kbyte[8 * c + n] = keep_nibble_bytes((col >> (4 * n)) & 0xFu);
                 }
@@ -625,7 +630,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t lane_off = rt.lane_off;
         const int i = qb * 128 + r;
         const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
-        const uint32_t t16 = a.thr << 16;
         float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
         // Row statistics of this query: -LSE * log2(e) (-inf past s, so its
         // probabilities recompute to 0), and the first estimate
@@ -663,6 +667,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
         const uint64_t nl22 = f2_pack(nl2, nl2);
         const uint64_t dt2 = f2_pack(d_tilde, d_tilde);
+        const uint64_t ndt2 = f2_pack(-d_tilde, -d_tilde);
+        const uint64_t zs2 = f2_pack(a.keep_scale, a.keep_scale);
+        const KeepSwar8 ks(a.thr);
         uint64_t dacc2 = f2_pack(0.f, 0.f);
         for (int j = 0; j < nk && ok; ++j) {
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
@@ -714,30 +721,29 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int c32 = 0; c32 < HK / 32; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
+                // keep decisions of these 32 keys: two Philox calls of 16 keys, one SWAR
+                // test per output word (keys 4k .. 4k + 3 of the chunk in keep[k])
+                uint32_t keep[8];
+                if (DROP) {
+                    const uint32_t grp = (uint32_t)(key0 >> 4) + 2u * (uint32_t)c32;
+                    const uint4 w0 = philox4x32_10_rk(grp, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
+                    const uint4 w1 = philox4x32_10_rk(grp + 1u, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
+                    keep[0] = ks(w0.x); keep[1] = ks(w0.y); keep[2] = ks(w0.z); keep[3] = ks(w0.w);
+                    keep[4] = ks(w1.x); keep[5] = ks(w1.y); keep[6] = ks(w1.z); keep[7] = ks(w1.w);
+                }
                 uint32_t w[16];
-                uint32_t kbits = 0u;                       // keep bits of these 32 keys
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {          // 8 keys per Philox call
-                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+                for (int e = 0; e < 16; ++e) {               // pair e: keys 2e, 2e + 1 of the chunk
+                    const int ep = c32 * 16 + e;
+                    uint32_t dlo = rr[2 * e], dhi = rr[2 * e + 1];
                     if (DROP) {
-                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + c32 * 4 + g, (uint32_t)i,
-                                                       (uint32_t)bh + a.bh0,
-                                                       a.offset, a.seed_lo, a.seed_hi);
-                        wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
+                        // dropped elements' dP_d is cleared; kept ones carry 1/(1-p) below
+                        dlo &= keep_mask32(keep[e >> 1], 2 * (e & 1));
+                        dhi &= keep_mask32(keep[e >> 1], 2 * (e & 1) + 1);
                     }
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int e = 4 * g + t;               // pair within this chunk
-                        const int ep = c32 * 16 + e;
-                        uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                        if (DROP) dp = f2_mul(dp, keep_factor2(wv[t], t16, a.keep_scale));
-                        if (DROP && MWS) {
-                            kbits |= (((wv[t] << 16) >= t16) ? 1u : 0u) << (2 * e);
-                            kbits |= ((wv[t] >= t16) ? 1u : 0u) << (2 * e + 1);
-                        }
-                        dacc2 = f2_fma(pp[ep], dp, dacc2);
-                        w[e] = pack_bf16x2(f2_mul(pp[ep], f2_sub(dp, dt2)));
-                    }
+                    const uint64_t dp = f2_pack(__uint_as_float(dlo), __uint_as_float(dhi));
+                    dacc2 = f2_fma(pp[ep], dp, dacc2);
+                    w[e] = pack_bf16x2(f2_mul(pp[ep], DROP ? f2_fma(dp, zs2, ndt2) : f2_sub(dp, dt2)));
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
                 if constexpr (DROP && MWS) {
@@ -746,7 +752,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
                     const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
                                         (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
-                    args.mask_ws[word] = kbits;
+                    args.mask_ws[word] = keep_bits32(keep);
                 }
             }
             tmem_st_wait();
@@ -757,7 +763,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         {
             float lo, hi;
             f2_unpack(dacc2, lo, hi);
-            d_exact = lo + hi;
+            d_exact = DROP ? (lo + hi) * a.keep_scale : lo + hi;   // dP = Z dP_d, Z = keep / (1 - p)
         }
         // exact row statistic: the two halves' partial sums
         dred[h * 128 + r] = d_exact;

@@ -45,7 +45,7 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8])
 // Keep flags of the 8 columns 8v .. 8v + 7 of one row (bit e: column 8v + e).
 __device__ __forceinline__ uint32_t dal_keep8(const DalArgs& a, uint32_t v, uint32_t row)
 {
-    const uint4 w = philox4x32_10(v, row, kDalStream, a.offset, a.seed_lo, a.seed_hi);
+    const uint4 w = philox4x32_10_rk(v, row, kDalStream, a.offset, a.rk);
     const uint32_t t16 = a.thr << 16;
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
     uint32_t bits = 0;

@@ -384,42 +384,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     m_run = m_new;
                 }
-                // p = 2^(x * scale_log2 - m), two at a time, and the dropout mask, in eight
-                // independent units of 8 keys (one Philox call each) so that the exp2
+                // p = 2^(x * scale_log2 - m), two at a time, and the dropout mask, in four
+                // independent units of 16 keys (one Philox call each) so that the exp2
                 // (MUFU) and Philox (integer multiply) work of different units overlap;
-                // the row sum is taken before dropout.
+                // the row sum is taken before dropout.  A unit's keep decisions come out
+                // of one SWAR test per output word (four keys) as byte sign bits, which
+                // mask the packed bf16 pairs directly.
                 const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
                 const uint64_t nm2 = f2_pack(-m_run, -m_run);
-                const uint32_t t16 = a.thr << 16;
-                uint64_t acc2 = f2_pack(0.f, 0.f);
+                const KeepSwar8 ks(a.thr);
+                uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
                 uint32_t pw[32];
+                uint4 w4[4];
 #pragma unroll
-                for (int g8 = 0; g8 < 8; ++g8) {
-                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
-                    if (DROP) {
-                        const uint4 w4 = philox4x32_10((uint32_t)(key0 >> 3) + g8, (uint32_t)i, (uint32_t)bh + a.bh0,
-                                                       a.offset, a.seed_lo, a.seed_hi);
-                        wv[0] = w4.x; wv[1] = w4.y; wv[2] = w4.z; wv[3] = w4.w;
-                    }
+                for (int u16 = 0; u16 < 4; ++u16)
+                    w4[u16] = DROP ? philox4x32_10_rk((uint32_t)(key0 >> 4) + u16, (uint32_t)i, (uint32_t)bh + a.bh0,
+                                                    a.offset, a.rk)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u16 = 0; u16 < 4; ++u16) {
+                    const uint32_t wv[4] = {w4[u16].x, w4[u16].y, w4[u16].z, w4[u16].w};
 #pragma unroll
                     for (int tt = 0; tt < 4; ++tt) {
-                        const int e = 4 * g8 + tt;       // pair e: keys key0 + 2e, 2e + 1
-                        float lo, hi;
-                        f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), lo, hi);
-                        lo = ex2_approx(lo);
-                        hi = ex2_approx(hi);
-                        acc2 = f2_add(acc2, f2_pack(lo, hi));
-                        if (DROP) {
-                            // Philox word tt decides pair 4 g8 + tt (low half: even key, high: odd)
-                            lo = (wv[tt] << 16) >= t16 ? lo : 0.f;
-                            hi = wv[tt] >= t16 ? hi : 0.f;
+                        const uint32_t keep = DROP ? ks(wv[tt]) : 0u;   // keys 16 u16 + 4 tt .. + 3
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int e = 8 * u16 + 2 * tt + q;            // pair e: keys key0 + 2e, 2e + 1
+                            float lo, hi;
+                            f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), lo, hi);
+                            lo = ex2_approx(lo);
+                            hi = ex2_approx(hi);
+                            acc2[q] = f2_add(acc2[q], f2_pack(lo, hi));
+                            pw[e] = DROP ? pack_bf16x2(lo, hi) & keep_pair16(keep, q) : pack_bf16x2(lo, hi);
                         }
-                        pw[e] = pack_bf16x2(lo, hi);
                     }
                 }
                 {
                     float lo, hi;
-                    f2_unpack(acc2, lo, hi);
+                    f2_unpack(f2_add(acc2[0], acc2[1]), lo, hi);
                     l_run += lo + hi;
                 }
                 tmem_st32(tS, pw);   // P_d of these 64 keys over the first 32 of the half's columns

@@ -26,9 +26,10 @@ struct CommonArgs {
     int32_t causal;
     float scale_log2;     // score scale * log2(e)
     float scale;          // score scale
-    float keep_scale;     // 1 / (1 - thr / 65536)
-    uint32_t thr;         // dropout threshold on a 16-bit draw (0: no dropout)
+    float keep_scale;     // 1 / (1 - thr / 256)
+    uint32_t thr;         // dropout threshold on an 8-bit draw (0: no dropout)
     uint32_t seed_lo, seed_hi, offset;
+    uint32_t rk[20];      // Philox key schedule of the seed (philox_round_keys)
     int32_t* status;      // caller-owned device status word (may be null)
     uint64_t timeout_ns;  // limit of every in-kernel wait
     int32_t inject_timeout;  // test hook: every thread waits on a barrier nothing completes
@@ -63,8 +64,9 @@ struct BwdArgs {
 // Keep bits handed from the dQ kernel to the dK/dV kernel.  For every
 // (query head, 128-query block qb, 128-key block kb) that the causal mask does
 // not hide, two 1 KB units (query rows 0-63 and 64-127 of the block); unit
-// word [g * 64 + row] holds, in bit k, whether the pair (query row, key
-// 32 g + k of the block) is kept.  Returns the index of the pair's first word.
+// word [g * 64 + row] holds whether the pairs (query row, key 32 g + c of the
+// block) are kept, key c at bit keep_bit_position(c) (philox.cuh).  Returns
+// the index of the pair's first word.
 __host__ __device__ inline size_t mask_pair_word(const CommonArgs& a, int bh, int qb, int kb)
 {
     const size_t per_head = a.causal ? (size_t)a.n_blk * (a.n_blk + 1) / 2 : (size_t)a.n_blk * a.n_blk_k;
@@ -91,6 +93,7 @@ struct DalArgs {
     float keep_scale;     // 1 / (1 - thr / 65536)
     uint32_t thr;         // dropout threshold on a 16-bit draw (0: no dropout)
     uint32_t seed_lo, seed_hi, offset;
+    uint32_t rk[20];             // Philox key schedule of the seed (philox_round_keys)
     const uint16_t* x;           // fwd: sub-layer output entering the dropout
     const uint16_t* residual;    // fwd
     const float* gamma;          // fwd, bwd

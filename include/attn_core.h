@@ -32,12 +32,14 @@
  *   - LSE is in natural-log units.
  *   - dropout acts on the normalised probabilities, before the product with V.
  *   - dropout mask: Philox-4x32-10 (Salmon et al., SC'11) with key
- *     (seed & 0xffffffff, seed >> 32) and counter (j / 8, i, b*h_q + h,
+ *     (seed & 0xffffffff, seed >> 32) and counter (j / 16, i, b*h_q + h,
  *     offset) for query i, key j of query head h in batch b; the call's four
- *     output words give eight 16-bit draws, key j taking the low half (j even)
- *     or high half (j odd) of word (j % 8) / 2.  With thr = round(p * 65536)
- *     (at most 65535) an element is dropped iff its draw < thr, and kept
- *     elements are scaled by 1 / (1 - thr / 65536).  p == 0 draws nothing.
+ *     output words give sixteen 8-bit draws, key j taking byte j % 4 (bits
+ *     8 (j % 4) .. 8 (j % 4) + 7) of word (j % 16) / 4.  With
+ *     thr = round(p * 256) (at most 255) an element is dropped iff its draw <
+ *     thr, and kept elements are scaled by 1 / (1 - thr / 256): the effective
+ *     rate is p rounded to a multiple of 1/256 (p = 0.1 drops 26/256 =
+ *     0.1015625 of the elements; p < 1/512 drops none).  p == 0 draws nothing.
  *
  * Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  * default stream).  The library allocates no device memory: the caller owns
@@ -229,8 +231,13 @@ const char* attn_core_strerror(int code);
  *     z = residual + dropout(x)                            stored, bf16
  *     y = gamma * (z - mean) * rstd + beta                 bf16
  *     rstd = 1 / sqrt(var + eps), var the biased variance of the stored z.
- * Dropout follows the attention core's reading with counter (col / 8, row,
- * 0xFFFFFFFF, offset): word 2 is a value no attention head index takes.  As
+ * Dropout mask: Philox-4x32-10 with the core's key, counter (col / 8, row,
+ * 0xFFFFFFFF, offset) (word 2 is a value no attention head index takes) and
+ * eight 16-bit draws per call, column col taking the low (col even) or high
+ * (col odd) half of word (col % 8) / 2; dropped iff the draw <
+ * round(p * 65536) (at most 65535), kept values scaled by
+ * 1 / (1 - thr / 65536).  This block is bound by memory traffic, not by the
+ * generator, so it keeps the finer 16-bit draws.  As
  * in the core, the backward redraws the mask from (seed, offset); the block
  * keeps z, mean and rstd only.
  *

@@ -75,8 +75,10 @@ def _load():
         lib.oracle_philox4x32_10.argtypes = [_U32, _U32, _U32]
         lib.oracle_drop_threshold.argtypes = [ctypes.c_float]
         lib.oracle_drop_threshold.restype = ctypes.c_uint32
-        lib.oracle_draw16.argtypes = [_PP, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
-        lib.oracle_draw16.restype = ctypes.c_uint32
+        lib.oracle_drop_threshold16.argtypes = [ctypes.c_float]
+        lib.oracle_drop_threshold16.restype = ctypes.c_uint32
+        lib.oracle_draw8.argtypes = [_PP, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_draw8.restype = ctypes.c_uint32
         lib.oracle_keep.argtypes = [_PP, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
         lib.oracle_keep.restype = ctypes.c_int
         lib.oracle_resolved_scale.argtypes = [_PP]
@@ -157,11 +159,18 @@ def philox4x32_10(counter, key) -> np.ndarray:
 
 
 def drop_threshold(p_drop: float) -> int:
+    """The attention core's threshold on an 8-bit draw: round(p * 256), at most 255."""
     return int(_load().oracle_drop_threshold(ctypes.c_float(p_drop)))
 
 
-def draw16(pr: Problem, bh: int, i: int, j: int) -> int:
-    return int(_load().oracle_draw16(ctypes.byref(pr._c()), bh, i, j))
+def drop_threshold16(p_drop: float) -> int:
+    """The dropout + layer norm block's threshold on a 16-bit draw:
+    round(p * 65536), at most 65535."""
+    return int(_load().oracle_drop_threshold16(ctypes.c_float(p_drop)))
+
+
+def draw8(pr: Problem, bh: int, i: int, j: int) -> int:
+    return int(_load().oracle_draw8(ctypes.byref(pr._c()), bh, i, j))
 
 
 def keep(pr: Problem, bh: int, i: int, j: int) -> int:

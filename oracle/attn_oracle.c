@@ -16,7 +16,7 @@
  *     (selective) and 2d (full); "Memory for compute, selectively": the
  *     Llama 3 70B worked example.
  * The pages fix no precision, no mask generator and no scaling; the readings
- * taken here (fp64 everywhere, Philox-4x32-10 with 16-bit draws, natural-log
+ * taken here (fp64 everywhere, Philox-4x32-10 with 8-bit draws, natural-log
  * LSE, top-left causal alignment, GQA head h -> h / (h_q/h_kv)) are listed in
  * the project's design notes and in the public ABI header.
  *
@@ -93,9 +93,21 @@ void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], ui
     out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
 
-/* Drop threshold on a 16-bit draw: round(p * 65536), at most 65535.  An
- * element is dropped iff its draw is below the threshold. */
+/* Drop threshold on an 8-bit draw: round(p * 256), at most 255 (some draw
+ * always survives).  An element is dropped iff its draw is below the
+ * threshold, so the effective rate is threshold / 256. */
 uint32_t oracle_drop_threshold(float p_drop)
+{
+    if (!(p_drop > 0.0f)) return 0u;
+    long long t = llround((double)p_drop * 256.0);
+    if (t > 255) t = 255;
+    if (t < 0) t = 0;
+    return (uint32_t)t;
+}
+
+/* The same on a 16-bit draw, round(p * 65536) and at most 65535: the
+ * reading of the dropout + residual add + layer norm block's mask. */
+uint32_t oracle_drop_threshold16(float p_drop)
 {
     if (!(p_drop > 0.0f)) return 0u;
     long long t = llround((double)p_drop * 65536.0);
@@ -104,19 +116,18 @@ uint32_t oracle_drop_threshold(float p_drop)
     return (uint32_t)t;
 }
 
-/* The 16-bit draw for element (query i, key j) of flattened query head bh:
- * counter (j / 8, i, bh, offset), key (seed low word, seed high word); the
- * eight draws of one call cover keys 8*(j/8) .. 8*(j/8)+7, key j taking the
- * low half (j even) or high half (j odd) of output word (j mod 8) / 2. */
-uint32_t oracle_draw16(const oracle_params* p, int64_t bh, int64_t i, int64_t j)
+/* The 8-bit draw for element (query i, key j) of flattened query head bh:
+ * counter (j / 16, i, bh, offset), key (seed low word, seed high word); the
+ * sixteen draws of one call cover keys 16*(j/16) .. 16*(j/16)+15, key j
+ * taking byte (j mod 4) (byte 0 = bits 0..7) of output word (j mod 16) / 4. */
+uint32_t oracle_draw8(const oracle_params* p, int64_t bh, int64_t i, int64_t j)
 {
-    uint32_t ctr[4] = {(uint32_t)(j / 8), (uint32_t)i, (uint32_t)bh, (uint32_t)p->offset};
+    uint32_t ctr[4] = {(uint32_t)(j / 16), (uint32_t)i, (uint32_t)bh, (uint32_t)p->offset};
     uint32_t key[2] = {(uint32_t)(p->seed & 0xffffffffu), (uint32_t)(p->seed >> 32)};
     uint32_t w[4];
     oracle_philox4x32_10(ctr, key, w);
-    int e = (int)(j % 8);
-    uint32_t word = w[e / 2];
-    return (e % 2 == 0) ? (word & 0xffffu) : (word >> 16);
+    int e = (int)(j % 16);
+    return (w[e / 4] >> (8 * (e % 4))) & 0xffu;
 }
 
 /* 1 if element (i, j) of head bh survives softmax dropout, 0 if dropped. */
@@ -124,13 +135,13 @@ int oracle_keep(const oracle_params* p, int64_t bh, int64_t i, int64_t j)
 {
     uint32_t thr = oracle_drop_threshold(p->p_drop);
     if (thr == 0) return 1;
-    return oracle_draw16(p, bh, i, j) >= thr ? 1 : 0;
+    return oracle_draw8(p, bh, i, j) >= thr ? 1 : 0;
 }
 
-/* Z_ij = keep_ij / (1 - p_eff), p_eff = threshold / 65536. */
+/* Z_ij = keep_ij / (1 - p_eff), p_eff = threshold / 256. */
 static double keep_scale(const oracle_params* p)
 {
-    double p_eff = (double)oracle_drop_threshold(p->p_drop) / 65536.0;
+    double p_eff = (double)oracle_drop_threshold(p->p_drop) / 256.0;
     return 1.0 / (1.0 - p_eff);
 }
 

@@ -41,7 +41,7 @@
 
 /* Philox-4x32-10 and the drop threshold, from attn_oracle.c (same library). */
 void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]);
-uint32_t oracle_drop_threshold(float p_drop);
+uint32_t oracle_drop_threshold16(float p_drop);
 
 typedef struct {
     int32_t n_rows, hidden;
@@ -53,7 +53,7 @@ typedef struct {
 /* 1 if element (row, col) of x survives the dropout, 0 if dropped. */
 int oracle_dal_keep(const oracle_dal_params* p, int64_t row, int64_t col)
 {
-    const uint32_t thr = oracle_drop_threshold(p->p_drop);
+    const uint32_t thr = oracle_drop_threshold16(p->p_drop);
     if (thr == 0) return 1;
     uint32_t ctr[4] = {(uint32_t)(col / 8), (uint32_t)row, 0xFFFFFFFFu, (uint32_t)p->offset};
     uint32_t key[2] = {(uint32_t)(p->seed & 0xffffffffu), (uint32_t)(p->seed >> 32)};
@@ -66,7 +66,7 @@ int oracle_dal_keep(const oracle_dal_params* p, int64_t row, int64_t col)
 
 static double dal_keep_scale(const oracle_dal_params* p)
 {
-    return 1.0 / (1.0 - (double)oracle_drop_threshold(p->p_drop) / 65536.0);
+    return 1.0 / (1.0 - (double)oracle_drop_threshold16(p->p_drop) / 65536.0);
 }
 
 /* z of one row, then its mean and 1/sqrt(var + eps). */

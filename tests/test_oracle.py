@@ -63,40 +63,44 @@ def test_philox_matches_second_statement():
 
 def test_drop_threshold_closed_form():
     assert oracle.drop_threshold(0.0) == 0
-    assert oracle.drop_threshold(0.1) == 6554          # round(6553.6)
-    assert oracle.drop_threshold(0.5) == 32768
-    assert oracle.drop_threshold(0.99999) == 65535     # capped: some draw always survives
+    assert oracle.drop_threshold(0.1) == 26            # round(25.6)
+    assert oracle.drop_threshold(0.5) == 128
+    assert oracle.drop_threshold(0.99999) == 255       # capped: some draw always survives
+    assert oracle.drop_threshold(0.001) == 0           # below half a step: no dropout
     assert oracle.drop_threshold(-1.0) == 0
+    # the dropout + layer norm block's 16-bit reading
+    assert oracle.drop_threshold16(0.1) == 6554        # round(6553.6)
+    assert oracle.drop_threshold16(0.99999) == 65535
 
 
 def test_mask_mapping_follows_header_definition():
-    """Element (i, j) of head bh uses counter (j//8, i, bh, offset), key
-    (seed lo, seed hi), and half (j%8)%2 of output word (j%8)//2."""
+    """Element (i, j) of head bh uses counter (j//16, i, bh, offset), key
+    (seed lo, seed hi), and byte (j%16)%4 of output word (j%16)//4."""
     pr = oracle.Problem(b=2, h_q=3, h_kv=3, s=64, d=16, p_drop=0.25,
                         seed=0x0123456789ABCDEF, offset=77)
     rng = np.random.default_rng(3)
     key = [pr.seed & 0xFFFFFFFF, pr.seed >> 32]
     for _ in range(300):
         bh, i, j = int(rng.integers(0, 6)), int(rng.integers(0, 64)), int(rng.integers(0, 64))
-        w = _philox_from_spec([j // 8, i, bh, pr.offset], key)
-        e = j % 8
-        draw = (w[e // 2] >> (16 * (e % 2))) & 0xFFFF
-        assert oracle.draw16(pr, bh, i, j) == draw
-        assert oracle.keep(pr, bh, i, j) == int(draw >= 16384)
+        w = _philox_from_spec([j // 16, i, bh, pr.offset], key)
+        e = j % 16
+        draw = (w[e // 4] >> (8 * (e % 4))) & 0xFF
+        assert oracle.draw8(pr, bh, i, j) == draw
+        assert oracle.keep(pr, bh, i, j) == int(draw >= 64)
 
 
 def test_mask_statistics():
-    """Drop rate within 5 sigma of p_eff; 16-bit draws uniform (chi^2, 256 bins)."""
+    """Drop rate within 5 sigma of p_eff; 8-bit draws uniform (chi^2, 256 bins)."""
     pr = oracle.Problem(b=1, h_q=4, h_kv=4, s=1024, d=64, causal=False, p_drop=0.1,
                         seed=987654321, offset=5)
     masks = np.concatenate([oracle.mask_rows(pr, bh, 0, 1024).ravel() for bh in range(4)])
     n = masks.size
-    p_eff = 6554 / 65536
+    p_eff = 26 / 256
     drop = 1.0 - masks.mean()
     sigma = math.sqrt(p_eff * (1 - p_eff) / n)
     assert abs(drop - p_eff) < 5 * sigma, (drop, p_eff, sigma)
-    draws = np.array([oracle.draw16(pr, 0, i, j) for i in range(64) for j in range(256)])
-    hist = np.bincount(draws >> 8, minlength=256)
+    draws = np.array([oracle.draw8(pr, 0, i, j) for i in range(64) for j in range(256)])
+    hist = np.bincount(draws, minlength=256)
     expected = len(draws) / 256
     chi2 = float(((hist - expected) ** 2 / expected).sum())
     # 255 degrees of freedom: mean 255, sd ~22.6; 5 sigma band
@@ -247,7 +251,7 @@ def test_cross_attention_dropout_matches_autograd_with_oracle_mask(shape):
     pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=False, p_drop=0.3,
                         seed=77, offset=4, s_kv=skv)
     t = random_inputs(b, hq, hkv, s, d, seed=22, s_kv=skv)
-    p_eff = oracle.drop_threshold(0.3) / 65536
+    p_eff = oracle.drop_threshold(0.3) / 256
     z = np.zeros((b, hq, s, skv))
     for bh in range(b * hq):
         m = oracle.mask_rows(pr, bh, 0, s)
@@ -286,7 +290,7 @@ def test_dropout_matches_autograd_with_oracle_mask(causal):
     pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=causal, p_drop=0.3,
                         seed=2024, offset=9)
     t = random_inputs(b, hq, hkv, s, d, seed=3)
-    p_eff = oracle.drop_threshold(0.3) / 65536
+    p_eff = oracle.drop_threshold(0.3) / 256
     z = np.zeros((b, hq, s, s))
     for bh in range(b * hq):
         z[bh // hq, bh % hq] = oracle.mask_rows(pr, bh, 0, s) / (1 - p_eff)

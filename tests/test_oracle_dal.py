@@ -45,7 +45,7 @@ def test_dropout_matches_autograd_with_oracle_mask():
     t = dal_inputs(n, h, seed=3)
     m = oracle.dal_mask(pr)
     assert 0 < (m == 0).sum() < m.size
-    zf = torch.from_numpy(m / (1 - oracle.drop_threshold(0.3) / 65536))
+    zf = torch.from_numpy(m / (1 - oracle.drop_threshold16(0.3) / 65536))
     z, y, _, _ = oracle.dal_fwd(pr, t.x, t.residual, t.gamma, t.beta)
     dx, dres, dg, db = oracle.dal_bwd(pr, t.x, t.residual, t.gamma, t.dy, t.dz_next)
     rz, ry, rdx, rdr, rdg, rdb = _torch_reference(t, pr, zf)
@@ -90,7 +90,7 @@ def test_mask_mapping_follows_definition():
     """Element (row, col) uses counter (col // 8, row, 0xFFFFFFFF, offset) and
     half (col % 8) % 2 of word (col % 8) // 2; kept iff the draw >= thr."""
     pr = oracle.DalProblem(n_rows=40, hidden=96, p_drop=0.4, seed=0xFEDCBA9876543210, offset=3)
-    thr = oracle.drop_threshold(0.4)
+    thr = oracle.drop_threshold16(0.4)
     key = [pr.seed & 0xFFFFFFFF, pr.seed >> 32]
     rng = np.random.default_rng(5)
     for _ in range(300):
