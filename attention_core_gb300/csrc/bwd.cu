@@ -684,21 +684,25 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int e = 0; e < 16; ++e) pp[c32 * 16 + e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
             }
             const int key0 = j * BN + HK * h;
+            // Scores of keys this query does not see (past the diagonal, or past the
+            // last key) become -inf before the exponential; only the blocks that hold
+            // such keys run this (a uniform branch), the others go straight on.
+            const int k_end = a.causal ? i + 1 : a.s_k;    // first key not seen
+            if (key0 + HK > (a.causal ? qb * 128 : a.s_k)) {
+#pragma unroll
+                for (int e = 0; e < HK / 2; ++e) {
+                    float lo, hi;
+                    f2_unpack(pp[e], lo, hi);
+                    if (key0 + 2 * e >= k_end) lo = -INFINITY;
+                    if (key0 + 2 * e + 1 >= k_end) hi = -INFINITY;
+                    pp[e] = f2_pack(lo, hi);
+                }
+            }
 #pragma unroll
             for (int e = 0; e < HK / 2; ++e) {
                 float lo, hi;
                 f2_unpack(f2_fma(pp[e], sc2, nl22), lo, hi);
-                lo = ex2_approx(lo);
-                hi = ex2_approx(hi);
-                if (a.causal && key0 + HK > qb * 128) {
-                    if (key0 + 2 * e > i) lo = 0.f;
-                    if (key0 + 2 * e + 1 > i) hi = 0.f;
-                }
-                if (!a.causal && key0 + HK > a.s_k) {
-                    if (key0 + 2 * e >= a.s_k) lo = 0.f;
-                    if (key0 + 2 * e + 1 >= a.s_k) hi = 0.f;
-                }
-                pp[e] = f2_pack(lo, hi);
+                pp[e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
             }
             // P (before dropout) over the first HK/2 of this half's S columns, for PK += P K
             {
