@@ -250,7 +250,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const uint32_t warp_key0 = (uint32_t)(kb * 128 + (int)(warp & 3u) * 32);
         const float* lse2_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
         const KeepSwar8 ks(a.thr);
-        const uint32_t zs_bits = __float_as_uint(a.keep_scale);
+        const uint64_t zs2 = f2_pack(a.keep_scale, a.keep_scale);
         const float* del_s = reinterpret_cast<const float*>(smem + C::OFF_DEL);
         // Keep bytes of this lane's key over the half's queries (transposed draw).  Those
         // of tile it + 1 are drawn right after tile it's dS, while the tensor core forms
@@ -266,9 +266,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // queries, transposed from the staged rows and spread to byte sign bits
         // (byte t of word n: query 4n + t of the half).
         uint32_t kbyte[HQ / 4] = {};
-        auto pair_mask = [&](int e) -> uint32_t {
-            if constexpr (MWS) return keep_pair_mask_nat(kbyte, e);
-            else return keep_pair_mask_col<HQ>(kw, e);
+        // the keep word (byte sign bits of four consecutive queries) holding the
+        // query pair (2e, 2e + 1) in its bytes 2 (e & 1) and 2 (e & 1) + 1
+        auto keep_word = [&](int e) -> uint32_t {
+            if constexpr (MWS) return kbyte[e >> 1];
+            else return kw[e >> 3][(e & 7) >> 1];
         };
         // The dQ kernel's words hold key 4k + b of a warp's 32 keys at bit 8b + 7 - k;
         // after the transpose, lane p holds the queries of bit position p, so the lane
@@ -296,21 +298,33 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     for (int n = 0; n < 8; ++n) kbyte[8 * c + n] = keep_nibble_bytes((col >> (4 * n)) & 0xFu);
                 }
             }
-            const float2* nl2 = reinterpret_cast<const float2*>(lse2_s + st * BQ + HQ * h);
-            const float2* dl2 = reinterpret_cast<const float2*>(del_s + st * BQ + HQ * h);
+            // per-query row statistics of this half (-LSE log2(e) and -D), four at a time
+            const float4* nl4 = reinterpret_cast<const float4*>(lse2_s + st * BQ + HQ * h);
+            const float4* dl4 = reinterpret_cast<const float4*>(del_s + st * BQ + HQ * h);
             const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
             uint64_t pp[HQ / 2];
+            uint32_t rs[HQ];
+            if constexpr (HQ == 64) {
+                tmem_ld64(tmem + C::T_S + lane_off + HQ * h, rs);
+            } else {
+                uint32_t r32[32];
+                tmem_ld32(tmem + C::T_S + lane_off + HQ * h, r32);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) rs[e] = r32[e];
+            }
 #pragma unroll
             for (int c32 = 0; c32 < HQ / 32; ++c32) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + C::T_S + lane_off + HQ * h + c32 * 32, rr);
+                const uint32_t* rr = rs + 32 * c32;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 l = nl2[c32 * 16 + e];
+                for (int e = 0; e < 16; e += 2) {
+                    const float4 l = nl4[c32 * 8 + e / 2];
                     float lo, hi;
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), sc2,
                                      f2_pack(l.x, l.y)), lo, hi);
                     pp[c32 * 16 + e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[2 * e + 2]), __uint_as_float(rr[2 * e + 3])), sc2,
+                                     f2_pack(l.z, l.w)), lo, hi);
+                    pp[c32 * 16 + e + 1] = f2_pack(ex2_approx(lo), ex2_approx(hi));
                 }
             }
             if (a.causal && q0 < kb * 128 + 128) {
@@ -329,7 +343,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 uint32_t pw[HQ / 2];
 #pragma unroll
                 for (int e = 0; e < HQ / 2; ++e)
-                    pw[e] = DROP ? pack_bf16x2(pp[e]) & pair_mask(e) : pack_bf16x2(pp[e]);
+                    pw[e] = DROP ? pack_bf16x2(pp[e]) & keep_pair16(keep_word(e), e & 1) : pack_bf16x2(pp[e]);
                 if constexpr (HQ / 2 == 32) {
                     tmem_st32(tmem + C::T_S + lane_off + HQ * h, pw);
                 } else {
@@ -351,15 +365,18 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int ep = c32 * 16 + e;
-                    uint64_t dp = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                    uint32_t dlo = rr[2 * e], dhi = rr[2 * e + 1];
                     if (DROP) {
-                        // dP = dP_d * Z: factor 1/(1-p) where kept, 0 where dropped
-                        const uint32_t m = pair_mask(ep);
-                        dp = f2_mul(dp, f2_pack(__uint_as_float(prmt(m, 0u, 0x9999u) & zs_bits),
-                                                __uint_as_float(prmt(m, 0u, 0xBBBBu) & zs_bits)));
+                        // dP = dP_d * Z: dropped elements' dP_d is cleared, kept ones carry
+                        // 1/(1-p) in the FMA below
+                        const uint32_t kwd = keep_word(ep);
+                        dlo &= keep_mask32(kwd, 2 * (ep & 1));
+                        dhi &= keep_mask32(kwd, 2 * (ep & 1) + 1);
                     }
-                    const float2 dl = dl2[ep];
-                    w[e] = pack_bf16x2(f2_mul(pp[ep], f2_sub(dp, f2_pack(dl.x, dl.y))));
+                    const float4 dl = dl4[ep >> 1];
+                    const uint64_t nd = (ep & 1) ? f2_pack(dl.z, dl.w) : f2_pack(dl.x, dl.y);   // -D
+                    const uint64_t dp = f2_pack(__uint_as_float(dlo), __uint_as_float(dhi));
+                    w[e] = pack_bf16x2(f2_mul(pp[ep], DROP ? f2_fma(dp, zs2, nd) : f2_add(dp, nd)));
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HQ * h + c32 * 16, w);
             }
@@ -424,7 +441,14 @@ struct DqCfg {
     static constexpr uint32_t QCH = G::template chunk_bytes<128>();
     static constexpr uint32_t KT = G::template tile_bytes<BN>();
     static constexpr uint32_t KCH = G::template chunk_bytes<BN>();
-    static constexpr int KST = 2, VST = 2;
+    // A K tile is an operand of three products (S, P K and dQ), so its ring slot
+    // frees only when the block's dQ product is done; the K ring takes every
+    // stage that fits beside Q, dO and a two-stage V ring, up to four, so that
+    // the next blocks' K tiles are resident when their S products are issued.
+    static constexpr int VST = 2;
+    static constexpr int KST_FIT = (int)((227u * 1024u - 2u * QT - (uint32_t)VST * KT - 256u - 2u * 128u * 4u - 1024u) / KT);
+    static constexpr int KST = KST_FIT < 4 ? KST_FIT : 4;
+    static_assert(KST >= 2, "K ring");
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_DO = QT;
     static constexpr uint32_t OFF_K = 2 * QT;
@@ -445,7 +469,7 @@ struct DqCfg {
 
 struct DqBars {
     uint64_t qdo_full;
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t k_full[4], k_empty[4], v_full[2], v_empty[2];
     uint64_t s_full, p_full, dp_full, ds_full, acc_done;
     uint64_t o_full, o_free;
     uint64_t never;
@@ -486,9 +510,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     if (threadIdx.x == 0) {
         mbar_init(bar(bars->qdo_full), 1);
-        for (int st = 0; st < 2; ++st) {
+        for (int st = 0; st < KST; ++st) {
             mbar_init(bar(bars->k_full[st]), 1);
             mbar_init(bar(bars->k_empty[st]), 1);
+        }
+        for (int st = 0; st < VST; ++st) {
             mbar_init(bar(bars->v_full[st]), 1);
             mbar_init(bar(bars->v_empty[st]), 1);
         }
@@ -676,12 +702,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!ok) break;
             tc_fence_after();
             uint64_t pp[HK / 2];
+            if constexpr (HK == 64) {
+                uint32_t rr[64];
+                tmem_ld64(tmem + C::T_S + lane_off + HK * h, rr);
 #pragma unroll
-            for (int c32 = 0; c32 < HK / 32; ++c32) {
+                for (int e = 0; e < 32; ++e) pp[e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+            } else {
                 uint32_t rr[32];
-                tmem_ld32(tmem + C::T_S + lane_off + HK * h + c32 * 32, rr);
+                tmem_ld32(tmem + C::T_S + lane_off + HK * h, rr);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pp[c32 * 16 + e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                for (int e = 0; e < 16; ++e) pp[e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
             }
             const int key0 = j * BN + HK * h;
             // Scores of keys this query does not see (past the diagonal, or past the
@@ -718,6 +748,34 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->p_full));
+            // The keep decisions of this block's keys (two Philox calls of 16 keys per
+            // 32, one SWAR test per output word: keys 4k .. 4k + 3 of the half in
+            // keep[k]) are drawn here, while the tensor core forms P K, dQ of the block
+            // before and this block's dP: they need no product, and the phase after dP
+            // is the one the tensor core waits for.
+            uint32_t keep[HK / 4];
+            if (DROP) {
+#pragma unroll
+                for (int c32 = 0; c32 < HK / 32; ++c32) {
+                    const uint32_t grp = (uint32_t)(key0 >> 4) + 2u * (uint32_t)c32;
+                    const uint4 w0 = philox4x32_10_rk(grp, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
+                    const uint4 w1 = philox4x32_10_rk(grp + 1u, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
+                    uint32_t* kc = keep + 8 * c32;
+                    kc[0] = ks(w0.x); kc[1] = ks(w0.y); kc[2] = ks(w0.z); kc[3] = ks(w0.w);
+                    kc[4] = ks(w1.x); kc[5] = ks(w1.y); kc[6] = ks(w1.z); kc[7] = ks(w1.w);
+                    if constexpr (MWS) {
+                        // hand the bits to the dK/dV kernel: key quarter of the 128-key block,
+                        // query unit (rows 0-63 / 64-127) and row within it
+                        uint32_t k8[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) k8[k] = kc[k];
+                        const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
+                        const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
+                                            (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
+                        args.mask_ws[word] = keep_bits32(k8);
+                    }
+                }
+            }
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
             tc_fence_after();
@@ -725,16 +783,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int c32 = 0; c32 < HK / 32; ++c32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
-                // keep decisions of these 32 keys: two Philox calls of 16 keys, one SWAR
-                // test per output word (keys 4k .. 4k + 3 of the chunk in keep[k])
-                uint32_t keep[8];
-                if (DROP) {
-                    const uint32_t grp = (uint32_t)(key0 >> 4) + 2u * (uint32_t)c32;
-                    const uint4 w0 = philox4x32_10_rk(grp, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
-                    const uint4 w1 = philox4x32_10_rk(grp + 1u, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
-                    keep[0] = ks(w0.x); keep[1] = ks(w0.y); keep[2] = ks(w0.z); keep[3] = ks(w0.w);
-                    keep[4] = ks(w1.x); keep[5] = ks(w1.y); keep[6] = ks(w1.z); keep[7] = ks(w1.w);
-                }
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {               // pair e: keys 2e, 2e + 1 of the chunk
@@ -742,22 +790,14 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     uint32_t dlo = rr[2 * e], dhi = rr[2 * e + 1];
                     if (DROP) {
                         // dropped elements' dP_d is cleared; kept ones carry 1/(1-p) below
-                        dlo &= keep_mask32(keep[e >> 1], 2 * (e & 1));
-                        dhi &= keep_mask32(keep[e >> 1], 2 * (e & 1) + 1);
+                        dlo &= keep_mask32(keep[8 * c32 + (e >> 1)], 2 * (e & 1));
+                        dhi &= keep_mask32(keep[8 * c32 + (e >> 1)], 2 * (e & 1) + 1);
                     }
                     const uint64_t dp = f2_pack(__uint_as_float(dlo), __uint_as_float(dhi));
                     dacc2 = f2_fma(pp[ep], dp, dacc2);
                     w[e] = pack_bf16x2(f2_mul(pp[ep], DROP ? f2_fma(dp, zs2, ndt2) : f2_sub(dp, dt2)));
                 }
                 tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
-                if constexpr (DROP && MWS) {
-                    // hand the bits to the dK/dV kernel: key quarter of the 128-key block,
-                    // query unit (rows 0-63 / 64-127) and row within it
-                    const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
-                    const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
-                                        (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
-                    args.mask_ws[word] = keep_bits32(keep);
-                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -787,7 +827,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     rq[e] = __float_as_uint(fmaf(-eps, __uint_as_float(rp[e]), __uint_as_float(rq[e])));
                 stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rq, a.scale);
             }
-            if (h == 0) args.delta_ws[srow] = d_exact;
+            if (h == 0) args.delta_ws[srow] = -d_exact;    // the dK/dV kernel adds it
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, kRowThreads);

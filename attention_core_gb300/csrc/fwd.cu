@@ -324,12 +324,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!ok) break;
                 tc_fence_after();
                 float x[64];
+                {
+                    uint32_t rr[64];
+                    tmem_ld64(tS, rr);
 #pragma unroll
-                for (int c32 = 0; c32 < 2; ++c32) {
-                    uint32_t rr[32];
-                    tmem_ld32(tS + c32 * 32, rr);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c32 * 32 + e] = __uint_as_float(rr[e]);
+                    for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(rr[e]);
                 }
                 const int key0 = j * 128 + 64 * h;
                 if (a.causal && j == qb) {

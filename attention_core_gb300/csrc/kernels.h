@@ -54,7 +54,7 @@ struct BwdArgs {
     const uint16_t* dout; // bf16 [b*h_q*s*d]
     const float* lse;     // [b*h_q*s]
     float* lse2_ws;       // [b*h_q*s_pad]  -LSE * log2(e); -inf past s
-    float* delta_ws;      // [b*h_q*s_pad]  exact row statistic D = sum_j P_ij dP_ij
+    float* delta_ws;      // [b*h_q*s_pad]  minus the exact row statistic D = sum_j P_ij dP_ij
                           // (written by the dQ kernel, read by the dK/dV kernel)
     uint32_t* mask_ws;    // dropout keep bits, written by the dQ kernel and read by the
                           // dK/dV kernel (layout: mask_pair_word); null: dK/dV draws its own

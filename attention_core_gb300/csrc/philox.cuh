@@ -180,15 +180,6 @@ __device__ __forceinline__ void keep_bytes_col16(const PhiloxKey& pk, const Keep
     }
 }
 
-// 16-bit lane mask of the query pair (2e, 2e+1) of the half-tile, for this
-// lane's key, from keep_bytes_col16's words.
-template <int HQ>
-__device__ __forceinline__ uint32_t keep_pair_mask_col(const uint32_t (&kw)[HQ / 16][4], int e)
-{
-    const int u = e >> 3, i = e & 7;          // queries 16u + 2i, 16u + 2i + 1
-    return keep_pair16(kw[u][i >> 1], i & 1);
-}
-
 // Keep bits of four consecutive queries (bit t = query t) as the sign bits of
 // four bytes (bit t -> bit 8t + 7).  Multiplying by 2^7 + 2^14 + 2^21 + 2^28
 // moves bit t up by 7t + 7; a cross term t + 7u + 7 (u != t) never lands on a
@@ -196,14 +187,6 @@ __device__ __forceinline__ uint32_t keep_pair_mask_col(const uint32_t (&kw)[HQ /
 __device__ __forceinline__ uint32_t keep_nibble_bytes(uint32_t nibble)
 {
     return (nibble * 0x10204080u) & 0x80808080u;
-}
-
-// The 16-bit lane mask of the query pair (2e, 2e+1) from such words (byte t
-// of word n: query 4n + t): low half from query 2e's byte, high half from
-// query 2e + 1's.
-__device__ __forceinline__ uint32_t keep_pair_mask_nat(const uint32_t* kbyte, int e)
-{
-    return prmt(kbyte[e >> 1], 0u, (e & 1) ? 0xBBAAu : 0x9988u);
 }
 
 // 32 x 32 bit transpose across a warp: on entry lane L holds row L (bit k =

@@ -29,21 +29,29 @@ struct TileGeom {
     template <int ROWS>
     __host__ __device__ static constexpr uint32_t chunk_bytes() { return (uint32_t)ROWS * ROWB; }
 
+    // The descriptors of a tile's slices differ only in their start-address
+    // field (address >> 4 in bits 0-13).  Tile bases and slice offsets are
+    // multiples of 16 and every shared-memory address is below 256 KB, so the
+    // descriptor of slice kk is that of slice 0 plus offset(kk) >> 4 in the low
+    // word, with no carry out of the field: one 32-bit add per slice on the
+    // MMA-issuing thread instead of rebuilding the descriptor.
+    template <int ROWS>
+    __host__ __device__ static constexpr uint32_t k_offset(int kk)
+    {
+        return (uint32_t)((kk * 16) / CW) * chunk_bytes<ROWS>() + (uint32_t)((kk * 16) % CW) * 2;
+    }
     // K-major operand: the 16-wide slice kk of the head dimension.
     template <int ROWS>
     __device__ static __forceinline__ uint64_t desc_k(uint32_t base, int kk)
     {
-        const int col = kk * 16;
-        const uint32_t addr = base + (uint32_t)(col / CW) * chunk_bytes<ROWS>() + (uint32_t)(col % CW) * 2;
-        return smem_desc(addr, 16, SBO, LAYOUT);
+        return desc_plus(smem_desc(base, 16, SBO, LAYOUT), k_offset<ROWS>(kk) >> 4);
     }
     // MN-major operand: rows [16 kk, 16 kk + 16) as the reduction slice,
     // the head dimension (D wide, chunk after chunk) as N.
     template <int ROWS>
     __device__ static __forceinline__ uint64_t desc_mn(uint32_t base, int kk)
     {
-        const uint32_t addr = base + (uint32_t)kk * 16 * ROWB;
-        return smem_desc(addr, chunk_bytes<ROWS>(), SBO, LAYOUT);
+        return desc_plus(smem_desc(base, chunk_bytes<ROWS>(), SBO, LAYOUT), ((uint32_t)kk * 16 * ROWB) >> 4);
     }
     // Byte offset of the 16-byte unit holding columns [col, col + 8) of row r.
     template <int ROWS>
