@@ -325,11 +325,12 @@ int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
     auto kmap = [&](CUtensorMap* m, const void* ptr, int rows) {
         return encode_map_strided(m, ptr, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, rows);
     };
-    CUtensorMap tq128, tdo128, to128, tqb, tdob, tk, tv, tkb, tvb, tdq, tdk, tdv;
+    CUtensorMap tq128, tdo128, to128, tdq128, tqb, tdob, tk, tv, tkb, tvb, tdk, tdv;
     if ((rc = qmap(&tq128, q, 128)) || (rc = qmap(&tdo128, dout, 128)) || (rc = qmap(&to128, o, 128)) ||
+        (rc = qmap(&tdq128, dq, 128)) ||
         (rc = qmap(&tqb, q, bq)) || (rc = qmap(&tdob, dout, bq)) || (rc = kmap(&tk, k, 128)) ||
         (rc = kmap(&tv, v, 128)) || (rc = kmap(&tkb, k, bn)) || (rc = kmap(&tvb, v, bn)) ||
-        (rc = qmap(&tdq, dq, 128)) || (rc = kmap(&tdk, dk, 128)) || (rc = kmap(&tdv, dv, 128)))
+        (rc = kmap(&tdk, dk, 128)) || (rc = kmap(&tdv, dv, 128)))
         return rc;
     ac::BwdArgs a{};
     a.c = common_args(p);
@@ -345,9 +346,10 @@ int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
                     ? reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) + 2 * padded_rows(p))
                     : nullptr;
     a.d = p->d;
+    if ((rc = device_sms(&a.num_sms))) return rc;
     const bool drop = a.c.thr != 0;
     if ((rc = record(p->timing_events, 0, st))) return rc;
-    if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, to128, tdq, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, to128, tdq128, a, st) != 0) return ATTN_CORE_ERR_CUDA;
     if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
     if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
     return record(p->timing_events, 3, st);

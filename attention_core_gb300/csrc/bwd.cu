@@ -30,6 +30,7 @@
 #include "kernels.h"
 #include "philox.cuh"
 #include "ptx.cuh"
+#include "sched.cuh"
 #include "tile.cuh"
 
 namespace ac {
@@ -38,7 +39,8 @@ namespace {
 
 enum : int32_t {
     kSiteInject = 1, kSiteKvFull, kSiteQEmpty, kSiteQFull, kSitePFull, kSiteDsFull, kSiteSFull,
-    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePRead, kSiteOFull, kSiteOFree
+    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePRead, kSiteOFull, kSiteStage,
+    kSiteX, kSiteDrain
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
@@ -183,7 +185,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
         }
     } else if (alive && warp == 1) {
-        if (lane == 0) {
+        {   // the whole warp issues (see mma_ss)
             // ---- MMA issuer.  Order: S0 dP0 | dV0 S1 dK0 dP1 | dV1 S2 dK1 dP2 | ...
             constexpr uint32_t IDS = idesc_bf16(128, BQ, false, false);  // S^T = K Q^T, dP^T = V dO^T
             constexpr uint32_t IDG = idesc_bf16(128, D, false, true);    // dV += P^T dO, dK += dS^T Q
@@ -203,8 +205,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                            G::template desc_k<BQ>(dobase, kk), IDS, kk > 0 ? 1u : 0u);
                 mma_commit(bar(bars->dp_full));
             };
-            bool ok = wait_bounded(wc, bar(bars->kv_full), 0, timeout_code(kSiteKvFull));
-            if (ok) ok = wait_bounded(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull));
+            bool ok = wait_warp(wc, bar(bars->kv_full), 0, timeout_code(kSiteKvFull));
+            if (ok) ok = wait_warp(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull));
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -214,7 +216,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 const int st = it % ST;
                 const uint32_t qbase = sb + C::OFF_Q + st * C::Q_TILE;
                 const uint32_t dobase = sb + C::OFF_DO + st * C::Q_TILE;
-                ok = wait_bounded(wc, bar(bars->p_full), it & 1, timeout_code(kSitePFull));
+                ok = wait_warp(wc, bar(bars->p_full), it & 1, timeout_code(kSitePFull));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -223,12 +225,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                            IDG, (it > 0 || kk > 0) ? 1u : 0u);
                 if (it + 1 < n_it) {
                     const int st1 = (it + 1) % ST;
-                    ok = wait_bounded(wc, bar(bars->q_full[st1]), ((it + 1) / ST) & 1, timeout_code(kSiteQFull));
+                    ok = wait_warp(wc, bar(bars->q_full[st1]), ((it + 1) / ST) & 1, timeout_code(kSiteQFull));
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(it + 1);
                 }
-                ok = wait_bounded(wc, bar(bars->ds_full), it & 1, timeout_code(kSiteDsFull));
+                ok = wait_warp(wc, bar(bars->ds_full), it & 1, timeout_code(kSiteDsFull));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -421,7 +423,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 }
 
 // =============================================================== dQ ======
-// One (query head, 128-query block) per CTA; queries on TMEM lanes.  Per
+// Tiles are (query head, 128-query block) pairs, queries on TMEM lanes.  Per
 // key block j: S = Q K_j^T and dP_d = dO V_j^T into TMEM; the row threads
 // form P, the mask, dP = dP_d * Z and
 //     dS~ = P (dP - D~),        D~ = rowsum(dO * O) from the bf16 output,
@@ -431,6 +433,17 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 // which equals scale * sum_j P_ij (dP_ij - D_i) K_j: the gradient with the
 // exact statistic, not the one rounded through the stored bf16 output.  The
 // exact D is written back to the workspace for the dK/dV kernel.
+//
+// Persistent: one CTA per SM walks its share of the tiles, longest first
+// (sched.cuh).  Q and dO have a buffer of their own, so the next tile's are
+// loaded while this one's epilogue runs (once its last S and dP products are
+// done and its rows have formed D~); the K and V rings, the score buffers and
+// the MMA stream run on across tiles, and the next tile's first P K product
+// only waits until the epilogue has read the accumulators.  The O buffer
+// serves twice per tile: O for D~, formed in the first block after the
+// probabilities, then the staged dQ of the epilogue, which one TMA store
+// writes out before the next tile's O comes in.  The row statistic -LSE is
+// read a tile ahead, and the next tile's Q, dO and O are pulled into L2.
 namespace {
 
 template <int D>
@@ -441,26 +454,22 @@ struct DqCfg {
     static constexpr uint32_t QCH = G::template chunk_bytes<128>();
     static constexpr uint32_t KT = G::template tile_bytes<BN>();
     static constexpr uint32_t KCH = G::template chunk_bytes<BN>();
+    static constexpr uint32_t RED_BYTES = 2 * 128 * 4;       // [2 halves][128] partial row statistics
     // A K tile is an operand of three products (S, P K and dQ), so its ring slot
     // frees only when the block's dQ product is done; the K ring takes every
-    // stage that fits beside Q, dO and a two-stage V ring, up to four, so that
-    // the next blocks' K tiles are resident when their S products are issued.
+    // stage that fits beside Q, dO, O and a two-stage V ring, up to four.
     static constexpr int VST = 2;
-    static constexpr int KST_FIT = (int)((227u * 1024u - 2u * QT - (uint32_t)VST * KT - 256u - 2u * 128u * 4u - 1024u) / KT);
+    static constexpr int KST_FIT = (int)((227u * 1024u - 3u * QT - (uint32_t)VST * KT - 256u - RED_BYTES - 1024u) / KT);
     static constexpr int KST = KST_FIT < 4 ? KST_FIT : 4;
     static_assert(KST >= 2, "K ring");
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_DO = QT;
-    static constexpr uint32_t OFF_K = 2 * QT;
+    static constexpr uint32_t OFF_O = 2 * QT;
+    static constexpr uint32_t OFF_K = 3 * QT;
     static constexpr uint32_t OFF_V = OFF_K + KST * KT;
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KT;
-    static constexpr uint32_t OFF_RED = OFF_BAR + 256;      // [2 halves][128] partial row statistics
-    static constexpr uint32_t SMEM = OFF_RED + 2 * 128 * 4 + 1024;
-    // The O tile (for the first estimate D~) is staged once at the end of the V
-    // ring; V stages from O_ST0 on are loaded only after the row threads have read it.
-    static_assert(VST * KT >= QT, "O tile must fit in the V ring");
-    static constexpr uint32_t OFF_O = OFF_V + VST * KT - QT;
-    static constexpr int O_ST0 = (int)((VST * KT - QT) / KT);
+    static constexpr uint32_t OFF_RED = OFF_BAR + 256;
+    static constexpr uint32_t SMEM = OFF_RED + RED_BYTES + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM: S (later P in the first half of each row half) | dP (later dS~) | dQ~ | PK
     static constexpr uint32_t T_S = 0, T_DP = BN, T_DQ = 2 * BN, T_PK = 2 * BN + D;
@@ -468,14 +477,35 @@ struct DqCfg {
 };
 
 struct DqBars {
-    uint64_t qdo_full;
+    uint64_t q_full, q_empty;          // Q and dO of a tile (freed by the products and the D~ reads)
+    uint64_t o_full, dq_staged;        // O of a tile in the O buffer / the tile's dQ staged there
     uint64_t k_full[4], k_empty[4], v_full[2], v_empty[2];
-    uint64_t s_full, p_full, dp_full, ds_full, acc_done;
-    uint64_t o_full, o_free;
-    uint64_t never;
+    uint64_t s_full, p_full, dp_full, ds_full;
+    uint64_t acc_done, acc_free;       // a tile's accumulators complete / read out
+    uint64_t xbar;                     // exchange barrier of the 256 row threads
+    uint64_t drain, never;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
+static_assert(sizeof(DqBars) <= 256, "barrier block");
+
+// Work tile t (longest first): query block, flattened query head, KV head and
+// key blocks.
+struct DqTile {
+    int qb, bh, bkv, nk;
+};
+template <int BN>
+__device__ __forceinline__ DqTile dq_tile(const CommonArgs& a, int t)
+{
+    DqTile w;
+    w.qb = a.n_blk - 1 - t / a.n_bh;
+    w.bh = t % a.n_bh;
+    const int group = a.h_q / a.h_kv;
+    w.bkv = (w.bh / a.h_q) * a.h_kv + (w.bh % a.h_q) / group;
+    const int n_kblk = (a.s_k + BN - 1) / BN;
+    w.nk = a.causal ? min((w.qb + 1) * (128 / BN), n_kblk) : n_kblk;
+    return w;
+}
 
 }  // namespace
 
@@ -499,17 +529,14 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     DqBars* bars = reinterpret_cast<DqBars*>(smem_raw + pad + C::OFF_BAR);
     auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
-    const int n_bh = a.n_bh;
-    const int qb = a.n_blk - 1 - (int)(blockIdx.x / n_bh);
-    const int bh = (int)(blockIdx.x % n_bh);
-    const int group = a.h_q / a.h_kv;
-    const int bkv = (bh / a.h_q) * a.h_kv + (bh % a.h_q) / group;
-    const int n_kblk = (a.s_k + BN - 1) / BN;
-    const int nk = a.causal ? min((qb + 1) * (128 / BN), n_kblk) : n_kblk;
+    const TileSched sched{a.n_blk * a.n_bh, (int)gridDim.x, (int)blockIdx.x};
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(bars->qdo_full), 1);
+        mbar_init(bar(bars->q_full), 1);
+        mbar_init(bar(bars->q_empty), 1 + kRowThreads);
+        mbar_init(bar(bars->o_full), 1);
+        mbar_init(bar(bars->dq_staged), kRowThreads);
         for (int st = 0; st < KST; ++st) {
             mbar_init(bar(bars->k_full[st]), 1);
             mbar_init(bar(bars->k_empty[st]), 1);
@@ -523,8 +550,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(bar(bars->dp_full), 1);
         mbar_init(bar(bars->ds_full), kRowThreads);
         mbar_init(bar(bars->acc_done), 1);
-        mbar_init(bar(bars->o_full), 1);
-        mbar_init(bar(bars->o_free), kRowThreads);
+        mbar_init(bar(bars->acc_free), kRowThreads);
+        mbar_init(bar(bars->xbar), kRowThreads);
+        mbar_init(bar(bars->drain), 1);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -535,6 +563,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
         tma_prefetch_desc(&tm_o);
+        tma_prefetch_desc(&tm_dq);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_base), 512);
@@ -551,52 +580,99 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     if (alive && warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer: Q and dO once, then the K ring
-            mbar_arrive_expect_tx(bar(bars->qdo_full), 2 * C::QT);
-            for (int ch = 0; ch < G::NCH; ++ch) {
-                tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
-                tma_load_3d(sb + C::OFF_DO + ch * C::QCH, &tm_do, ch * G::CW, qb * 128, bh, bar(bars->qdo_full));
+            // ---- TMA producer: the K ring over all blocks of all tiles
+            int g = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const DqTile w = dq_tile<BN>(a, t);
+                for (int j = 0; j < w.nk; ++j, ++g) {
+                    const int st = g % KST;
+                    ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / KST) & 1) ^ 1, timeout_code(kSiteKEmpty));
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(bars->k_full[st]), C::KT);
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_load_3d(sb + C::OFF_K + st * C::KT + ch * C::KCH, &tm_k, ch * G::CW, j * BN, w.bkv,
+                                    bar(bars->k_full[st]));
+                }
             }
-            mbar_arrive_expect_tx(bar(bars->o_full), C::QT);
-            for (int ch = 0; ch < G::NCH; ++ch)
-                tma_load_3d(sb + C::OFF_O + ch * C::QCH, &tm_o, ch * G::CW, qb * 128, bh, bar(bars->o_full));
-            for (int j = 0; j < nk; ++j) {
-                const int st = j % KST;
-                if (!wait_bounded(wc, bar(bars->k_empty[st]), ((j / KST) & 1) ^ 1, timeout_code(kSiteKEmpty)))
-                    break;
-                mbar_arrive_expect_tx(bar(bars->k_full[st]), C::KT);
+        } else if (lane == 1) {
+            // ---- TMA producer and dQ store: per tile its Q and dO (once the previous
+            // tile's last S and dP products are done and its rows have formed D~),
+            // then the previous tile's dQ (staged by the row threads in the O
+            // buffer) goes out by TMA, and once that store has read the buffer this
+            // tile's O comes in.  The next tile's Q, dO and O are pulled into L2
+            // meanwhile, so their loads at the tile boundary are short.
+            DqTile prev{};
+            for (int u = 0;; ++u) {
+                const int t = sched.tile(u);
+                DqTile w{};
+                if (t >= 0) {
+                    w = dq_tile<BN>(a, t);
+                    if (!wait_bounded(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
+                    mbar_arrive_expect_tx(bar(bars->q_full), 2 * C::QT);
+                    for (int ch = 0; ch < G::NCH; ++ch) {
+                        tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, w.qb * 128, w.bh,
+                                    bar(bars->q_full));
+                        tma_load_3d(sb + C::OFF_DO + ch * C::QCH, &tm_do, ch * G::CW, w.qb * 128, w.bh,
+                                    bar(bars->q_full));
+                    }
+                }
+                if (u > 0) {
+                    if (!wait_bounded(wc, bar(bars->dq_staged), (u - 1) & 1, timeout_code(kSiteStage))) break;
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_store_3d(&tm_dq, sb + C::OFF_O + ch * C::QCH, ch * G::CW, prev.qb * 128, prev.bh);
+                    bulk_commit();
+                    bulk_wait_read0();
+                }
+                if (t < 0) break;
+                mbar_arrive_expect_tx(bar(bars->o_full), C::QT);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_K + st * C::KT + ch * C::KCH, &tm_k, ch * G::CW, j * BN, bkv,
-                                bar(bars->k_full[st]));
+                    tma_load_3d(sb + C::OFF_O + ch * C::QCH, &tm_o, ch * G::CW, w.qb * 128, w.bh, bar(bars->o_full));
+                const int tn = sched.tile(u + 1);
+                if (tn >= 0) {
+                    const DqTile wn = dq_tile<BN>(a, tn);
+                    for (int ch = 0; ch < G::NCH; ++ch) {
+                        tma_prefetch_3d(&tm_q, ch * G::CW, wn.qb * 128, wn.bh);
+                        tma_prefetch_3d(&tm_do, ch * G::CW, wn.qb * 128, wn.bh);
+                        tma_prefetch_3d(&tm_o, ch * G::CW, wn.qb * 128, wn.bh);
+                    }
+                }
+                prev = w;
             }
         }
     } else if (alive && warp == 2) {
         if (lane == 0) {
-            // ---- TMA producer: the V ring
-            for (int j = 0; j < nk; ++j) {
-                const int st = j % VST;
-                if (!wait_bounded(wc, bar(bars->v_empty[st]), ((j / VST) & 1) ^ 1, timeout_code(kSiteVEmpty)))
-                    break;
-                if (j < VST && j >= C::O_ST0 &&
-                    !wait_bounded(wc, bar(bars->o_free), 0, timeout_code(kSiteOFree)))
-                    break;
-                mbar_arrive_expect_tx(bar(bars->v_full[st]), C::KT);
-                for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_V + st * C::KT + ch * C::KCH, &tm_v, ch * G::CW, j * BN, bkv,
-                                bar(bars->v_full[st]));
+            // ---- TMA producer: the V ring over all blocks of all tiles
+            int g = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const DqTile w = dq_tile<BN>(a, t);
+                for (int j = 0; j < w.nk; ++j, ++g) {
+                    const int st = g % VST;
+                    ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / VST) & 1) ^ 1, timeout_code(kSiteVEmpty));
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(bars->v_full[st]), C::KT);
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_load_3d(sb + C::OFF_V + st * C::KT + ch * C::KCH, &tm_v, ch * G::CW, j * BN, w.bkv,
+                                    bar(bars->v_full[st]));
+                }
             }
         }
     } else if (alive && warp == 1) {
-        if (lane == 0) {
-            // ---- MMA issuer.  Order: S0 dP0 | PK0 S1 dQ0 dP1 | PK1 S2 dQ1 dP2 | ...
+        {   // the whole warp issues (see mma_ss)
+            // ---- MMA issuer.  Per tile: S0 dP0 | PK0 S1 dQ0 dP1 | PK1 S2 dQ1 dP2 | ...
             // PK_j reads P_j from the S columns as soon as the row threads have
             // stored it, so after dS_j only dQ_j and dP_{j+1} stand between the
-            // row threads and their next dS.
+            // row threads and their next dS.  g counts blocks over all tiles.
             constexpr uint32_t IDS = idesc_bf16(128, BN, false, false);  // S = Q K^T, dP_d = dO V^T
             constexpr uint32_t IDQ = idesc_bf16(128, D, false, true);    // dQ~ += dS~ K, PK += P K
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % KST;
-                if (!wait_bounded(wc, bar(bars->k_full[st]), (j / KST) & 1, timeout_code(kSiteKFull))) return false;
+            auto issue_s = [&](int g) -> bool {
+                const int st = g % KST;
+                if (!wait_warp(wc, bar(bars->k_full[st]), (g / KST) & 1, timeout_code(kSiteKFull))) return false;
                 tc_fence_after();
                 const uint32_t kbase = sb + C::OFF_K + st * C::KT;
 #pragma unroll
@@ -606,9 +682,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 mma_commit(bar(bars->s_full));
                 return true;
             };
-            auto issue_dp = [&](int j) -> bool {
-                const int st = j % VST;
-                if (!wait_bounded(wc, bar(bars->v_full[st]), (j / VST) & 1, timeout_code(kSiteVFull))) return false;
+            auto issue_dp = [&](int g) -> bool {
+                const int st = g % VST;
+                if (!wait_warp(wc, bar(bars->v_full[st]), (g / VST) & 1, timeout_code(kSiteVFull))) return false;
                 tc_fence_after();
                 const uint32_t vbase = sb + C::OFF_V + st * C::KT;
 #pragma unroll
@@ -619,34 +695,54 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 mma_commit(bar(bars->dp_full));
                 return true;
             };
-            bool ok = wait_bounded(wc, bar(bars->qdo_full), 0, timeout_code(kSiteQFull));
-            if (ok) ok = issue_s(0);
-            if (ok) ok = issue_dp(0);
-            for (int j = 0; j < nk && ok; ++j) {
-                const int st = j % KST;
-                const uint32_t kbase = sb + C::OFF_K + st * C::KT;
-                ok = wait_bounded(wc, bar(bars->p_full), j & 1, timeout_code(kSitePRead));
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C::T_PK, tmem + C::T_S + split_a_col(kk, BN), G::template desc_mn<BN>(kbase, kk), IDQ,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                if (j + 1 < nk) {
-                    ok = issue_s(j + 1);      // overwrites P_j: after PK_j in the tensor pipe
+            int g = 0;
+            bool ok = true;
+            for (int u = 0; ok; ++u) {
+                const int t = sched.tile(u);
+                if (t < 0) break;
+                const DqTile w = dq_tile<BN>(a, t);
+                const int g0 = g;
+                ok = wait_warp(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
+                if (ok) ok = issue_s(g0);
+                if (ok) ok = issue_dp(g0);
+                // Q and dO are free once the tile's last S and dP products are done
+                if (ok && w.nk == 1) mma_commit(bar(bars->q_empty));
+                for (int j = 0; j < w.nk && ok; ++j, ++g) {
+                    const int st = g % KST;
+                    const uint32_t kbase = sb + C::OFF_K + st * C::KT;
+                    ok = wait_warp(wc, bar(bars->p_full), g & 1, timeout_code(kSitePRead));
+                    // the first P K of a tile overwrites PK: the epilogue of the tile
+                    // before must have read the accumulators
+                    if (ok && j == 0)
+                        ok = wait_warp(wc, bar(bars->acc_free), (u & 1) ^ 1, timeout_code(kSiteAcc));
                     if (!ok) break;
-                }
-                ok = wait_bounded(wc, bar(bars->ds_full), j & 1, timeout_code(kSiteDsFull));
-                if (!ok) break;
-                tc_fence_after();
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + C::T_DQ, tmem + C::T_DP + split_a_col(kk, BN), G::template desc_mn<BN>(kbase, kk),
-                           IDQ, (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(bars->k_empty[st]));
-                if (j + 1 < nk) ok = issue_dp(j + 1);
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(tmem + C::T_PK, tmem + C::T_S + split_a_col(kk, BN), G::template desc_mn<BN>(kbase, kk),
+                               IDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (j + 1 < w.nk) {
+                        ok = issue_s(g + 1);      // overwrites P_j: after PK_j in the tensor pipe
+                        if (!ok) break;
+                    }
+                    ok = wait_warp(wc, bar(bars->ds_full), g & 1, timeout_code(kSiteDsFull));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(tmem + C::T_DQ, tmem + C::T_DP + split_a_col(kk, BN), G::template desc_mn<BN>(kbase, kk),
+                               IDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(bars->k_empty[st]));
+                    if (j + 1 < w.nk) {
+                        ok = issue_dp(g + 1);
+                        if (ok && j + 2 == w.nk) mma_commit(bar(bars->q_empty));
+                    }
+                }
+                if (ok) mma_commit(bar(bars->acc_done));
             }
-            if (ok) mma_commit(bar(bars->acc_done));
+            // every MMA must be complete before the CTA releases TMEM
+            mma_commit(bar(bars->drain));
+            wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 4) {
         // ---- row threads: query row = TMEM lane, half = which BN/2 keys of a block
@@ -654,167 +750,194 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const RowThread rt = row_thread();
         const int h = rt.half, r = rt.row;
         const uint32_t lane_off = rt.lane_off;
-        const int i = qb * 128 + r;
-        const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
-        float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);
-        // Row statistics of this query: -LSE * log2(e) (-inf past s, so its
-        // probabilities recompute to 0), and the first estimate
-        // D~ = rowsum(dO * O) from the staged bf16 O and dO tiles (rows past s
-        // were filled with zeros by TMA).  Each half sums its D/2 columns; the
-        // halves meet in shared memory.
-        const float nl2 = i < a.s ? -args.lse[(size_t)bh * a.lse_stride + i] * 1.44269504088896340736f : -INFINITY;
-        if (h == 0) args.lse2_ws[srow] = nl2;
-        bool ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_full), 0, timeout_code(kSiteOFull)));
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->qdo_full), 0, timeout_code(kSiteQFull)));
-        float d_tilde = 0.f;
-        if (ok) {
-            uint64_t acc2 = f2_pack(0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < D / 16; ++u) {
-                const uint32_t off = G::template unit_offset<128>(r, h * (D / 2) + 8 * u);
-                const uint4 ov = ld_shared_v4(sb + C::OFF_O + off);
-                const uint4 gv = ld_shared_v4(sb + C::OFF_DO + off);
-                const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    acc2 = f2_fma(f2_pack(__uint_as_float(ow[e] << 16), __uint_as_float(ow[e] & 0xFFFF0000u)),
-                                  f2_pack(__uint_as_float(gw[e] << 16), __uint_as_float(gw[e] & 0xFFFF0000u)), acc2);
-            }
-            float lo, hi;
-            f2_unpack(acc2, lo, hi);
-            d_tilde = lo + hi;
-        }
-        mbar_arrive(bar(bars->o_free));     // the V producer may now overwrite the O tile
-        dred[h * 128 + r] = d_tilde;
-        named_barrier_sync(1, kRowThreads);
-        d_tilde += dred[(h ^ 1) * 128 + r];
-        named_barrier_sync(1, kRowThreads);     // dred is reused for the exact statistic
+        float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);   // [2 halves][128]
         const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-        const uint64_t nl22 = f2_pack(nl2, nl2);
-        const uint64_t dt2 = f2_pack(d_tilde, d_tilde);
-        const uint64_t ndt2 = f2_pack(-d_tilde, -d_tilde);
         const uint64_t zs2 = f2_pack(a.keep_scale, a.keep_scale);
         const KeepSwar8 ks(a.thr);
-        uint64_t dacc2 = f2_pack(0.f, 0.f);
-        for (int j = 0; j < nk && ok; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), j & 1, timeout_code(kSiteSFull)));
-            if (!ok) break;
-            tc_fence_after();
-            uint64_t pp[HK / 2];
-            if constexpr (HK == 64) {
-                uint32_t rr[64];
-                tmem_ld64(tmem + C::T_S + lane_off + HK * h, rr);
+        // -LSE * log2(e) of this thread's query in a tile (-inf past s, so its
+        // probabilities recompute to 0); the next tile's value is loaded a whole
+        // tile ahead of its use.
+        auto row_nl2 = [&](int t) -> float {
+            if (t < 0) return 0.f;
+            const DqTile w = dq_tile<BN>(a, t);
+            const int i = w.qb * 128 + r;
+            return i < a.s ? -args.lse[(size_t)w.bh * a.lse_stride + i] * 1.44269504088896340736f : -INFINITY;
+        };
+        float nl2_next = row_nl2(sched.tile(0));
+        int g = 0, nx = 0;
+        bool ok = true;
+        for (int u = 0; ok; ++u) {
+            const int t = sched.tile(u);
+            if (t < 0) break;
+            const DqTile w = dq_tile<BN>(a, t);
+            const int qb = w.qb, bh = w.bh, nk = w.nk;
+            const int i = qb * 128 + r;
+            const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
+            const float nl2 = nl2_next;
+            nl2_next = row_nl2(sched.tile(u + 1));
+            if (h == 0) args.lse2_ws[srow] = nl2;
+            const uint64_t nl22 = f2_pack(nl2, nl2);
+            // The first estimate D~ = rowsum(dO * O) comes from the staged bf16 O
+            // and dO tiles (rows past s were filled with zeros by TMA), formed in
+            // the first block after its probabilities, which hides the O load;
+            // both halves sum the whole row.
+            float d_tilde = 0.f;
+            uint64_t dt2 = 0, ndt2 = 0;
+            uint64_t dacc2 = f2_pack(0.f, 0.f);
+            for (int j = 0; j < nk && ok; ++j, ++g) {
+                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
+                if (!ok) break;
+                tc_fence_after();
+                uint64_t pp[HK / 2];
+                if constexpr (HK == 64) {
+                    uint32_t rr[64];
+                    tmem_ld64(tmem + C::T_S + lane_off + HK * h, rr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pp[e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-            } else {
-                uint32_t rr[32];
-                tmem_ld32(tmem + C::T_S + lane_off + HK * h, rr);
+                    for (int e = 0; e < 32; ++e)
+                        pp[e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                } else {
+                    uint32_t rr[32];
+                    tmem_ld32(tmem + C::T_S + lane_off + HK * h, rr);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pp[e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-            }
-            const int key0 = j * BN + HK * h;
-            // Scores of keys this query does not see (past the diagonal, or past the
-            // last key) become -inf before the exponential; only the blocks that hold
-            // such keys run this (a uniform branch), the others go straight on.
-            const int k_end = a.causal ? i + 1 : a.s_k;    // first key not seen
-            if (key0 + HK > (a.causal ? qb * 128 : a.s_k)) {
+                    for (int e = 0; e < 16; ++e)
+                        pp[e] = f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                }
+                const int key0 = j * BN + HK * h;
+                // Scores of keys this query does not see (past the diagonal, or past the
+                // last key) become -inf before the exponential; only the blocks that
+                // hold such keys run this (a uniform branch), the others go straight on.
+                const int k_end = a.causal ? i + 1 : a.s_k;    // first key not seen
+                if (key0 + HK > (a.causal ? qb * 128 : a.s_k)) {
+#pragma unroll
+                    for (int e = 0; e < HK / 2; ++e) {
+                        float lo, hi;
+                        f2_unpack(pp[e], lo, hi);
+                        if (key0 + 2 * e >= k_end) lo = -INFINITY;
+                        if (key0 + 2 * e + 1 >= k_end) hi = -INFINITY;
+                        pp[e] = f2_pack(lo, hi);
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < HK / 2; ++e) {
                     float lo, hi;
-                    f2_unpack(pp[e], lo, hi);
-                    if (key0 + 2 * e >= k_end) lo = -INFINITY;
-                    if (key0 + 2 * e + 1 >= k_end) hi = -INFINITY;
-                    pp[e] = f2_pack(lo, hi);
+                    f2_unpack(f2_fma(pp[e], sc2, nl22), lo, hi);
+                    pp[e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
                 }
-            }
+                // P (before dropout) over the first HK/2 of this half's S columns, for PK += P K
+                {
+                    uint32_t pw[HK / 2];
 #pragma unroll
-            for (int e = 0; e < HK / 2; ++e) {
-                float lo, hi;
-                f2_unpack(f2_fma(pp[e], sc2, nl22), lo, hi);
-                pp[e] = f2_pack(ex2_approx(lo), ex2_approx(hi));
-            }
-            // P (before dropout) over the first HK/2 of this half's S columns, for PK += P K
-            {
-                uint32_t pw[HK / 2];
-#pragma unroll
-                for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(pp[e]);
-                if constexpr (HK / 2 == 32) {
-                    tmem_st32(tmem + C::T_S + lane_off + HK * h, pw);
-                } else {
-                    tmem_st16(tmem + C::T_S + lane_off + HK * h, pw);
+                    for (int e = 0; e < HK / 2; ++e) pw[e] = pack_bf16x2(pp[e]);
+                    if constexpr (HK / 2 == 32) {
+                        tmem_st32(tmem + C::T_S + lane_off + HK * h, pw);
+                    } else {
+                        tmem_st16(tmem + C::T_S + lane_off + HK * h, pw);
+                    }
                 }
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(bars->p_full));
-            // The keep decisions of this block's keys (two Philox calls of 16 keys per
-            // 32, one SWAR test per output word: keys 4k .. 4k + 3 of the half in
-            // keep[k]) are drawn here, while the tensor core forms P K, dQ of the block
-            // before and this block's dP: they need no product, and the phase after dP
-            // is the one the tensor core waits for.
-            uint32_t keep[HK / 4];
-            if (DROP) {
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(bars->p_full));
+                // The keep decisions of this block's keys (two Philox calls of 16 keys per
+                // 32, one SWAR test per output word: keys 4k .. 4k + 3 of the half in
+                // keep[k]) are drawn here, while the tensor core forms P K, dQ of the block
+                // before and this block's dP: they need no product, and the phase after dP
+                // is the one the tensor core waits for.
+                uint32_t keep[HK / 4];
+                if (DROP) {
+#pragma unroll
+                    for (int c32 = 0; c32 < HK / 32; ++c32) {
+                        const uint32_t grp = (uint32_t)(key0 >> 4) + 2u * (uint32_t)c32;
+                        const uint4 w0 = philox4x32_10_rk(grp, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
+                        const uint4 w1 = philox4x32_10_rk(grp + 1u, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
+                        uint32_t* kc = keep + 8 * c32;
+                        kc[0] = ks(w0.x); kc[1] = ks(w0.y); kc[2] = ks(w0.z); kc[3] = ks(w0.w);
+                        kc[4] = ks(w1.x); kc[5] = ks(w1.y); kc[6] = ks(w1.z); kc[7] = ks(w1.w);
+                        if constexpr (MWS) {
+                            // hand the bits to the dK/dV kernel: key quarter of the 128-key
+                            // block, query unit (rows 0-63 / 64-127) and row within it
+                            uint32_t k8[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) k8[k] = kc[k];
+                            const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
+                            const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
+                                                (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
+                            args.mask_ws[word] = keep_bits32(k8);
+                        }
+                    }
+                }
+                if (j == 0) {
+                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_full), u & 1, timeout_code(kSiteOFull)));
+                    if (ok)
+                        ok = __all_sync(0xffffffffu,
+                                        wait_bounded(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull)));
+                    if (!ok) break;
+                    uint64_t acc2 = f2_pack(0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint32_t off = G::template unit_offset<128>(r, 8 * c);
+                        const uint4 ov = ld_shared_v4(sb + C::OFF_O + off);
+                        const uint4 gv = ld_shared_v4(sb + C::OFF_DO + off);
+                        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc2 = f2_fma(f2_pack(__uint_as_float(ow[e] << 16), __uint_as_float(ow[e] & 0xFFFF0000u)),
+                                          f2_pack(__uint_as_float(gw[e] << 16), __uint_as_float(gw[e] & 0xFFFF0000u)),
+                                          acc2);
+                    }
+                    mbar_arrive(bar(bars->q_empty));    // this thread has read dO
+                    float lo, hi;
+                    f2_unpack(acc2, lo, hi);
+                    d_tilde = lo + hi;
+                    dt2 = f2_pack(d_tilde, d_tilde);
+                    ndt2 = f2_pack(-d_tilde, -d_tilde);
+                }
+                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
                 for (int c32 = 0; c32 < HK / 32; ++c32) {
-                    const uint32_t grp = (uint32_t)(key0 >> 4) + 2u * (uint32_t)c32;
-                    const uint4 w0 = philox4x32_10_rk(grp, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
-                    const uint4 w1 = philox4x32_10_rk(grp + 1u, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
-                    uint32_t* kc = keep + 8 * c32;
-                    kc[0] = ks(w0.x); kc[1] = ks(w0.y); kc[2] = ks(w0.z); kc[3] = ks(w0.w);
-                    kc[4] = ks(w1.x); kc[5] = ks(w1.y); kc[6] = ks(w1.z); kc[7] = ks(w1.w);
-                    if constexpr (MWS) {
-                        // hand the bits to the dK/dV kernel: key quarter of the 128-key block,
-                        // query unit (rows 0-63 / 64-127) and row within it
-                        uint32_t k8[8];
+                    uint32_t rr[32];
+                    tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
+                    uint32_t wd[16];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) k8[k] = kc[k];
-                        const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
-                        const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
-                                            (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
-                        args.mask_ws[word] = keep_bits32(k8);
+                    for (int e = 0; e < 16; ++e) {               // pair e: keys 2e, 2e + 1 of the chunk
+                        const int ep = c32 * 16 + e;
+                        uint32_t dlo = rr[2 * e], dhi = rr[2 * e + 1];
+                        if (DROP) {
+                            // dropped elements' dP_d is cleared; kept ones carry 1/(1-p) below
+                            dlo &= keep_mask32(keep[8 * c32 + (e >> 1)], 2 * (e & 1));
+                            dhi &= keep_mask32(keep[8 * c32 + (e >> 1)], 2 * (e & 1) + 1);
+                        }
+                        const uint64_t dp = f2_pack(__uint_as_float(dlo), __uint_as_float(dhi));
+                        dacc2 = f2_fma(pp[ep], dp, dacc2);
+                        wd[e] = pack_bf16x2(f2_mul(pp[ep], DROP ? f2_fma(dp, zs2, ndt2) : f2_sub(dp, dt2)));
                     }
+                    tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, wd);
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(bars->ds_full));
             }
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), j & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c32 = 0; c32 < HK / 32; ++c32) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + C::T_DP + lane_off + HK * h + c32 * 32, rr);
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {               // pair e: keys 2e, 2e + 1 of the chunk
-                    const int ep = c32 * 16 + e;
-                    uint32_t dlo = rr[2 * e], dhi = rr[2 * e + 1];
-                    if (DROP) {
-                        // dropped elements' dP_d is cleared; kept ones carry 1/(1-p) below
-                        dlo &= keep_mask32(keep[8 * c32 + (e >> 1)], 2 * (e & 1));
-                        dhi &= keep_mask32(keep[8 * c32 + (e >> 1)], 2 * (e & 1) + 1);
-                    }
-                    const uint64_t dp = f2_pack(__uint_as_float(dlo), __uint_as_float(dhi));
-                    dacc2 = f2_fma(pp[ep], dp, dacc2);
-                    w[e] = pack_bf16x2(f2_mul(pp[ep], DROP ? f2_fma(dp, zs2, ndt2) : f2_sub(dp, dt2)));
-                }
-                tmem_st16(tmem + C::T_DP + lane_off + HK * h + c32 * 16, w);
+            // ---- epilogue: the exact row statistic from both halves, then
+            // dQ = scale (dQ~ - (D - D~) PK), staged in the O buffer (its O was
+            // read for D~ before the exchange below) for the producer's TMA store
+            float d_exact;
+            {
+                float lo, hi;
+                f2_unpack(dacc2, lo, hi);
+                d_exact = DROP ? (lo + hi) * a.keep_scale : lo + hi;   // dP = Z dP_d, Z = keep / (1 - p)
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(bars->ds_full));
-        }
-        float d_exact;
-        {
-            float lo, hi;
-            f2_unpack(dacc2, lo, hi);
-            d_exact = DROP ? (lo + hi) * a.keep_scale : lo + hi;   // dP = Z dP_d, Z = keep / (1 - p)
-        }
-        // exact row statistic: the two halves' partial sums
-        dred[h * 128 + r] = d_exact;
-        named_barrier_sync(1, kRowThreads);
-        d_exact += dred[(h ^ 1) * 128 + r];
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
-        if (ok) {
+            dred[h * 128 + r] = d_exact;
+            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xbar), nx++ & 1, timeout_code(kSiteX)));
+            if (!ok) break;
+            d_exact += dred[(h ^ 1) * 128 + r];
+            // every row thread has read the region before anyone writes it again
+            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xbar), nx++ & 1, timeout_code(kSiteX)));
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), u & 1, timeout_code(kSiteAcc)));
+            if (!ok) break;
             tc_fence_after();
             const float eps = d_exact - d_tilde;
 #pragma unroll 1
@@ -823,22 +946,17 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_ld32(tmem + C::T_DQ + lane_off + c32 * 32, rq);
                 tmem_ld32(tmem + C::T_PK + lane_off + c32 * 32, rp);
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    rq[e] = __float_as_uint(fmaf(-eps, __uint_as_float(rp[e]), __uint_as_float(rq[e])));
-                stage_row32<D, 128>(sb + C::OFF_Q, r, c32 * 32, rq, a.scale);
+                for (int c = 0; c < 32; ++c)
+                    rq[c] = __float_as_uint(fmaf(-eps, __uint_as_float(rp[c]), __uint_as_float(rq[c])));
+                stage_row32<D, 128>(sb + C::OFF_O, r, c32 * 32, rq, a.scale);
             }
+            tc_fence_before();
+            mbar_arrive(bar(bars->acc_free));   // the next tile's P K and dQ may overwrite them
+            fence_proxy_async_smem();
+            mbar_arrive(bar(bars->dq_staged));
             if (h == 0) args.delta_ws[srow] = -d_exact;    // the dK/dV kernel adds it
         }
-        fence_proxy_async_smem();
-        named_barrier_sync(1, kRowThreads);
-        if (h == 0 && r == 0 && !bars->abort_flag) {
-            for (int ch = 0; ch < G::NCH; ++ch)
-                tma_store_3d(&tm_dq, sb + C::OFF_Q + ch * C::QCH, ch * G::CW, qb * 128, bh);
-            bulk_commit();
-            bulk_wait_read0();
-        }
     }
-
     __syncthreads();
     if (bars->abort_flag) {
         for (int k = 0; k < 20; ++k) __nanosleep(50000);
@@ -875,7 +993,8 @@ static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     auto kern = attn_bwd_dq_kernel<D, DROP, MWS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
-    const unsigned grid = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
+    const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
+    const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
     return (int)cudaGetLastError();
 }
@@ -905,8 +1024,8 @@ int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap&
 {
 #define AC_DQ_CASE(DD)                                                                              \
     case DD:                                                                                        \
-        return !dropout     ? launch_dq_t<DD, false, false>(tq, tk, tv, tdo, to, tdq, a, stream)        \
-               : a.mask_ws ? launch_dq_t<DD, true, true>(tq, tk, tv, tdo, to, tdq, a, stream)         \
+        return !dropout     ? launch_dq_t<DD, false, false>(tq, tk, tv, tdo, to, tdq, a, stream)             \
+               : a.mask_ws ? launch_dq_t<DD, true, true>(tq, tk, tv, tdo, to, tdq, a, stream)              \
                            : launch_dq_t<DD, true, false>(tq, tk, tv, tdo, to, tdq, a, stream);
     switch (d) {
         AC_DQ_CASE(64)

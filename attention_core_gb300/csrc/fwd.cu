@@ -227,7 +227,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else if (alive && warp == 1) {
-        if (lane == 0) {
+        {   // the whole warp issues (see mma_ss)
             // ---- MMA issuer.  One stream over all blocks of all tiles of this CTA:
             // S_g, then O += P_{g-1} V_{g-1} for the block before (which may belong to
             // the previous tile), so the next tile's first scores overlap the last
@@ -238,12 +238,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 int g, j, nk, u;
             };
             auto issue_pv = [&](const Blk& k) -> bool {
-                if (k.j == 0 && !wait_bounded(wc, bar(bars->o_free), (k.u & 1) ^ 1, timeout_code(kSiteOFree)))
+                if (k.j == 0 && !wait_warp(wc, bar(bars->o_free), (k.u & 1) ^ 1, timeout_code(kSiteOFree)))
                     return false;
-                if (!wait_bounded(wc, bar(bars->p_full[k.g & 1]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
+                if (!wait_warp(wc, bar(bars->p_full[k.g & 1]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
                     return false;
                 const int st = k.g % ST;
-                if (!wait_bounded(wc, bar(bars->v_full[st]), (k.g / ST) & 1, timeout_code(kSiteVFull)))
+                if (!wait_warp(wc, bar(bars->v_full[st]), (k.g / ST) & 1, timeout_code(kSiteVFull)))
                     return false;
                 tc_fence_after();
                 const uint32_t vbase = sb + C::OFF_V + st * C::TILE;
@@ -268,16 +268,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // tile's Q and first K block are already resident: it must never wait on
                 // this tile's loads.
                 const int qs = u % C::NQ;
-                if (prev.g >= 0 && (!mbar_test_wait(bar(bars->q_full[qs]), (u / C::NQ) & 1) ||
-                                    !mbar_test_wait(bar(bars->k_full[g % ST]), (g / ST) & 1))) {
+                if (prev.g >= 0 && (!test_wait_warp(bar(bars->q_full[qs]), (u / C::NQ) & 1) ||
+                                    !test_wait_warp(bar(bars->k_full[g % ST]), (g / ST) & 1))) {
                     ok = issue_pv(prev);
                     prev.g = -1;
                     if (!ok) break;
                 }
-                ok = wait_bounded(wc, bar(bars->q_full[qs]), (u / C::NQ) & 1, timeout_code(kSiteQFull));
+                ok = wait_warp(wc, bar(bars->q_full[qs]), (u / C::NQ) & 1, timeout_code(kSiteQFull));
                 for (int j = 0; j < w.nk && ok; ++j, ++g) {
                     const int st = g % ST;
-                    ok = wait_bounded(wc, bar(bars->k_full[st]), (g / ST) & 1, timeout_code(kSiteKFull));
+                    ok = wait_warp(wc, bar(bars->k_full[st]), (g / ST) & 1, timeout_code(kSiteKFull));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t kbase = sb + C::OFF_K + st * C::TILE;
@@ -297,7 +297,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (ok && prev.g >= 0) ok = issue_pv(prev);
             // every MMA must be complete before the CTA releases TMEM
             mma_commit(bar(bars->drain));
-            wait_bounded(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
+            wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 4) {
         // ---- softmax / epilogue: row = TMEM lane, half = which 64 keys of a block

@@ -59,6 +59,7 @@ struct BwdArgs {
     uint32_t* mask_ws;    // dropout keep bits, written by the dQ kernel and read by the
                           // dK/dV kernel (layout: mask_pair_word); null: dK/dV draws its own
     int32_t d;
+    int32_t num_sms;      // persistent grid size
 };
 
 // Keep bits handed from the dQ kernel to the dK/dV kernel.  For every

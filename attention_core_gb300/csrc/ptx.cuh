@@ -105,6 +105,18 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx& w, uint32_t bar, uin
     }
 }
 
+// Bounded wait taken by a whole warp: true for every lane only if every lane
+// saw the phase complete (a lane that gave up has raised the abort flag).
+__device__ __forceinline__ bool wait_warp(const WaitCtx& w, uint32_t bar, uint32_t parity, int32_t code)
+{
+    return __all_sync(0xffffffffu, wait_bounded(w, bar, parity, code));
+}
+// Non-blocking test, with lane 0's answer given to the whole warp.
+__device__ __forceinline__ bool test_wait_warp(uint32_t bar, uint32_t parity)
+{
+    return __shfl_sync(0xffffffffu, (int)mbar_test_wait(bar, parity), 0) != 0;
+}
+
 // Row threads of a tile: warps 4..11; `half` selects the column half, `row`
 // is the TMEM lane (warp w reads lanes 32 * (w % 4) .. + 31).
 struct RowThread {
@@ -148,6 +160,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
         " [%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+// Pull a tile into L2 ahead of its TMA load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y, int z)
 {
@@ -199,13 +218,21 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // D[tmem] (+)= A[smem] * B[smem]^T   (kind::f16: bf16 in, fp32 accumulate)
+// The MMA issuers are whole warps: every lane runs the issue loop (so the
+// descriptor arithmetic is warp-uniform) and elect.sync picks the one lane that
+// issues each tcgen05 instruction.  A single-thread issue loop loses issue slots
+// to the busy row warps of its sub-partition and slows the tensor pipe; the
+// warp-uniform form does not.  Call these from all 32 lanes, converged.
+//
+// D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -214,16 +241,21 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
                                        uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
+// Arrive once on `bar` when every tcgen05 operation issued so far by the
+// elected lane completes (the same lane elect.sync picks for the MMAs: the
+// lowest active one).
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
                  ::"r"(bar) : "memory");
 }
 
