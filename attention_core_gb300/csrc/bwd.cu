@@ -39,7 +39,7 @@ namespace {
 
 enum : int32_t {
     kSiteInject = 1, kSiteKvFull, kSiteQEmpty, kSiteQFull, kSitePFull, kSiteDsFull, kSiteSFull,
-    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePRead, kSiteOFull, kSiteStage,
+    kSiteDpFull, kSiteAcc, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePRead, kSiteOFull, kSiteStage, kSiteRng,
     kSiteX, kSiteDrain
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
@@ -455,11 +455,20 @@ struct DqCfg {
     static constexpr uint32_t KT = G::template tile_bytes<BN>();
     static constexpr uint32_t KCH = G::template chunk_bytes<BN>();
     static constexpr uint32_t RED_BYTES = 2 * 128 * 4;       // [2 halves][128] partial row statistics
+    // Keep bits of a key block, drawn by the RNG warps: [BN / 32][128 rows]
+    // words, key 32 q + c of row r at bit keep_bit_position(c) of word [q][r];
+    // a ring of RNG_ST blocks lets the RNG warps run ahead of the row threads.
+    static constexpr int RNG_ST = 4;
+    static constexpr uint32_t RNG_BYTES = (BN / 32) * 128 * 4;
+    static constexpr uint32_t BAR_BYTES = 512;
     // A K tile is an operand of three products (S, P K and dQ), so its ring slot
-    // frees only when the block's dQ product is done; the K ring takes every
-    // stage that fits beside Q, dO, O and a two-stage V ring, up to four.
-    static constexpr int VST = 2;
-    static constexpr int KST_FIT = (int)((227u * 1024u - 3u * QT - (uint32_t)VST * KT - 256u - RED_BYTES - 1024u) / KT);
+    // frees only when the block's dQ product is done.  V is read by one
+    // product, dP, issued about a block after its slot frees, so where two V
+    // stages would leave the K ring short of four, V gets one; the K ring takes
+    // every stage that fits beside Q, dO, O, V and the keep-bit ring, up to four.
+    static constexpr uint32_t FIXED = 3u * QT + BAR_BYTES + RED_BYTES + RNG_ST * RNG_BYTES + 1024u;
+    static constexpr int VST = (227u * 1024u - FIXED - 2u * KT) / KT >= 4 ? 2 : 1;
+    static constexpr int KST_FIT = (int)((227u * 1024u - FIXED - (uint32_t)VST * KT) / KT);
     static constexpr int KST = KST_FIT < 4 ? KST_FIT : 4;
     static_assert(KST >= 2, "K ring");
     static constexpr uint32_t OFF_Q = 0;
@@ -468,8 +477,9 @@ struct DqCfg {
     static constexpr uint32_t OFF_K = 3 * QT;
     static constexpr uint32_t OFF_V = OFF_K + KST * KT;
     static constexpr uint32_t OFF_BAR = OFF_V + VST * KT;
-    static constexpr uint32_t OFF_RED = OFF_BAR + 256;
-    static constexpr uint32_t SMEM = OFF_RED + RED_BYTES + 1024;
+    static constexpr uint32_t OFF_RED = OFF_BAR + BAR_BYTES;
+    static constexpr uint32_t OFF_RNG = OFF_RED + RED_BYTES;
+    static constexpr uint32_t SMEM = OFF_RNG + RNG_ST * RNG_BYTES + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     // TMEM: S (later P in the first half of each row half) | dP (later dS~) | dQ~ | PK
     static constexpr uint32_t T_S = 0, T_DP = BN, T_DQ = 2 * BN, T_PK = 2 * BN + D;
@@ -483,11 +493,12 @@ struct DqBars {
     uint64_t s_full, p_full, dp_full, ds_full;
     uint64_t acc_done, acc_free;       // a tile's accumulators complete / read out
     uint64_t xbar;                     // exchange barrier of the 256 row threads
+    uint64_t rng_full[4], rng_empty[4];  // keep-bit ring
     uint64_t drain, never;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
-static_assert(sizeof(DqBars) <= 256, "barrier block");
+static_assert(sizeof(DqBars) <= DqCfg<64>::BAR_BYTES, "barrier block");
 
 // Work tile t (longest first): query block, flattened query head, KV head and
 // key blocks.
@@ -510,7 +521,7 @@ __device__ __forceinline__ DqTile dq_tile(const CommonArgs& a, int t)
 }  // namespace
 
 template <int D, bool DROP, bool MWS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dq,
@@ -552,6 +563,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(bar(bars->acc_done), 1);
         mbar_init(bar(bars->acc_free), kRowThreads);
         mbar_init(bar(bars->xbar), kRowThreads);
+        for (int st = 0; st < C::RNG_ST; ++st) {
+            mbar_init(bar(bars->rng_full[st]), kRngThreads);
+            mbar_init(bar(bars->rng_empty[st]), kRowThreads);
+        }
         mbar_init(bar(bars->drain), 1);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
@@ -578,7 +593,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     bool alive = true;
     if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
 
+    // Registers: the row warps raise their share to 176, every other warp
+    // lowers its own to 80 (8 x 32 x 176 + 8 x 32 x 80 = 512 threads x 128).
+    // Each role branch adjusts first thing, before any wait.
     if (alive && warp == 0) {
+        regs_lower<80>();
         if (lane == 0) {
             // ---- TMA producer: the K ring over all blocks of all tiles
             int g = 0;
@@ -643,6 +662,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
     } else if (alive && warp == 2) {
+        regs_lower<80>();
         if (lane == 0) {
             // ---- TMA producer: the V ring over all blocks of all tiles
             int g = 0;
@@ -663,6 +683,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
     } else if (alive && warp == 1) {
+        regs_lower<80>();
         {   // the whole warp issues (see mma_ss)
             // ---- MMA issuer.  Per tile: S0 dP0 | PK0 S1 dQ0 dP1 | PK1 S2 dQ1 dP2 | ...
             // PK_j reads P_j from the S columns as soon as the row threads have
@@ -744,7 +765,51 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mma_commit(bar(bars->drain));
             wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
-    } else if (alive && warp >= 4) {
+    } else if (alive && warp >= 12 && DROP) {
+        regs_lower<80>();
+        // ---- RNG warps: the keep bits of every key block, drawn ahead of the
+        // row threads into the ring (thread = query row of the tile; two Philox
+        // calls of 16 keys per 32-key word, one SWAR test per output word), and
+        // handed to the dK/dV kernel when it reads them instead of drawing.
+        const int r = (int)threadIdx.x - 12 * 32;
+        const KeepSwar8 ks(a.thr);
+        int g = 0;
+        bool ok = true;
+        for (int u = 0; ok; ++u) {
+            const int t = sched.tile(u);
+            if (t < 0) break;
+            const DqTile w = dq_tile<BN>(a, t);
+            const uint32_t i = (uint32_t)(w.qb * 128 + r);
+            const uint32_t bhc = (uint32_t)w.bh + a.bh0;
+            for (int j = 0; j < w.nk; ++j, ++g) {
+                const int rs = g % C::RNG_ST;
+                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->rng_empty[rs]), ((g / C::RNG_ST) & 1) ^ 1,
+                                                          timeout_code(kSiteRng)));
+                if (!ok) break;
+                uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw + pad + C::OFF_RNG + rs * C::RNG_BYTES);
+#pragma unroll
+                for (int q = 0; q < BN / 32; ++q) {
+                    const uint32_t grp = (uint32_t)((j * BN) >> 4) + 2u * (uint32_t)q;
+                    const uint4 w0 = philox4x32_10_rk(grp, i, bhc, a.offset, a.rk);
+                    const uint4 w1 = philox4x32_10_rk(grp + 1u, i, bhc, a.offset, a.rk);
+                    const uint32_t k8[8] = {ks(w0.x), ks(w0.y), ks(w0.z), ks(w0.w),
+                                            ks(w1.x), ks(w1.y), ks(w1.z), ks(w1.w)};
+                    const uint32_t bits = keep_bits32(k8);
+                    ring[q * 128 + r] = bits;
+                    if constexpr (MWS) {
+                        // key quarter of the 128-key block, query unit (rows 0-63 /
+                        // 64-127) and row within it
+                        const int kq = ((j * BN) & 127) + 32 * q;
+                        const size_t word = mask_pair_word(a, w.bh, w.qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
+                                            (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
+                        args.mask_ws[word] = bits;
+                    }
+                }
+                mbar_arrive(bar(bars->rng_full[rs]));
+            }
+        }
+    } else if (alive && warp >= 4 && warp < 12) {
+        regs_raise<176>();
         // ---- row threads: query row = TMEM lane, half = which BN/2 keys of a block
         constexpr int HK = BN / 2;
         const RowThread rt = row_thread();
@@ -753,7 +818,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);   // [2 halves][128]
         const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
         const uint64_t zs2 = f2_pack(a.keep_scale, a.keep_scale);
-        const KeepSwar8 ks(a.thr);
         // -LSE * log2(e) of this thread's query in a tile (-inf past s, so its
         // probabilities recompute to 0); the next tile's value is loaded a whole
         // tile ahead of its use.
@@ -837,34 +901,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(bars->p_full));
-                // The keep decisions of this block's keys (two Philox calls of 16 keys per
-                // 32, one SWAR test per output word: keys 4k .. 4k + 3 of the half in
-                // keep[k]) are drawn here, while the tensor core forms P K, dQ of the block
-                // before and this block's dP: they need no product, and the phase after dP
-                // is the one the tensor core waits for.
-                uint32_t keep[HK / 4];
-                if (DROP) {
-#pragma unroll
-                    for (int c32 = 0; c32 < HK / 32; ++c32) {
-                        const uint32_t grp = (uint32_t)(key0 >> 4) + 2u * (uint32_t)c32;
-                        const uint4 w0 = philox4x32_10_rk(grp, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
-                        const uint4 w1 = philox4x32_10_rk(grp + 1u, (uint32_t)i, (uint32_t)bh + a.bh0, a.offset, a.rk);
-                        uint32_t* kc = keep + 8 * c32;
-                        kc[0] = ks(w0.x); kc[1] = ks(w0.y); kc[2] = ks(w0.z); kc[3] = ks(w0.w);
-                        kc[4] = ks(w1.x); kc[5] = ks(w1.y); kc[6] = ks(w1.z); kc[7] = ks(w1.w);
-                        if constexpr (MWS) {
-                            // hand the bits to the dK/dV kernel: key quarter of the 128-key
-                            // block, query unit (rows 0-63 / 64-127) and row within it
-                            uint32_t k8[8];
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) k8[k] = kc[k];
-                            const int kq = ((j * BN) & 127) + HK * h + 32 * c32;
-                            const size_t word = mask_pair_word(a, bh, qb, (j * BN) >> 7) + (size_t)(r >> 6) * 256 +
-                                                (size_t)(kq >> 5) * 64 + (size_t)(r & 63);
-                            args.mask_ws[word] = keep_bits32(k8);
-                        }
-                    }
-                }
                 if (j == 0) {
                     ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_full), u & 1, timeout_code(kSiteOFull)));
                     if (ok)
@@ -891,6 +927,25 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     d_tilde = lo + hi;
                     dt2 = f2_pack(d_tilde, d_tilde);
                     ndt2 = f2_pack(-d_tilde, -d_tilde);
+                }
+                // The keep decisions of this half's keys, from the RNG warps' bits: keys
+                // 4k .. 4k + 3 of each 32 as the byte sign bits of keep[k] (one shift
+                // and one mask per word, the inverse of keep_bits32).
+                uint32_t keep[HK / 4];
+                if (DROP) {
+                    const int rs = g % C::RNG_ST;
+                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->rng_full[rs]), (g / C::RNG_ST) & 1,
+                                                              timeout_code(kSiteRng)));
+                    if (!ok) break;
+                    const uint32_t* ring =
+                        reinterpret_cast<const uint32_t*>(smem_raw + pad + C::OFF_RNG + rs * C::RNG_BYTES);
+#pragma unroll
+                    for (int c32 = 0; c32 < HK / 32; ++c32) {
+                        const uint32_t bits = ring[(h * (HK / 32) + c32) * 128 + r];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) keep[8 * c32 + k] = (bits << k) & 0x80808080u;
+                    }
+                    mbar_arrive(bar(bars->rng_empty[rs]));
                 }
                 ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
                 if (!ok) break;
@@ -956,6 +1011,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_arrive(bar(bars->dq_staged));
             if (h == 0) args.delta_ws[srow] = -d_exact;    // the dK/dV kernel adds it
         }
+    } else if (alive) {
+        regs_lower<80>();   // idle warps (and the RNG warps without dropout)
     }
     __syncthreads();
     if (bars->abort_flag) {
@@ -995,7 +1052,7 @@ static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return (int)e;
     const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
     const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;
-    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
+    kern<<<grid, kDqThreads, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
     return (int)cudaGetLastError();
 }
 

@@ -15,6 +15,10 @@ constexpr int kBlockRows = 128;
 // sub-partition runs two of them.
 constexpr int kThreads = 384;
 constexpr int kRowThreads = 256;
+// The dQ kernel adds four warps (12..15) that draw the dropout mask ahead of
+// its row threads.
+constexpr int kRngThreads = 128;
+constexpr int kDqThreads = kThreads + kRngThreads;
 
 struct CommonArgs {
     int32_t s;            // queries per head

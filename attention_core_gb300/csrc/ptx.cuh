@@ -199,6 +199,21 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Register reallocation between warps of a warp-specialised block: the
+// warps that need more registers raise their share, the others lower theirs;
+// the shares of all warps must add up to no more than the block was launched
+// with (threads x registers per thread at launch).  Executed by whole warps.
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------ tcgen05 ---
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
