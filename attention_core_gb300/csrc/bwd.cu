@@ -521,7 +521,7 @@ __device__ __forceinline__ DqTile dq_tile(const CommonArgs& a, int t)
 }  // namespace
 
 template <int D, bool DROP, bool MWS>
-__global__ void __launch_bounds__(kDqThreads, 1)
+__global__ void __launch_bounds__(kThreadsRng, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dq,
@@ -593,11 +593,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     bool alive = true;
     if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
 
-    // Registers: the row warps raise their share to 176, every other warp
-    // lowers its own to 80 (8 x 32 x 176 + 8 x 32 x 80 = 512 threads x 128).
-    // Each role branch adjusts first thing, before any wait.
+    // Registers: the row warps raise their share to kDqRowRegs (176), every
+    // other warp lowers its own to kDqOtherRegs (80); kernels.h checks the sum
+    // against the launch.  Each role branch adjusts first thing, before any wait.
     if (alive && warp == 0) {
-        regs_lower<80>();
+        regs_lower<kDqOtherRegs>();
         if (lane == 0) {
             // ---- TMA producer: the K ring over all blocks of all tiles
             int g = 0;
@@ -662,7 +662,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
     } else if (alive && warp == 2) {
-        regs_lower<80>();
+        regs_lower<kDqOtherRegs>();
         if (lane == 0) {
             // ---- TMA producer: the V ring over all blocks of all tiles
             int g = 0;
@@ -683,7 +683,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
     } else if (alive && warp == 1) {
-        regs_lower<80>();
+        regs_lower<kDqOtherRegs>();
         {   // the whole warp issues (see mma_ss)
             // ---- MMA issuer.  Per tile: S0 dP0 | PK0 S1 dQ0 dP1 | PK1 S2 dQ1 dP2 | ...
             // PK_j reads P_j from the S columns as soon as the row threads have
@@ -766,7 +766,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 12 && DROP) {
-        regs_lower<80>();
+        regs_lower<kDqOtherRegs>();
         // ---- RNG warps: the keep bits of every key block, drawn ahead of the
         // row threads into the ring (thread = query row of the tile; two Philox
         // calls of 16 keys per 32-key word, one SWAR test per output word), and
@@ -809,7 +809,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
     } else if (alive && warp >= 4 && warp < 12) {
-        regs_raise<176>();
+        regs_raise<kDqRowRegs>();
         // ---- row threads: query row = TMEM lane, half = which BN/2 keys of a block
         constexpr int HK = BN / 2;
         const RowThread rt = row_thread();
@@ -1012,7 +1012,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (h == 0) args.delta_ws[srow] = -d_exact;    // the dK/dV kernel adds it
         }
     } else if (alive) {
-        regs_lower<80>();   // idle warps (and the RNG warps without dropout)
+        regs_lower<kDqOtherRegs>();   // idle warps (and the RNG warps without dropout)
     }
     __syncthreads();
     if (bars->abort_flag) {
@@ -1050,9 +1050,15 @@ static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     auto kern = attn_bwd_dq_kernel<D, DROP, MWS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
+    // the row warps' register raise waits until the others' shares are free:
+    // refuse a build whose register count cannot cover the shares
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return (int)e;
+    if (fa.numRegs * kThreadsRng < reg_shares(kDqRowRegs, kDqOtherRegs, kThreadsRng))
+        return (int)cudaErrorInvalidConfiguration;
     const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
     const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;
-    kern<<<grid, kDqThreads, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
+    kern<<<grid, kThreadsRng, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
     return (int)cudaGetLastError();
 }
 

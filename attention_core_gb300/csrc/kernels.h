@@ -18,7 +18,20 @@ constexpr int kRowThreads = 256;
 // The dQ kernel adds four warps (12..15) that draw the dropout mask ahead of
 // its row threads.
 constexpr int kRngThreads = 128;
-constexpr int kDqThreads = kThreads + kRngThreads;
+constexpr int kThreadsRng = kThreads + kRngThreads;
+// Register shares after setmaxnreg: row warps / every other warp.  A block
+// is launched with (65536 / threads, rounded down to a multiple of 8)
+// registers per thread, and the shares must add up to no more than that, or
+// the row warps' raise would wait forever; the launcher also checks the
+// count the compiler actually gave the kernel.
+constexpr int kDqRowRegs = 176, kDqOtherRegs = 80;
+constexpr int launch_regs(int threads) { return (65536 / threads) / 8 * 8; }
+constexpr int reg_shares(int row_regs, int other_regs, int threads)
+{
+    return kRowThreads * row_regs + (threads - kRowThreads) * other_regs;
+}
+static_assert(reg_shares(kDqRowRegs, kDqOtherRegs, kThreadsRng) <= kThreadsRng * launch_regs(kThreadsRng),
+              "dQ register shares");
 
 struct CommonArgs {
     int32_t s;            // queries per head
