@@ -73,8 +73,6 @@ int check_params(const attn_core_params* p)
     if (p == nullptr) return ATTN_CORE_ERR_INVALID_ARG;
     if (p->b <= 0 || p->h_q <= 0 || p->h_kv <= 0 || p->s <= 0 || p->d <= 0 || p->s_kv < 0)
         return ATTN_CORE_ERR_INVALID_ARG;
-    // Causal masking is defined for square score matrices only (s_kv == s).
-    if (p->causal && keys_of(p) != p->s) return ATTN_CORE_ERR_INVALID_ARG;
     if (p->h_q % p->h_kv != 0) return ATTN_CORE_ERR_INVALID_ARG;
     if (p->causal != 0 && p->causal != 1) return ATTN_CORE_ERR_INVALID_ARG;
     if (!(p->p_drop >= 0.0f && p->p_drop < 1.0f)) return ATTN_CORE_ERR_INVALID_ARG;
@@ -196,6 +194,9 @@ size_t padded_rows(const attn_core_params* p)
 size_t mask_bytes(const attn_core_params* p)
 {
     if (drop_threshold(p->p_drop) == 0 || p->d > 128 || (p->flags & ATTN_CORE_FLAG_REDRAW_MASK)) return 0;
+    // the hand-over layout covers the square causal pattern; causal
+    // cross-attention draws the mask twice
+    if (p->causal && keys_of(p) != p->s) return 0;
     const ac::CommonArgs c = common_args(p);
     return sizeof(uint32_t) * ac::mask_ws_words(c);
 }
@@ -352,6 +353,24 @@ int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
     if (ac::launch_bwd_dq(p->d, drop, tq128, tkb, tvb, tdo128, to128, tdq128, a, st) != 0) return ATTN_CORE_ERR_CUDA;
     if ((rc = record(p->timing_events, 1, st)) || (rc = record(p->timing_events, 2, st))) return rc;
     if (ac::launch_bwd_dkdv(p->d, drop, tqb, tk, tv, tdob, tdk, tdv, a, st) != 0) return ATTN_CORE_ERR_CUDA;
+    // Causal with more keys than queries: keys from the end of the last query
+    // block on are seen by no query (top-left alignment) and the dK/dV kernel
+    // skips their blocks, so their gradients are set to zero here.
+    const int64_t kz = (int64_t)a.c.n_blk * kBlockRows;
+    if (p->causal && sk > kz) {
+        const size_t row_bytes = (size_t)g.kv_row * sizeof(uint16_t);
+        for (void* t : {dk, dv}) {
+            uint8_t* base = static_cast<uint8_t*>(t) + (size_t)kz * row_bytes;
+            cudaError_t e;
+            if (g.kv_head == p->d) {        // token-major rows: all heads of a row are adjacent
+                e = cudaMemsetAsync(base, 0, (size_t)(sk - kz) * row_bytes, st);
+            } else {                        // head-major: rows kz .. sk - 1 of every head
+                e = cudaMemset2DAsync(base, (size_t)g.kv_head * sizeof(uint16_t), 0, (size_t)(sk - kz) * row_bytes,
+                                      (size_t)g.kv_heads, st);
+            }
+            if (e != cudaSuccess) return ATTN_CORE_ERR_CUDA;
+        }
+    }
     return record(p->timing_events, 3, st);
 }
 
@@ -405,7 +424,6 @@ int check_varlen(const attn_core_varlen_params* vp, int64_t* total_q, int64_t* t
     for (int i = 0; i < vp->n_seq; ++i) {
         const int32_t lq = cq[i + 1] - cq[i], lk = ck[i + 1] - ck[i];
         if (lq < 0 || lk < 0 || (lq > 0 && lk == 0)) return ATTN_CORE_ERR_INVALID_ARG;
-        if (vp->base.causal && lq != lk) return ATTN_CORE_ERR_INVALID_ARG;
         if (lq == 0) continue;
         attn_core_params ps = vp->base;
         ps.b = 1;

@@ -870,8 +870,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 // Scores of keys this query does not see (past the diagonal, or past the
                 // last key) become -inf before the exponential; only the blocks that
                 // hold such keys run this (a uniform branch), the others go straight on.
-                const int k_end = a.causal ? i + 1 : a.s_k;    // first key not seen
-                if (key0 + HK > (a.causal ? qb * 128 : a.s_k)) {
+                const int k_end = a.causal ? min(i + 1, a.s_k) : a.s_k;    // first key not seen
+                if (key0 + HK > (a.causal ? min(qb * 128, a.s_k) : a.s_k)) {
 #pragma unroll
                     for (int e = 0; e < HK / 2; ++e) {
                         float lo, hi;
@@ -1037,7 +1037,10 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
-    const unsigned grid = (unsigned)a.c.n_blk_k * n_bkv;
+    // under a causal mask the key blocks past the last query block are seen by
+    // no query (the caller zeroes their gradients)
+    const unsigned n_kb = (unsigned)(a.c.causal && a.c.n_blk < a.c.n_blk_k ? a.c.n_blk : a.c.n_blk_k);
+    const unsigned grid = n_kb * n_bkv;
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return (int)cudaGetLastError();
 }

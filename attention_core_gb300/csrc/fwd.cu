@@ -99,7 +99,7 @@ __device__ __forceinline__ FwdTile fwd_tile(const CommonArgs& a, int t)
     w.bh = t % a.n_bh;
     const int group = a.h_q / a.h_kv;
     w.bkv = (w.bh / a.h_q) * a.h_kv + (w.bh % a.h_q) / group;
-    w.nk = a.causal ? (w.qb + 1) : a.n_blk_k;
+    w.nk = a.causal ? min(w.qb + 1, a.n_blk_k) : a.n_blk_k;   // top-left causal: keys 0 .. i
     return w;
 }
 
@@ -336,7 +336,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int c = 0; c < 64; ++c)
                         if (64 * h + c > r) x[c] = -INFINITY;
                 }
-                if (!a.causal && key0 + 64 > a.s_k) {
+                if (key0 + 64 > a.s_k) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
                         if (key0 + c >= a.s_k) x[c] = -INFINITY;

@@ -59,8 +59,7 @@ extern "C" {
  * output has been written, except ATTN_CORE_ERR_CUDA from a launch, which
  * reports the CUDA error of that launch. */
 #define ATTN_CORE_OK 0
-#define ATTN_CORE_ERR_INVALID_ARG 1         /* null pointer, bad shape, p outside [0,1), offset >= 2^32,
-                                               causal with s_kv != s */
+#define ATTN_CORE_ERR_INVALID_ARG 1         /* null pointer, bad shape, p outside [0,1), offset >= 2^32 */
 #define ATTN_CORE_ERR_UNSUPPORTED 2         /* head dimension or device not supported */
 #define ATTN_CORE_ERR_MISALIGNED 3          /* a pointer is not 16-byte aligned (workspace: 256) */
 #define ATTN_CORE_ERR_WORKSPACE_TOO_SMALL 4 /* bwd workspace smaller than attn_core_bwd_workspace_bytes */
@@ -95,9 +94,11 @@ typedef struct {
      * dQ, dK/dV), recorded on `stream` immediately before and
      * after each launch.  May be NULL. */
     void** timing_events;
-    /* Keys (and value rows) per KV head; 0 selects s.  s_kv != s requires
-     * causal == 0.  The dropout mask of (query i, key j) does not depend on
-     * s or s_kv. */
+    /* Keys (and value rows) per KV head; 0 selects s.  With s_kv != s the
+     * causal mask is aligned top-left: query i sees keys 0 .. min(i, s_kv - 1)
+     * (with more keys than queries, keys s .. s_kv - 1 are seen by no query
+     * and get zero dK and dV).  The dropout mask of (query i, key j) does not
+     * depend on s or s_kv. */
     int32_t s_kv;
 } attn_core_params;
 
@@ -125,8 +126,9 @@ int attn_core_fwd(const attn_core_params* p, const void* q, const void* k, const
  *                                       d <= 128,
  *   2048 * b * h_q * N                  the dropout keep bits, one bit per
  *                                       (query, key) of each 128 x 128 block,
- * with N = n (n + 1) / 2 blocks per head if causal (n = ceil(s / 128)), else
- * ceil(s / 128) * ceil(s_kv / 128).  The keep bits are transient (written and
+ * with N = n (n + 1) / 2 blocks per head if causal with s_kv == s
+ * (n = ceil(s / 128)), ceil(s / 128) * ceil(s_kv / 128) if not causal, and no
+ * keep bits for causal with s_kv != s (the second kernel draws the mask again).  The keep bits are transient (written and
  * read within one backward call) but scale with s^2: 6.7 MB for b = 2,
  * h_q = 12, s = 2048, and 272 MB for h_q = 64, s = 8192.  Callers short of
  * memory set ATTN_CORE_FLAG_REDRAW_MASK to leave them out. */
@@ -184,8 +186,8 @@ int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, co
  *   K, V, dK, dV : bf16 [total_k, h_kv, d]
  *   LSE          : fp32 [h_q, total_q]
  * Each sequence attends only within itself, as batch element i of the
- * padded layout would: the same causal rule (causal needs equal query and
- * key counts per sequence), and the same dropout mask (Philox counter word 2
+ * padded layout would: the same causal rule (top-left aligned when a
+ * sequence's query and key counts differ), and the same dropout mask (Philox counter word 2
  * = i * h_q + head).  The sequence tables are HOST arrays of n_seq + 1 int32
  * starting at 0 and nondecreasing; an empty sequence is skipped, one with
  * queries but no keys is invalid; one with keys but no queries gets zero

@@ -7,12 +7,16 @@ head, position) the error is the largest absolute difference divided by that
 row's own largest absolute oracle value; the test value is the maximum over
 rows.  No floor is applied to a row's denominator, with one exception: rows
 whose oracle max-abs is below NEAR_ZERO (1e-3) times the median row max-abs
-of the compared rows.  Those rows cancel to (nearly) zero by construction --
-causal query 0 has dQ = 0 exactly, one key gives dK = 0 -- and carry the
-rounding residue of terms as large as a typical row, which no relative bar
-can meet.  They are held to an absolute bound instead: TOL times the median
-row max-abs, the absolute error a typical row is allowed.  If every compared
-row is exactly zero the bound is TOL in absolute terms.
+of the compared rows that are not exactly zero.  Those rows cancel to
+(nearly) zero by construction -- causal query 0 has dQ = 0 exactly, one key
+gives dK = 0 -- and carry the rounding residue of terms as large as a
+typical row, which no relative bar can meet.  They are held to an absolute
+bound instead: TOL times that median, the absolute error a typical row is
+allowed.  Rows that are exactly zero in the oracle (keys that no query sees
+under a top-left causal mask with more keys than queries) have no terms at
+all, so they do not enter the median that sets the typical row; they are
+held to the same absolute bound.  If every compared row is exactly zero the
+bound is TOL in absolute terms.
 
 Every call records the strict figure (the largest relative error over the
 rows held to the relative bar), the near-zero rows' error against their
@@ -40,7 +44,8 @@ def row_errors(gpu, ref) -> dict:
     r = np.asarray(ref, dtype=np.float64).reshape(-1, np.shape(ref)[-1])
     rowmax = np.abs(r).max(axis=1)
     err = np.abs(g - r).max(axis=1)
-    med = float(np.median(rowmax))
+    nonzero = rowmax[rowmax > 0]
+    med = float(np.median(nonzero)) if nonzero.size else 0.0
     near = rowmax < NEAR_ZERO * med if med > 0 else np.ones_like(rowmax, dtype=bool)
     strict = float((err[~near] / rowmax[~near]).max()) if (~near).any() else 0.0
     near_err = float(err[near].max() / (med if med > 0 else 1.0)) if near.any() else 0.0

@@ -107,6 +107,41 @@ def test_cross_attention_matches_oracle(case):
     assert all(e <= TOL for e in errs.values()), errs
 
 
+# Causal cross-attention, aligned top-left (query i sees keys 0 .. min(i, s_kv - 1)):
+# (b, h_q, h_kv, s, s_kv, d, p_drop); more keys than queries (whole key blocks that no
+# query sees), fewer, ragged, GQA, each head dimension.
+CAUSAL_CROSS = [
+    (1, 2, 2, 200, 330, 64, 0.1),
+    (1, 2, 2, 330, 200, 128, 0.1),
+    (2, 4, 2, 129, 520, 96, 0.2),
+    (1, 2, 1, 300, 130, 160, 0.1),
+    (1, 2, 2, 256, 640, 128, 0.0),
+    (1, 2, 2, 77, 1, 64, 0.1),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL_CROSS,
+                         ids=lambda c: f"b{c[0]}_h{c[1]}x{c[2]}_s{c[3]}_kv{c[4]}_d{c[5]}_p{c[6]}")
+def test_causal_cross_attention_matches_oracle(case):
+    b, hq, hkv, s, skv, d, p = case
+    seed = 977 + s + skv
+    t = random_inputs(b, hq, hkv, s, d, seed=s * 11 + skv, s_kv=skv)
+    out = run_gpu(t, True, p, seed)
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=True, p_drop=p, seed=seed, s_kv=skv)
+    ro, rlse = oracle.fwd(pr, t.q, t.k, t.v)
+    rdq, rdk, rdv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+    errs = {"o": row_rel_err(to_np(out["o"]), ro, "causal-cross o"),
+            "dq": row_rel_err(to_np(out["dq"]), rdq, "causal-cross dq"),
+            "dk": row_rel_err(to_np(out["dk"]), rdk, "causal-cross dk"),
+            "dv": row_rel_err(to_np(out["dv"]), rdv, "causal-cross dv")}
+    lse_err = float(np.abs(to_np(out["lse"]) - rlse).max())
+    assert lse_err <= LSE_TOL, lse_err
+    assert all(e <= TOL for e in errs.values()), errs
+    if skv > s:
+        # keys past the last query are seen by no query: exactly zero gradients
+        assert not to_np(out["dk"])[:, :, s:].any() and not to_np(out["dv"])[:, :, s:].any()
+
+
 @pytest.mark.parametrize("shape", [(1, 2, 128, 64), (1, 2, 300, 128), (2, 1, 260, 96),
                                    (1, 2, 200, 160)])
 @pytest.mark.parametrize("causal", [True, False])

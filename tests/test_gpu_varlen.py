@@ -47,6 +47,7 @@ CASES = [
     ([200, 64, 129], None, 4, 2, 128, True, 0.1),
     ([100, 300], [257, 40], 2, 1, 128, False, 0.2),
     ([90, 150], None, 2, 2, 160, True, 0.1),
+    ([100, 300, 5], [257, 40, 5], 2, 1, 128, True, 0.1),    # causal, top-left per sequence
 ]
 
 
