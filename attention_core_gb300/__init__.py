@@ -66,7 +66,8 @@ class _CParams(ctypes.Structure):
 class _CVarlenParams(ctypes.Structure):
     _fields_ = [("base", _CParams), ("n_seq", ctypes.c_int32),
                 ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)),
-                ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32))]
+                ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32)),
+                ("cu_seqlens_q_dev", ctypes.c_void_p), ("cu_seqlens_k_dev", ctypes.c_void_p)]
 
 
 class _CDalParams(ctypes.Structure):
@@ -242,32 +243,47 @@ def attn_core_dropout_add_ln_bwd(p: DalParams, dy: int, dz_next: int, z: int, me
                                                        workspace, workspace_bytes, stream or None)
 
 
-def _varlen_c(p: Params, cu_q, cu_k):
-    """(_CVarlenParams, keep-alive arrays) for host sequence tables."""
+def _varlen_c(p: Params, cu_q, cu_k, cu_q_dev: int = 0, cu_k_dev: int = 0):
+    """(_CVarlenParams, keep-alive arrays) for host sequence tables and the
+    device addresses of their copies."""
     aq = (ctypes.c_int32 * len(cu_q))(*[int(x) for x in cu_q])
     ak = (ctypes.c_int32 * len(cu_k))(*[int(x) for x in cu_k]) if cu_k is not None else None
     vp = _CVarlenParams(p.to_c(), len(cu_q) - 1, ctypes.cast(aq, ctypes.POINTER(ctypes.c_int32)),
-                        ctypes.cast(ak, ctypes.POINTER(ctypes.c_int32)) if ak is not None else None)
+                        ctypes.cast(ak, ctypes.POINTER(ctypes.c_int32)) if ak is not None else None,
+                        cu_q_dev or None, cu_k_dev or None)
     return vp, (aq, ak)
 
 
-def attn_core_fwd_varlen(p: Params, cu_q, cu_k, q: int, k: int, v: int, o: int, lse: int, stream: int) -> int:
+def attn_core_fwd_varlen(p: Params, cu_q, cu_k, q: int, k: int, v: int, o: int, lse: int, stream: int, *,
+                         cu_q_dev: int = 0, cu_k_dev: int = 0) -> int:
     """p supplies h_q, h_kv, d, causal, p_drop, scale, seed, offset, dev_status,
-    flags and wait_timeout_ms; cu_q / cu_k are host sequence tables."""
-    vp, keep = _varlen_c(p, cu_q, cu_k)
+    flags and wait_timeout_ms; cu_q / cu_k are host sequence tables and
+    cu_q_dev / cu_k_dev the device addresses of their copies."""
+    vp, keep = _varlen_c(p, cu_q, cu_k, cu_q_dev, cu_k_dev)
     return load_library().attn_core_fwd_varlen(ctypes.byref(vp), q, k, v, o, lse, stream or None)
 
 
-def attn_core_bwd_varlen_workspace_bytes(p: Params, cu_q, cu_k) -> int:
-    vp, keep = _varlen_c(p, cu_q, cu_k)
+def attn_core_bwd_varlen_workspace_bytes(p: Params, cu_q, cu_k, *, cu_q_dev: int = 0, cu_k_dev: int = 0) -> int:
+    vp, keep = _varlen_c(p, cu_q, cu_k, cu_q_dev, cu_k_dev)
     return int(load_library().attn_core_bwd_varlen_workspace_bytes(ctypes.byref(vp)))
 
 
 def attn_core_bwd_varlen(p: Params, cu_q, cu_k, q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int,
-                         dk: int, dv: int, workspace: int, workspace_bytes: int, stream: int) -> int:
-    vp, keep = _varlen_c(p, cu_q, cu_k)
+                         dk: int, dv: int, workspace: int, workspace_bytes: int, stream: int, *,
+                         cu_q_dev: int = 0, cu_k_dev: int = 0) -> int:
+    vp, keep = _varlen_c(p, cu_q, cu_k, cu_q_dev, cu_k_dev)
     return load_library().attn_core_bwd_varlen(ctypes.byref(vp), q, k, v, o, lse, dout, dq, dk, dv, workspace,
                                                workspace_bytes, stream or None)
+
+
+def _device_tables(cq, ck, device):
+    """Device copies of the host sequence tables (kept alive by the caller until
+    the kernels that read them are queued: the caching allocator reuses the
+    memory only in stream order)."""
+    import torch
+    tq = torch.tensor(cq, dtype=torch.int32, device=device)
+    tk = torch.tensor(ck, dtype=torch.int32, device=device) if ck is not None else None
+    return tq, tk, tq.data_ptr(), (tk.data_ptr() if tk is not None else 0)
 
 
 def attn_core_gelu_fwd(n: int, x: int, y: int, stream: int) -> int:
@@ -448,8 +464,9 @@ def _varlen_params(q, k, causal, p_drop, seed, offset, scale, **kw) -> Params:
 def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k=None, *, causal: bool = True, p_drop: float = 0.0,
                seed: int = 0, offset: int = 0, scale: float = 0.0, **kw):
     """Forward over a packed batch: q [total_q, h_q, d], k/v [total_k, h_kv, d];
-    cu_seqlens_* host sequence tables (lists or CPU tensors).  Returns (O, LSE
-    [h_q, total_q])."""
+    cu_seqlens_* host sequence tables (lists or CPU tensors; their device
+    copies are made here).  The batch is one launch per kernel.  Returns (O,
+    LSE [h_q, total_q])."""
     import torch
     p = _varlen_params(q, k, causal, p_drop, seed, offset, scale, **kw)
     cq = [int(x) for x in cu_seqlens_q]
@@ -459,8 +476,9 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k=None, *, causal: bool = True,
     _check(v, "v", torch.bfloat16, ((ck or cq)[-1], p.h_kv, p.d))
     o = torch.empty_like(q)
     lse = torch.empty((p.h_q, cq[-1]), dtype=torch.float32, device=q.device)
+    tq, tk, dq_ptr, dk_ptr = _device_tables(cq, ck, q.device)
     rc = attn_core_fwd_varlen(p, cq, ck, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                              lse.data_ptr(), _stream())
+                              lse.data_ptr(), _stream(), cu_q_dev=dq_ptr, cu_k_dev=dk_ptr)
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_fwd_varlen")
     return o, lse
@@ -477,11 +495,12 @@ def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k=None, *, causal
     _check(dout, "dout", torch.bfloat16, tuple(q.shape))
     _check(lse, "lse", torch.float32, (p.h_q, cq[-1]))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = attn_core_bwd_varlen_workspace_bytes(p, cq, ck)
+    tq, tk, dq_ptr, dk_ptr = _device_tables(cq, ck, q.device)
+    ws_bytes = attn_core_bwd_varlen_workspace_bytes(p, cq, ck, cu_q_dev=dq_ptr, cu_k_dev=dk_ptr)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
     rc = attn_core_bwd_varlen(p, cq, ck, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                               lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                              ws.data_ptr(), ws.numel(), _stream())
+                              ws.data_ptr(), ws.numel(), _stream(), cu_q_dev=dq_ptr, cu_k_dev=dk_ptr)
     if rc != OK:
         raise AttnCoreError(rc, "attn_core_bwd_varlen")
     return dq, dk, dv

@@ -166,6 +166,11 @@ struct Geometry {
     int64_t q_row, q_head, kv_row, kv_head; // strides in elements
     int64_t lse_stride;                     // LSE elements from one query head to the next
     uint32_t bh0;                           // Philox head-index offset
+    int64_t q_rows, k_rows;                 // rows per map head: s and s_kv, or a packed
+                                            // batch's total query and key counts
+    int64_t ws_stride;                      // backward workspace rows per query head
+    const int32_t* cu_q;                    // a packed batch's device sequence tables,
+    const int32_t* cu_k;                    // or null
 };
 
 Geometry padded_geometry(const attn_core_params* p, int sk)
@@ -178,6 +183,10 @@ Geometry padded_geometry(const attn_core_params* p, int sk)
     g.kv_head = (int64_t)sk * p->d;
     g.lse_stride = p->s;
     g.bh0 = 0;
+    g.q_rows = p->s;
+    g.k_rows = sk;
+    g.ws_stride = ((int64_t)p->s + kBlockRows - 1) / kBlockRows * kBlockRows;
+    g.cu_q = g.cu_k = nullptr;
     return g;
 }
 
@@ -258,16 +267,20 @@ int fwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
 {
     int rc;
     const int sk = keys_of(p);
+    (void)sk;
     CUtensorMap tq, tk, tv, to;
-    if ((rc = encode_map_strided(&tq, q, p->d, p->s, g.q_heads, g.q_row, g.q_head, 128)) ||
-        (rc = encode_map_strided(&tk, k, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, 128)) ||
-        (rc = encode_map_strided(&tv, v, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, 128)) ||
-        (rc = encode_map_strided(&to, o, p->d, p->s, g.q_heads, g.q_row, g.q_head, 128)))
+    if ((rc = encode_map_strided(&tq, q, p->d, (int)g.q_rows, g.q_heads, g.q_row, g.q_head, 128)) ||
+        (rc = encode_map_strided(&tk, k, p->d, (int)g.k_rows, g.kv_heads, g.kv_row, g.kv_head, 128)) ||
+        (rc = encode_map_strided(&tv, v, p->d, (int)g.k_rows, g.kv_heads, g.kv_row, g.kv_head, 128)) ||
+        (rc = encode_map_strided(&to, o, p->d, (int)g.q_rows, g.q_heads, g.q_row, g.q_head, 128)))
         return rc;
     ac::FwdArgs a{};
     a.c = common_args(p);
     a.c.bh0 = g.bh0;
     a.c.lse_stride = g.lse_stride;
+    a.c.cu_q = g.cu_q;
+    a.c.cu_k = g.cu_k;
+    a.c.ws_stride = g.ws_stride;
     a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     a.o_head_stride = g.q_head;
@@ -321,10 +334,10 @@ int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
     const int bn = ac::dq_key_tile(p->d);
     const int sk = keys_of(p);
     auto qmap = [&](CUtensorMap* m, const void* ptr, int rows) {
-        return encode_map_strided(m, ptr, p->d, p->s, g.q_heads, g.q_row, g.q_head, rows);
+        return encode_map_strided(m, ptr, p->d, (int)g.q_rows, g.q_heads, g.q_row, g.q_head, rows);
     };
     auto kmap = [&](CUtensorMap* m, const void* ptr, int rows) {
-        return encode_map_strided(m, ptr, p->d, sk, g.kv_heads, g.kv_row, g.kv_head, rows);
+        return encode_map_strided(m, ptr, p->d, (int)g.k_rows, g.kv_heads, g.kv_row, g.kv_head, rows);
     };
     CUtensorMap tq128, tdo128, to128, tdq128, tqb, tdob, tk, tv, tkb, tvb, tdk, tdv;
     if ((rc = qmap(&tq128, q, 128)) || (rc = qmap(&tdo128, dout, 128)) || (rc = qmap(&to128, o, 128)) ||
@@ -337,15 +350,26 @@ int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
     a.c = common_args(p);
     a.c.bh0 = g.bh0;
     a.c.lse_stride = g.lse_stride;
+    a.c.cu_q = g.cu_q;
+    a.c.cu_k = g.cu_k;
+    a.c.ws_stride = g.ws_stride;
     a.s_pad = a.c.n_blk * kBlockRows;
+    const size_t ws_rows = (size_t)g.q_heads * (size_t)g.ws_stride;
     a.o = static_cast<const uint16_t*>(o);
     a.dout = static_cast<const uint16_t*>(dout);
     a.lse = lse;
     a.lse2_ws = static_cast<float*>(workspace);
-    a.delta_ws = static_cast<float*>(workspace) + padded_rows(p);
-    a.mask_ws = (share_mask && mask_bytes(p) != 0)
-                    ? reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) + 2 * padded_rows(p))
+    a.delta_ws = static_cast<float*>(workspace) + ws_rows;
+    a.mask_ws = (share_mask && g.cu_q == nullptr && mask_bytes(p) != 0)
+                    ? reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) + 2 * ws_rows)
                     : nullptr;
+    a.dq = static_cast<uint16_t*>(dq);
+    a.dk = static_cast<uint16_t*>(dk);
+    a.dv = static_cast<uint16_t*>(dv);
+    a.q_head_stride = g.q_head;
+    a.q_row_stride = g.q_row;
+    a.kv_head_stride = g.kv_head;
+    a.kv_row_stride = g.kv_row;
     a.d = p->d;
     if ((rc = device_sms(&a.num_sms))) return rc;
     const bool drop = a.c.thr != 0;
@@ -357,7 +381,7 @@ int bwd_launch(const attn_core_params* p, const Geometry& g, const void* q, cons
     // block on are seen by no query (top-left alignment) and the dK/dV kernel
     // skips their blocks, so their gradients are set to zero here.
     const int64_t kz = (int64_t)a.c.n_blk * kBlockRows;
-    if (p->causal && sk > kz) {
+    if (g.cu_q == nullptr && p->causal && sk > kz) {
         const size_t row_bytes = (size_t)g.kv_row * sizeof(uint16_t);
         for (void* t : {dk, dv}) {
             uint8_t* base = static_cast<uint8_t*>(t) + (size_t)kz * row_bytes;
@@ -408,47 +432,61 @@ int attn_core_bwd_recompute(const attn_core_params* p, const void* q, const void
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// Variable-length (packed) batches: one launch per sequence, each over that
-// sequence's rows of the packed tensors.
+// Variable-length (packed) batches: one launch per kernel over the whole batch.
+// The kernels take the n_seq sequences as a batch of n_seq elements of the
+// longest sequence's length and read each tile's own lengths and first rows
+// from the device copies of the sequence tables.
 namespace {
 
-// Checks the sequence table and fills the per-sequence parameters' shared part.
-int check_varlen(const attn_core_varlen_params* vp, int64_t* total_q, int64_t* total_k)
+struct VarlenShape {
+    int64_t total_q, total_k;
+    int32_t max_q, max_k;
+    const int32_t* cu_q_dev;
+    const int32_t* cu_k_dev;
+};
+
+// Checks the host sequence tables and the device copies' presence.
+int check_varlen(const attn_core_varlen_params* vp, VarlenShape* out)
 {
     if (vp == nullptr || vp->n_seq <= 0 || vp->cu_seqlens_q == nullptr) return ATTN_CORE_ERR_INVALID_ARG;
+    if (vp->cu_seqlens_q_dev == nullptr || (vp->cu_seqlens_k != nullptr && vp->cu_seqlens_k_dev == nullptr))
+        return ATTN_CORE_ERR_INVALID_ARG;
     if (vp->base.timing_events != nullptr) return ATTN_CORE_ERR_INVALID_ARG;
     if ((int64_t)vp->n_seq * vp->base.h_q >= (int64_t)INT32_MAX) return ATTN_CORE_ERR_INVALID_ARG;
     const int32_t* cq = vp->cu_seqlens_q;
     const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
     if (cq[0] != 0 || ck[0] != 0) return ATTN_CORE_ERR_INVALID_ARG;
+    int32_t max_q = 0, max_k = 0;
     for (int i = 0; i < vp->n_seq; ++i) {
         const int32_t lq = cq[i + 1] - cq[i], lk = ck[i + 1] - ck[i];
         if (lq < 0 || lk < 0 || (lq > 0 && lk == 0)) return ATTN_CORE_ERR_INVALID_ARG;
-        if (lq == 0) continue;
-        attn_core_params ps = vp->base;
-        ps.b = 1;
-        ps.s = lq;
-        ps.s_kv = lk;
-        if (int rc = check_params(&ps)) return rc;
+        if (lq > max_q) max_q = lq;
+        if (lk > max_k) max_k = lk;
     }
-    *total_q = cq[vp->n_seq];
-    *total_k = ck[vp->n_seq];
+    out->total_q = cq[vp->n_seq];
+    out->total_k = ck[vp->n_seq];
+    if (out->total_q >= (int64_t)INT32_MAX - 132 * (int64_t)vp->n_seq - 4 || out->total_k >= (int64_t)INT32_MAX)
+        return ATTN_CORE_ERR_INVALID_ARG;
+    out->max_q = max_q;
+    out->max_k = max_k;
+    out->cu_q_dev = vp->cu_seqlens_q_dev;
+    out->cu_k_dev = vp->cu_seqlens_k ? vp->cu_seqlens_k_dev : vp->cu_seqlens_q_dev;
     return ATTN_CORE_OK;
 }
 
-// Sequence i as a one-batch launch: its parameters and geometry.
-attn_core_params seq_params(const attn_core_varlen_params* vp, int i)
+// The batch as one launch: n_seq elements of the longest sequence's length.
+attn_core_params batch_params(const attn_core_varlen_params* vp, const VarlenShape& vs)
 {
-    const int32_t* cq = vp->cu_seqlens_q;
-    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
     attn_core_params ps = vp->base;
-    ps.b = 1;
-    ps.s = cq[i + 1] - cq[i];
-    ps.s_kv = ck[i + 1] - ck[i];
+    ps.b = vp->n_seq;
+    ps.s = vs.max_q;
+    ps.s_kv = vs.max_k;
     return ps;
 }
 
-Geometry seq_geometry(const attn_core_varlen_params* vp, int i, int64_t total_q)
+// Packed [tokens, heads, d] tensors: one map head per attention head, rows of
+// the whole batch.
+Geometry packed_geometry(const attn_core_varlen_params* vp, const VarlenShape& vs)
 {
     Geometry g;
     g.q_heads = vp->base.h_q;
@@ -456,9 +494,21 @@ Geometry seq_geometry(const attn_core_varlen_params* vp, int i, int64_t total_q)
     g.q_row = (int64_t)vp->base.h_q * vp->base.d;
     g.kv_row = (int64_t)vp->base.h_kv * vp->base.d;
     g.q_head = g.kv_head = vp->base.d;
-    g.lse_stride = total_q;
-    g.bh0 = (uint32_t)i * (uint32_t)vp->base.h_q;
+    g.lse_stride = vs.total_q;
+    g.bh0 = 0;
+    g.q_rows = vs.total_q;
+    g.k_rows = vs.total_k;
+    g.ws_stride = ((vs.total_q + 3) & ~(int64_t)3) + 132 * (int64_t)vp->n_seq;   // see packed_ws_row0
+    g.cu_q = vs.cu_q_dev;
+    g.cu_k = vs.cu_k_dev;
     return g;
+}
+
+size_t varlen_ws_bytes(const attn_core_varlen_params* vp, const VarlenShape& vs)
+{
+    const size_t rows = (size_t)((vs.total_q + 3) & ~(int64_t)3) + 132 * (size_t)vp->n_seq;
+    const size_t b = 2 * sizeof(float) * (size_t)vp->base.h_q * rows;
+    return (b + 255) & ~(size_t)255;
 }
 
 }  // namespace
@@ -467,84 +517,55 @@ extern "C" {
 
 size_t attn_core_bwd_varlen_workspace_bytes(const attn_core_varlen_params* vp)
 {
-    int64_t tq = 0, tk = 0;
-    if (check_varlen(vp, &tq, &tk)) return 0;
-    size_t total = 0;
-    for (int i = 0; i < vp->n_seq; ++i) {
-        const attn_core_params ps = seq_params(vp, i);
-        if (ps.s > 0) total += launch_ws_bytes(&ps, true);
-    }
-    return total;
+    VarlenShape vs;
+    if (check_varlen(vp, &vs)) return 0;
+    return varlen_ws_bytes(vp, vs);
 }
 
 int attn_core_fwd_varlen(const attn_core_varlen_params* vp, const void* q, const void* k, const void* v, void* o,
                          float* lse, void* stream)
 {
-    int64_t tq = 0, tk = 0;
-    int rc = check_varlen(vp, &tq, &tk);
+    VarlenShape vs;
+    int rc = check_varlen(vp, &vs);
     if (rc) return rc;
     if (!q || !k || !v || !o || !lse) return ATTN_CORE_ERR_INVALID_ARG;
     if (!supported_d(vp->base.d)) return ATTN_CORE_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_CORE_ERR_MISALIGNED;
+    if (vs.max_q == 0) return ATTN_CORE_OK;          // no queries: nothing to compute
+    const attn_core_params ps = batch_params(vp, vs);
+    if ((rc = check_params(&ps))) return rc;
     if ((rc = check_device())) return rc;
     if ((rc = get_encoder())) return rc;
-    const int d = vp->base.d, hq = vp->base.h_q, hkv = vp->base.h_kv;
-    const int32_t* cq = vp->cu_seqlens_q;
-    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
-    for (int i = 0; i < vp->n_seq; ++i) {
-        const attn_core_params ps = seq_params(vp, i);
-        if (ps.s == 0) continue;
-        const size_t qo = (size_t)cq[i] * hq * d, ko = (size_t)ck[i] * hkv * d;
-        rc = fwd_launch(&ps, seq_geometry(vp, i, tq), static_cast<const uint16_t*>(q) + qo,
-                        static_cast<const uint16_t*>(k) + ko, static_cast<const uint16_t*>(v) + ko,
-                        static_cast<uint16_t*>(o) + qo, lse + cq[i], reinterpret_cast<cudaStream_t>(stream));
-        if (rc) return rc;
-    }
-    return ATTN_CORE_OK;
+    return fwd_launch(&ps, packed_geometry(vp, vs), q, k, v, o, lse, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_core_bwd_varlen(const attn_core_varlen_params* vp, const void* q, const void* k, const void* v,
                          const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                          void* workspace, size_t workspace_bytes, void* stream)
 {
-    int64_t tq = 0, tk = 0;
-    int rc = check_varlen(vp, &tq, &tk);
+    VarlenShape vs;
+    int rc = check_varlen(vp, &vs);
     if (rc) return rc;
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return ATTN_CORE_ERR_INVALID_ARG;
     if (!supported_d(vp->base.d)) return ATTN_CORE_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return ATTN_CORE_ERR_MISALIGNED;
-    if (workspace_bytes < attn_core_bwd_varlen_workspace_bytes(vp)) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < varlen_ws_bytes(vp, vs)) return ATTN_CORE_ERR_WORKSPACE_TOO_SMALL;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (vs.max_q == 0) {
+        // no query sees any key: every key's gradients are zero
+        const size_t nb = (size_t)vs.total_k * vp->base.h_kv * vp->base.d * sizeof(uint16_t);
+        if (nb && (cudaMemsetAsync(dk, 0, nb, st) != cudaSuccess || cudaMemsetAsync(dv, 0, nb, st) != cudaSuccess))
+            return ATTN_CORE_ERR_CUDA;
+        return ATTN_CORE_OK;
+    }
+    const attn_core_params ps = batch_params(vp, vs);
+    if ((rc = check_params(&ps))) return rc;
     if ((rc = check_device())) return rc;
     if ((rc = get_encoder())) return rc;
-    const int d = vp->base.d, hq = vp->base.h_q, hkv = vp->base.h_kv;
-    const int32_t* cq = vp->cu_seqlens_q;
-    const int32_t* ck = vp->cu_seqlens_k ? vp->cu_seqlens_k : cq;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    for (int i = 0; i < vp->n_seq; ++i) {
-        const attn_core_params ps = seq_params(vp, i);
-        const size_t qo = (size_t)cq[i] * hq * d, ko = (size_t)ck[i] * hkv * d;
-        if (ps.s == 0) {
-            // No query sees these keys: their gradients are zero.
-            const size_t nb = (size_t)ps.s_kv * hkv * d * sizeof(uint16_t);
-            if (nb && (cudaMemsetAsync(static_cast<uint16_t*>(dk) + ko, 0, nb, reinterpret_cast<cudaStream_t>(stream)) !=
-                           cudaSuccess ||
-                       cudaMemsetAsync(static_cast<uint16_t*>(dv) + ko, 0, nb, reinterpret_cast<cudaStream_t>(stream)) !=
-                           cudaSuccess))
-                return ATTN_CORE_ERR_CUDA;
-            continue;
-        }
-        rc = bwd_launch(&ps, seq_geometry(vp, i, tq), static_cast<const uint16_t*>(q) + qo,
-                        static_cast<const uint16_t*>(k) + ko, static_cast<const uint16_t*>(v) + ko,
-                        static_cast<const uint16_t*>(o) + qo, lse + cq[i], static_cast<const uint16_t*>(dout) + qo,
-                        static_cast<uint16_t*>(dq) + qo, static_cast<uint16_t*>(dk) + ko,
-                        static_cast<uint16_t*>(dv) + ko, ws, true, reinterpret_cast<cudaStream_t>(stream));
-        if (rc) return rc;
-        ws += launch_ws_bytes(&ps, true);
-    }
-    return ATTN_CORE_OK;
+    return bwd_launch(&ps, packed_geometry(vp, vs), q, k, v, o, lse, dout, dq, dk, dv, workspace, false, st);
 }
 
 }  // extern "C"

@@ -110,13 +110,32 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     const int n_bkv = a.n_bh / a.h_q * a.h_kv;
     const int kb = (int)(blockIdx.x / n_bkv);          // small key blocks carry the most work
-    const int bkv = (int)(blockIdx.x % n_bkv);
+    const int bkv = (int)(blockIdx.x % n_bkv);         // flattened KV head: sequence * h_kv + head
     const int group = a.h_q / a.h_kv;
-    const int bh0 = (bkv / a.h_kv) * a.h_q + (bkv % a.h_kv) * group;
-    const int n_qt = args.s_pad / BQ;
+    const int seq = bkv / a.h_kv, kvh = bkv % a.h_kv;
+    const int bh0 = seq * a.h_q + kvh * group;         // the group's first flattened query head
+    // The sequence's query and key counts and first rows (a packed batch), or the
+    // padded layout's; a packed batch's key blocks past its sequence's end have no work.
+    const bool packed = a.cu_q != nullptr;
+    const int q_first = packed ? a.cu_q[seq] : 0, k_first = packed ? a.cu_k[seq] : 0;
+    const int lq = packed ? a.cu_q[seq + 1] - q_first : a.s;
+    const int lk = packed ? a.cu_k[seq + 1] - k_first : a.s_k;
+    if (kb * 128 >= lk) return;
+    const bool tail = packed && (kb + 1) * 128 > lk;   // rows past the end are not stored
+    const int n_qt = ((lq + 127) / 128) * 128 / BQ;
     const int qt0 = a.causal ? (kb * 128) / BQ : 0;
-    const int per_head = n_qt - qt0;
+    // under a top-left causal mask a key block past the last query is seen by none:
+    // zero gradients
+    const int per_head = n_qt > qt0 ? n_qt - qt0 : 0;
     const int n_it = group * per_head;
+    const int yk = k_first + kb * 128, zk = packed ? kvh : bkv;   // TMA coordinates of the key block
+    // TMA row / head coordinates and workspace row of query tile qt of head `hq` of the group
+    auto q_coords = [&](int hq, int qt, int& yq, int& zq, size_t& srow) {
+        yq = q_first + qt * BQ;
+        zq = packed ? kvh * group + hq : bh0 + hq;
+        srow = packed ? (size_t)(kvh * group + hq) * a.ws_stride + packed_ws_row0(q_first, seq) + qt * BQ
+                      : (size_t)(bh0 + hq) * a.ws_stride + qt * BQ;
+    };
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
@@ -158,23 +177,24 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             // ---- TMA producer: K and V once, then (Q, dO, LSE2, D) per query tile
             mbar_arrive_expect_tx(bar(bars->kv_full), 2 * C::KV_TILE);
             for (int ch = 0; ch < G::NCH; ++ch) {
-                tma_load_3d(sb + C::OFF_K + ch * C::KV_CHUNK, &tm_k, ch * G::CW, kb * 128, bkv, bar(bars->kv_full));
-                tma_load_3d(sb + C::OFF_V + ch * C::KV_CHUNK, &tm_v, ch * G::CW, kb * 128, bkv, bar(bars->kv_full));
+                tma_load_3d(sb + C::OFF_K + ch * C::KV_CHUNK, &tm_k, ch * G::CW, yk, zk, bar(bars->kv_full));
+                tma_load_3d(sb + C::OFF_V + ch * C::KV_CHUNK, &tm_v, ch * G::CW, yk, zk, bar(bars->kv_full));
             }
             for (int it = 0; it < n_it; ++it) {
                 const int st = it % ST;
                 const int bh = bh0 + it / per_head;
                 const int qt = qt0 + it % per_head;
+                int yq, zq;
+                size_t srow;
+                q_coords(it / per_head, qt, yq, zq, srow);
                 if (!wait_bounded(wc, bar(bars->q_empty[st]), ((it / ST) & 1) ^ 1, timeout_code(kSiteQEmpty)))
                     break;
                 const uint32_t fb = bar(bars->q_full[st]);
                 mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 2 * BQ * 4 + (MWS ? C::MSK_BYTES : 0u));
                 for (int ch = 0; ch < G::NCH; ++ch) {
-                    tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, qt * BQ, bh, fb);
-                    tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, qt * BQ, bh,
-                                fb);
+                    tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, yq, zq, fb);
+                    tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, yq, zq, fb);
                 }
-                const size_t srow = (size_t)bh * args.s_pad + (size_t)qt * BQ;
                 bulk_load_1d(sb + C::OFF_LSE + st * BQ * 4, args.lse2_ws + srow, BQ * 4, fb);
                 bulk_load_1d(sb + C::OFF_DEL + st * BQ * 4, args.delta_ws + srow, BQ * 4, fb);
                 if constexpr (MWS) {
@@ -206,8 +226,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 mma_commit(bar(bars->dp_full));
             };
             bool ok = wait_warp(wc, bar(bars->kv_full), 0, timeout_code(kSiteKvFull));
-            if (ok) ok = wait_warp(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull));
-            if (ok) {
+            if (ok && n_it > 0) ok = wait_warp(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull));
+            if (ok && n_it > 0) {
                 tc_fence_after();
                 issue_s(0);
                 issue_dp(0);
@@ -388,23 +408,51 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (DROP && !MWS && it + 1 < n_it) draw_mask(it + 1);
         }
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
+        // dV and dK of this key row: staged for one TMA store of the block, or (a
+        // packed batch's tail block, whose tensor map runs on into the next
+        // sequence) stored row by row; zero when no query sees the block
+        auto put_row = [&](uint16_t* base, uint32_t stage_off, int c32, uint32_t (&rr)[32], float mul) {
+            if (!tail) {
+                stage_row32<D, 128>(sb + stage_off, r, c32 * 32, rr, mul);
+            } else if (kb * 128 + r < lk) {
+                uint4* row = reinterpret_cast<uint4*>(base + (size_t)zk * args.kv_head_stride +
+                                                      (size_t)(yk + r) * args.kv_row_stride) + c32 * 4;
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wv[e] = pack_bf16x2(__uint_as_float(rr[8 * u4 + 2 * e]) * mul,
+                                            __uint_as_float(rr[8 * u4 + 2 * e + 1]) * mul);
+                    row[u4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            }
+        };
         if (ok) {
             tc_fence_after();
 #pragma unroll 1
             for (int c32 = h; c32 < D / 32; c32 += 2) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
-                stage_row32<D, 128>(sb + C::OFF_V, r, c32 * 32, rr, DROP ? a.keep_scale : 1.0f);
+                if (n_it == 0) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+                put_row(args.dv, C::OFF_V, c32, rr, DROP ? a.keep_scale : 1.0f);
                 tmem_ld32(tmem + C::T_DK + lane_off + c32 * 32, rr);
-                stage_row32<D, 128>(sb + C::OFF_K, r, c32 * 32, rr, a.scale);
+                if (n_it == 0) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+                put_row(args.dk, C::OFF_K, c32, rr, a.scale);
             }
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, kRowThreads);
-        if (h == 0 && r == 0 && !bars->abort_flag) {
+        if (!tail && h == 0 && r == 0 && !bars->abort_flag) {
             for (int ch = 0; ch < G::NCH; ++ch) {
-                tma_store_3d(&tm_dv, sb + C::OFF_V + ch * C::KV_CHUNK, ch * G::CW, kb * 128, bkv);
-                tma_store_3d(&tm_dk, sb + C::OFF_K + ch * C::KV_CHUNK, ch * G::CW, kb * 128, bkv);
+                tma_store_3d(&tm_dv, sb + C::OFF_V + ch * C::KV_CHUNK, ch * G::CW, yk, zk);
+                tma_store_3d(&tm_dk, sb + C::OFF_K + ch * C::KV_CHUNK, ch * G::CW, yk, zk);
             }
             bulk_commit();
             bulk_wait_read0();
@@ -500,24 +548,6 @@ struct DqBars {
 };
 static_assert(sizeof(DqBars) <= DqCfg<64>::BAR_BYTES, "barrier block");
 
-// Work tile t (longest first): query block, flattened query head, KV head and
-// key blocks.
-struct DqTile {
-    int qb, bh, bkv, nk;
-};
-template <int BN>
-__device__ __forceinline__ DqTile dq_tile(const CommonArgs& a, int t)
-{
-    DqTile w;
-    w.qb = a.n_blk - 1 - t / a.n_bh;
-    w.bh = t % a.n_bh;
-    const int group = a.h_q / a.h_kv;
-    w.bkv = (w.bh / a.h_q) * a.h_kv + (w.bh % a.h_q) / group;
-    const int n_kblk = (a.s_k + BN - 1) / BN;
-    w.nk = a.causal ? min((w.qb + 1) * (128 / BN), n_kblk) : n_kblk;
-    return w;
-}
-
 }  // namespace
 
 template <int D, bool DROP, bool MWS>
@@ -602,17 +632,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // ---- TMA producer: the K ring over all blocks of all tiles
             int g = 0;
             bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const DqTile w = dq_tile<BN>(a, t);
+            int vt = 0;
+            QTile w;
+            while (ok && next_qtile(sched, a, BN, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % KST;
                     ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / KST) & 1) ^ 1, timeout_code(kSiteKEmpty));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->k_full[st]), C::KT);
                     for (int ch = 0; ch < G::NCH; ++ch)
-                        tma_load_3d(sb + C::OFF_K + st * C::KT + ch * C::KCH, &tm_k, ch * G::CW, j * BN, w.bkv,
+                        tma_load_3d(sb + C::OFF_K + st * C::KT + ch * C::KCH, &tm_k, ch * G::CW, w.yk + j * BN, w.zk,
                                     bar(bars->k_full[st]));
                 }
             }
@@ -623,42 +652,44 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // buffer) goes out by TMA, and once that store has read the buffer this
             // tile's O comes in.  The next tile's Q, dO and O are pulled into L2
             // meanwhile, so their loads at the tile boundary are short.
-            DqTile prev{};
+            // (A packed batch's tail tile stores its dQ rows itself: its tensor map
+            // runs on into the next sequence.)
+            QTile prev{}, w{}, wn{};
+            int vt = 0;
+            bool have = next_qtile(sched, a, BN, vt, w);
             for (int u = 0;; ++u) {
-                const int t = sched.tile(u);
-                DqTile w{};
-                if (t >= 0) {
-                    w = dq_tile<BN>(a, t);
+                if (have) {
                     if (!wait_bounded(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
                     mbar_arrive_expect_tx(bar(bars->q_full), 2 * C::QT);
                     for (int ch = 0; ch < G::NCH; ++ch) {
-                        tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, w.qb * 128, w.bh,
-                                    bar(bars->q_full));
-                        tma_load_3d(sb + C::OFF_DO + ch * C::QCH, &tm_do, ch * G::CW, w.qb * 128, w.bh,
-                                    bar(bars->q_full));
+                        tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, w.yq, w.zq, bar(bars->q_full));
+                        tma_load_3d(sb + C::OFF_DO + ch * C::QCH, &tm_do, ch * G::CW, w.yq, w.zq, bar(bars->q_full));
                     }
                 }
                 if (u > 0) {
                     if (!wait_bounded(wc, bar(bars->dq_staged), (u - 1) & 1, timeout_code(kSiteStage))) break;
-                    for (int ch = 0; ch < G::NCH; ++ch)
-                        tma_store_3d(&tm_dq, sb + C::OFF_O + ch * C::QCH, ch * G::CW, prev.qb * 128, prev.bh);
-                    bulk_commit();
-                    bulk_wait_read0();
+                    if (!prev.tail) {
+                        for (int ch = 0; ch < G::NCH; ++ch)
+                            tma_store_3d(&tm_dq, sb + C::OFF_O + ch * C::QCH, ch * G::CW, prev.yq, prev.zq);
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
                 }
-                if (t < 0) break;
+                if (!have) break;
                 mbar_arrive_expect_tx(bar(bars->o_full), C::QT);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_O + ch * C::QCH, &tm_o, ch * G::CW, w.qb * 128, w.bh, bar(bars->o_full));
-                const int tn = sched.tile(u + 1);
-                if (tn >= 0) {
-                    const DqTile wn = dq_tile<BN>(a, tn);
+                    tma_load_3d(sb + C::OFF_O + ch * C::QCH, &tm_o, ch * G::CW, w.yq, w.zq, bar(bars->o_full));
+                const bool have_next = next_qtile(sched, a, BN, vt, wn);
+                if (have_next) {
                     for (int ch = 0; ch < G::NCH; ++ch) {
-                        tma_prefetch_3d(&tm_q, ch * G::CW, wn.qb * 128, wn.bh);
-                        tma_prefetch_3d(&tm_do, ch * G::CW, wn.qb * 128, wn.bh);
-                        tma_prefetch_3d(&tm_o, ch * G::CW, wn.qb * 128, wn.bh);
+                        tma_prefetch_3d(&tm_q, ch * G::CW, wn.yq, wn.zq);
+                        tma_prefetch_3d(&tm_do, ch * G::CW, wn.yq, wn.zq);
+                        tma_prefetch_3d(&tm_o, ch * G::CW, wn.yq, wn.zq);
                     }
                 }
                 prev = w;
+                w = wn;
+                have = have_next;
             }
         }
     } else if (alive && warp == 2) {
@@ -667,17 +698,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // ---- TMA producer: the V ring over all blocks of all tiles
             int g = 0;
             bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const DqTile w = dq_tile<BN>(a, t);
+            int vt = 0;
+            QTile w;
+            while (ok && next_qtile(sched, a, BN, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % VST;
                     ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / VST) & 1) ^ 1, timeout_code(kSiteVEmpty));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->v_full[st]), C::KT);
                     for (int ch = 0; ch < G::NCH; ++ch)
-                        tma_load_3d(sb + C::OFF_V + st * C::KT + ch * C::KCH, &tm_v, ch * G::CW, j * BN, w.bkv,
+                        tma_load_3d(sb + C::OFF_V + st * C::KT + ch * C::KCH, &tm_v, ch * G::CW, w.yk + j * BN, w.zk,
                                     bar(bars->v_full[st]));
                 }
             }
@@ -718,10 +748,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             };
             int g = 0;
             bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const DqTile w = dq_tile<BN>(a, t);
+            int vt = 0;
+            QTile w;
+            for (int u = 0; ok && next_qtile(sched, a, BN, vt, w); ++u) {
                 const int g0 = g;
                 ok = wait_warp(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
                 if (ok) ok = issue_s(g0);
@@ -775,10 +804,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const KeepSwar8 ks(a.thr);
         int g = 0;
         bool ok = true;
-        for (int u = 0; ok; ++u) {
-            const int t = sched.tile(u);
-            if (t < 0) break;
-            const DqTile w = dq_tile<BN>(a, t);
+        int vt = 0;
+        QTile w;
+        while (ok && next_qtile(sched, a, BN, vt, w)) {
             const uint32_t i = (uint32_t)(w.qb * 128 + r);
             const uint32_t bhc = (uint32_t)w.bh + a.bh0;
             for (int j = 0; j < w.nk; ++j, ++g) {
@@ -818,27 +846,26 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         float* dred = reinterpret_cast<float*>(smem_raw + pad + C::OFF_RED);   // [2 halves][128]
         const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
         const uint64_t zs2 = f2_pack(a.keep_scale, a.keep_scale);
-        // -LSE * log2(e) of this thread's query in a tile (-inf past s, so its
-        // probabilities recompute to 0); the next tile's value is loaded a whole
-        // tile ahead of its use.
-        auto row_nl2 = [&](int t) -> float {
-            if (t < 0) return 0.f;
-            const DqTile w = dq_tile<BN>(a, t);
-            const int i = w.qb * 128 + r;
-            return i < a.s ? -args.lse[(size_t)w.bh * a.lse_stride + i] * 1.44269504088896340736f : -INFINITY;
+        // -LSE * log2(e) of this thread's query in a tile (-inf past the sequence's
+        // end, so its probabilities recompute to 0); the next tile's value is
+        // loaded a whole tile ahead of its use.
+        auto row_nl2 = [&](const QTile& x) -> float {
+            return x.qb * 128 + r < x.lq ? -args.lse[(size_t)x.zq * a.lse_stride + x.yq + r] * 1.44269504088896340736f
+                                         : -INFINITY;
         };
-        float nl2_next = row_nl2(sched.tile(0));
+        int vt = 0;
+        QTile w, wn;
+        bool have = next_qtile(sched, a, BN, vt, w);
+        float nl2_next = have ? row_nl2(w) : 0.f;
         int g = 0, nx = 0;
         bool ok = true;
-        for (int u = 0; ok; ++u) {
-            const int t = sched.tile(u);
-            if (t < 0) break;
-            const DqTile w = dq_tile<BN>(a, t);
-            const int qb = w.qb, bh = w.bh, nk = w.nk;
-            const int i = qb * 128 + r;
-            const size_t srow = (size_t)bh * args.s_pad + (size_t)i;
+        for (int u = 0; ok && have; ++u) {
+            const int qb = w.qb, nk = w.nk;
+            const int i = qb * 128 + r;              // query of the sequence
+            const size_t srow = (size_t)w.ws0 + r;
             const float nl2 = nl2_next;
-            nl2_next = row_nl2(sched.tile(u + 1));
+            const bool have_next = next_qtile(sched, a, BN, vt, wn);
+            nl2_next = have_next ? row_nl2(wn) : 0.f;
             if (h == 0) args.lse2_ws[srow] = nl2;
             const uint64_t nl22 = f2_pack(nl2, nl2);
             // The first estimate D~ = rowsum(dO * O) comes from the staged bf16 O
@@ -870,8 +897,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 // Scores of keys this query does not see (past the diagonal, or past the
                 // last key) become -inf before the exponential; only the blocks that
                 // hold such keys run this (a uniform branch), the others go straight on.
-                const int k_end = a.causal ? min(i + 1, a.s_k) : a.s_k;    // first key not seen
-                if (key0 + HK > (a.causal ? min(qb * 128, a.s_k) : a.s_k)) {
+                const int k_end = a.causal ? min(i + 1, w.lk) : w.lk;    // first key not seen
+                if (key0 + HK > (a.causal ? min(qb * 128, w.lk) : w.lk)) {
 #pragma unroll
                     for (int e = 0; e < HK / 2; ++e) {
                         float lo, hi;
@@ -1003,13 +1030,30 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
                     rq[c] = __float_as_uint(fmaf(-eps, __uint_as_float(rp[c]), __uint_as_float(rq[c])));
-                stage_row32<D, 128>(sb + C::OFF_O, r, c32 * 32, rq, a.scale);
+                if (!w.tail) {
+                    stage_row32<D, 128>(sb + C::OFF_O, r, c32 * 32, rq, a.scale);
+                } else if (i < w.lq) {
+                    // a packed batch's tail tile: this row straight to global memory
+                    uint4* qrow = reinterpret_cast<uint4*>(args.dq + (size_t)w.zq * args.q_head_stride +
+                                                           (size_t)(w.yq + r) * args.q_row_stride) + c32 * 4;
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16x2(__uint_as_float(rq[8 * u4 + 2 * e]) * a.scale,
+                                                __uint_as_float(rq[8 * u4 + 2 * e + 1]) * a.scale);
+                        qrow[u4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
             }
             tc_fence_before();
             mbar_arrive(bar(bars->acc_free));   // the next tile's P K and dQ may overwrite them
             fence_proxy_async_smem();
             mbar_arrive(bar(bars->dq_staged));
             if (h == 0) args.delta_ws[srow] = -d_exact;    // the dK/dV kernel adds it
+            w = wn;
+            have = have_next;
         }
     } else if (alive) {
         regs_lower<kDqOtherRegs>();   // idle warps (and the RNG warps without dropout)
@@ -1038,8 +1082,10 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return (int)e;
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
     // under a causal mask the key blocks past the last query block are seen by
-    // no query (the caller zeroes their gradients)
-    const unsigned n_kb = (unsigned)(a.c.causal && a.c.n_blk < a.c.n_blk_k ? a.c.n_blk : a.c.n_blk_k);
+    // no query (the caller zeroes their gradients); a packed batch's sequences
+    // differ, so there every key block runs and such blocks store zeros
+    const unsigned n_kb =
+        (unsigned)(a.c.causal && a.c.n_blk < a.c.n_blk_k && a.c.cu_q == nullptr ? a.c.n_blk : a.c.n_blk_k);
     const unsigned grid = n_kb * n_bkv;
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return (int)cudaGetLastError();

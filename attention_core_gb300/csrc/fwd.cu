@@ -88,21 +88,6 @@ enum : int32_t {
 };
 __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site << 8); }
 
-// Work tile t (longest first): query block and flattened query head.
-struct FwdTile {
-    int qb, bh, bkv, nk;
-};
-__device__ __forceinline__ FwdTile fwd_tile(const CommonArgs& a, int t)
-{
-    FwdTile w;
-    w.qb = a.n_blk - 1 - t / a.n_bh;
-    w.bh = t % a.n_bh;
-    const int group = a.h_q / a.h_kv;
-    w.bkv = (w.bh / a.h_q) * a.h_kv + (w.bh % a.h_q) / group;
-    w.nk = a.causal ? min(w.qb + 1, a.n_blk_k) : a.n_blk_k;   // top-left causal: keys 0 .. i
-    return w;
-}
-
 }  // namespace
 
 template <int D, bool DROP>
@@ -177,32 +162,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ---- TMA producer: the K ring over all blocks of all tiles
             int g = 0;
             bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const FwdTile w = fwd_tile(a, t);
+            int vt = 0;
+            QTile w;
+            while (ok && next_qtile(sched, a, 128, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteKEmpty));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->k_full[st]), C::TILE);
                     for (int ch = 0; ch < G::NCH; ++ch)
-                        tma_load_3d(sb + C::OFF_K + st * C::TILE + ch * C::CHUNK, &tm_k, ch * G::CW, j * 128, w.bkv,
-                                    bar(bars->k_full[st]));
+                        tma_load_3d(sb + C::OFF_K + st * C::TILE + ch * C::CHUNK, &tm_k, ch * G::CW, w.yk + j * 128,
+                                    w.zk, bar(bars->k_full[st]));
                 }
             }
         } else if (lane == 1) {
             // ---- TMA producer: each tile's Q as soon as its buffer is free
-            for (int u = 0;; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const FwdTile w = fwd_tile(a, t);
+            int vt = 0;
+            QTile w;
+            for (int u = 0; next_qtile(sched, a, 128, vt, w); ++u) {
                 const int qs = u % C::NQ;
                 if (!wait_bounded(wc, bar(bars->q_empty[qs]), ((u / C::NQ) & 1) ^ 1, timeout_code(kSiteQEmpty)))
                     break;
                 mbar_arrive_expect_tx(bar(bars->q_full[qs]), C::TILE);
                 for (int ch = 0; ch < G::NCH; ++ch)
-                    tma_load_3d(sb + C::OFF_Q + qs * C::TILE + ch * C::CHUNK, &tm_q, ch * G::CW, w.qb * 128, w.bh,
+                    tma_load_3d(sb + C::OFF_Q + qs * C::TILE + ch * C::CHUNK, &tm_q, ch * G::CW, w.yq, w.zq,
                                 bar(bars->q_full[qs]));
             }
         }
@@ -211,18 +194,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ---- TMA producer: the V ring
             int g = 0;
             bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const FwdTile w = fwd_tile(a, t);
+            int vt = 0;
+            QTile w;
+            while (ok && next_qtile(sched, a, 128, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteVEmpty));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->v_full[st]), C::TILE);
                     for (int ch = 0; ch < G::NCH; ++ch)
-                        tma_load_3d(sb + C::OFF_V + st * C::TILE + ch * C::CHUNK, &tm_v, ch * G::CW, j * 128, w.bkv,
-                                    bar(bars->v_full[st]));
+                        tma_load_3d(sb + C::OFF_V + st * C::TILE + ch * C::CHUNK, &tm_v, ch * G::CW, w.yk + j * 128,
+                                    w.zk, bar(bars->v_full[st]));
                 }
             }
         }
@@ -260,10 +242,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             Blk prev{-1, 0, 0, 0};
             int g = 0;
             bool ok = true;
-            for (int u = 0; ok; ++u) {
-                const int t = sched.tile(u);
-                if (t < 0) break;
-                const FwdTile w = fwd_tile(a, t);
+            int vt = 0;
+            QTile w;
+            for (int u = 0; ok && next_qtile(sched, a, 128, vt, w); ++u) {
                 // At a tile boundary the previous tile's last P.V goes first unless this
                 // tile's Q and first K block are already resident: it must never wait on
                 // this tile's loads.
@@ -308,12 +289,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int pv_done = 0;            // P.V products completed into O by earlier tiles
         int g0 = 0;
         bool ok = true;
-        for (int u = 0; ok; ++u) {
-            const int t = sched.tile(u);
-            if (t < 0) break;
-            const FwdTile w = fwd_tile(a, t);
+        int vt = 0;
+        QTile w;
+        for (int u = 0; ok && next_qtile(sched, a, 128, vt, w); ++u) {
             const int qb = w.qb, bh = w.bh, nk = w.nk;
-            const int i = qb * 128 + r;
+            const int i = qb * 128 + r;          // query of the sequence
+            const bool live = i < w.lq;          // rows past the end are computed, not stored
             const uint32_t tO = tmem + C::T_O + lane_off;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nk; ++j) {
@@ -336,10 +317,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int c = 0; c < 64; ++c)
                         if (64 * h + c > r) x[c] = -INFINITY;
                 }
-                if (key0 + 64 > a.s_k) {
+                if (key0 + 64 > w.lk) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (key0 + c >= a.s_k) x[c] = -INFINITY;
+                        if (key0 + c >= w.lk) x[c] = -INFINITY;
                 }
                 float mx = fmax3(x[0], x[1], x[2]);
 #pragma unroll
@@ -443,36 +424,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok) break;
             tc_fence_after();
             const float inv = a.keep_scale / l_tot;
-            if constexpr (C::STAGE_O) {
-                // O / l -> bf16 into the stage, then one TMA store of the tile (rows past s
-                // are clipped by the tensor map).  The stage is reused only after the
-                // previous tile's store has read it.
-                if (h == 0 && r == 0) bulk_wait_read0();
-                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_free), u & 1, timeout_code(kSiteStage)));
-                if (!ok) break;
-#pragma unroll 1
-                for (int c32 = h; c32 < D / 32; c32 += 2) {
-                    uint32_t rr[32];
-                    tmem_ld32(tO + c32 * 32, rr);
-                    stage_row32<D, 128>(sb + C::OFF_OST, r, c32 * 32, rr, inv);
-                }
-                if (i < a.s && h == 0)
-                    args.lse[(size_t)bh * a.lse_stride + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
-                fence_proxy_async_smem();
-                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_full), u & 1, timeout_code(kSiteStage)));
-                if (!ok) break;
-                if (h == 0 && r == 0 && !bars->abort_flag) {
-                    for (int ch = 0; ch < G::NCH; ++ch)
-                        tma_store_3d(&tm_o, sb + C::OFF_OST + ch * C::CHUNK, ch * G::CW, qb * 128, bh);
-                    bulk_commit();
-                }
-            } else {
-                // O row i straight to global memory: 16-byte stores of this half's
-                // 32-column chunks.  The TMEM loads are warp-collective, so every
-                // lane takes them; only the stores are guarded (rows past s).
-                const bool live = i < a.s;
-                uint4* orow = reinterpret_cast<uint4*>(args.o + (size_t)bh * args.o_head_stride +
-                                                       (size_t)(live ? i : 0) * args.o_row_stride);
+            const float lse_i = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+            // O row i straight to global memory: 16-byte stores of this half's
+            // 32-column chunks.  The TMEM loads are warp-collective, so every lane
+            // takes them; only the stores are guarded (rows past the sequence's end).
+            auto store_rows = [&]() {
+                uint4* orow = reinterpret_cast<uint4*>(args.o + (size_t)w.zq * args.o_head_stride +
+                                                       (size_t)(live ? w.yq + r : 0) * args.o_row_stride);
 #pragma unroll 1
                 for (int c32 = h; c32 < D / 32; c32 += 2) {
                     uint32_t rr[32];
@@ -487,8 +445,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (live) orow[c32 * 4 + u4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                     }
                 }
-                if (live && h == 0)
-                    args.lse[(size_t)bh * a.lse_stride + i] = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+            };
+            if (live && h == 0) args.lse[(size_t)w.zq * a.lse_stride + w.yq + r] = lse_i;
+            if constexpr (C::STAGE_O) {
+                // O / l -> bf16 into the stage, then one TMA store of the tile (rows past
+                // s are clipped by the tensor map).  The stage is reused only after the
+                // previous tile's store has read it.  A packed batch's tail tile stores
+                // its rows one by one instead: its tensor map runs on into the next
+                // sequence.  Both take the stage barriers, which count tiles.
+                if (h == 0 && r == 0) bulk_wait_read0();
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_free), u & 1, timeout_code(kSiteStage)));
+                if (!ok) break;
+                if (!w.tail) {
+#pragma unroll 1
+                    for (int c32 = h; c32 < D / 32; c32 += 2) {
+                        uint32_t rr[32];
+                        tmem_ld32(tO + c32 * 32, rr);
+                        stage_row32<D, 128>(sb + C::OFF_OST, r, c32 * 32, rr, inv);
+                    }
+                } else {
+                    store_rows();
+                }
+                fence_proxy_async_smem();
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->ost_full), u & 1, timeout_code(kSiteStage)));
+                if (!ok) break;
+                if (!w.tail && h == 0 && r == 0 && !bars->abort_flag) {
+                    for (int ch = 0; ch < G::NCH; ++ch)
+                        tma_store_3d(&tm_o, sb + C::OFF_OST + ch * C::CHUNK, ch * G::CW, w.yq, w.zq);
+                    bulk_commit();
+                }
+            } else {
+                store_rows();
             }
             tc_fence_before();
             mbar_arrive(bar(bars->o_free));

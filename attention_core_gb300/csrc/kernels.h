@@ -54,13 +54,89 @@ struct CommonArgs {
                           // sequence of a packed batch draws as batch element bh0 / h_q)
     int64_t lse_stride;   // LSE elements from one query head to the next (s, or the
                           // packed batch's total query count)
+    // Packed (variable-length) batch in one launch: device copies of the
+    // sequence tables (n_seq + 1 entries each), or null for the padded layout.
+    // Then the batch is n_seq sequences of at most n_blk query blocks and
+    // n_blk_k key blocks, n_bh = n_seq * h_q, and every tile takes its own
+    // lengths from the tables.
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int64_t ws_stride;    // backward workspace rows from one query head to the next:
+                          // n_blk * 128 for the padded layout; for a packed batch
+                          // the total query count rounded up to 4, plus 132 per
+                          // sequence (packed_ws_row0)
 };
+
+// First workspace row of sequence `seq` of a packed batch whose queries start
+// at row q_first: each sequence's rows padded to whole 128-row blocks, every
+// region starting on a multiple of 4 rows (16 bytes, for the bulk copies of
+// the dK/dV kernel); the 132-row gap per sequence covers the rounding, so
+// regions never overlap.
+__host__ __device__ inline int64_t packed_ws_row0(int q_first, int seq)
+{
+    return (int64_t)((q_first + 3) & ~3) + 132 * (int64_t)seq;
+}
+
+// Where one work tile of the query-major kernels (the forward and dQ) lives:
+// the query block of one head of one sequence (or batch element), for both
+// layouts.  Tile t: query block n_blk - 1 - t / n_bh (longest first), and
+// flattened head bh = t % n_bh = sequence * h_q + head.
+struct QTile {
+    int qb;          // query block within its sequence
+    int bh;          // flattened query head (Philox counter word 2, minus bh0)
+    int bkv;         // flattened KV head
+    int nk;          // key blocks of width BN to visit
+    int yq, zq;      // TMA row / head coordinates of the tile's first query row
+    int yk, zk;      // TMA row / head coordinates of the sequence's first key row
+    int lq, lk;      // queries and keys of the sequence
+    int64_t ws0;     // workspace row of the tile's first query row
+    bool empty;      // a packed batch's tile past its sequence's end: no work
+    bool tail;       // a packed batch's tile that holds rows past its sequence's
+                     // end (they are not stored: the next sequence follows)
+};
+__host__ __device__ inline QTile q_tile(const CommonArgs& a, int t, int bn)
+{
+    QTile w;
+    w.qb = a.n_blk - 1 - t / a.n_bh;
+    w.bh = t % a.n_bh;
+    const int group = a.h_q / a.h_kv;
+    const int seq = w.bh / a.h_q, head = w.bh % a.h_q;
+    w.bkv = seq * a.h_kv + head / group;
+    if (a.cu_q == nullptr) {
+        w.lq = a.s;
+        w.lk = a.s_k;
+        w.yq = w.qb * 128;
+        w.zq = w.bh;
+        w.yk = 0;
+        w.zk = w.bkv;
+        w.ws0 = (int64_t)w.bh * a.ws_stride + w.qb * 128;
+        w.empty = false;
+        w.tail = false;
+    } else {
+        const int q0 = a.cu_q[seq], k0 = a.cu_k[seq];
+        w.lq = a.cu_q[seq + 1] - q0;
+        w.lk = a.cu_k[seq + 1] - k0;
+        w.yq = q0 + w.qb * 128;
+        w.zq = head;
+        w.yk = k0;
+        w.zk = head / group;
+        w.ws0 = (int64_t)head * a.ws_stride + packed_ws_row0(q0, seq) + w.qb * 128;
+        w.empty = w.qb * 128 >= w.lq;
+        w.tail = (w.qb + 1) * 128 > w.lq;
+    }
+    const int n_kblk = (w.lk + bn - 1) / bn;
+    const int nk_causal = (w.qb + 1) * (128 / bn);
+    w.nk = w.empty ? 0 : (a.causal ? (nk_causal < n_kblk ? nk_causal : n_kblk) : n_kblk);
+    return w;
+}
 
 struct FwdArgs {
     CommonArgs c;
-    uint16_t* o;          // bf16 [b*h_q*s*d], or one sequence of a packed [tokens, h_q, d]
-    float* lse;           // query head bh, row i at lse[bh * c.lse_stride + i]
-    int64_t o_head_stride, o_row_stride;   // elements, for O stored row by row (d = 160)
+    uint16_t* o;          // bf16 [b*h_q*s*d], or a packed [tokens, h_q, d]
+    float* lse;           // tile row r at lse[zq * c.lse_stride + yq + r] (QTile)
+    int64_t o_head_stride, o_row_stride;   // elements, for O stored row by row (d = 160,
+                                           // and a packed batch's tail tiles): tile row r
+                                           // at o + zq * head + (yq + r) * row
     int32_t num_sms;      // persistent grid size
 };
 
@@ -77,6 +153,12 @@ struct BwdArgs {
                           // dK/dV kernel (layout: mask_pair_word); null: dK/dV draws its own
     int32_t d;
     int32_t num_sms;      // persistent grid size
+    // For rows stored one by one (a packed batch's tail tiles): the gradients
+    // and their strides in elements, as FwdArgs::o.
+    uint16_t* dq;
+    uint16_t* dk;
+    uint16_t* dv;
+    int64_t q_head_stride, q_row_stride, kv_head_stride, kv_row_stride;
 };
 
 // Keep bits handed from the dQ kernel to the dK/dV kernel.  For every

@@ -8,6 +8,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace ac {
 
 struct TileSched {
@@ -21,5 +23,22 @@ struct TileSched {
         return t < n_tiles ? (int)t : -1;
     }
 };
+
+// The next tile with work of this CTA's list for the query-major kernels,
+// scanning from position v (advanced past it): false when none is left.  A
+// packed batch's list holds tiles past the end of short sequences, which every
+// role of the kernel skips the same way.
+__device__ __forceinline__ bool next_qtile(const TileSched& sched, const CommonArgs& a, int bn, int& v, QTile& w)
+{
+    for (;; ++v) {
+        const int t = sched.tile(v);
+        if (t < 0) return false;
+        w = q_tile(a, t, bn);
+        if (!w.empty) {
+            ++v;
+            return true;
+        }
+    }
+}
 
 }  // namespace ac

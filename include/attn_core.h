@@ -187,27 +187,39 @@ int attn_core_bwd_recompute_noalloc(const attn_core_params* p, const void* q, co
  *   LSE          : fp32 [h_q, total_q]
  * Each sequence attends only within itself, as batch element i of the
  * padded layout would: the same causal rule (top-left aligned when a
- * sequence's query and key counts differ), and the same dropout mask (Philox counter word 2
- * = i * h_q + head).  The sequence tables are HOST arrays of n_seq + 1 int32
- * starting at 0 and nondecreasing; an empty sequence is skipped, one with
- * queries but no keys is invalid; one with keys but no queries gets zero
- * dK and dV rows.  `base` supplies h_q, h_kv, d, causal,
+ * sequence's query and key counts differ), and the same dropout mask
+ * (Philox counter word 2 = i * h_q + head).  The sequence tables are arrays
+ * of n_seq + 1 int32 starting at 0 and nondecreasing, given twice: in host
+ * memory (cu_seqlens_q / _k: checked, and used to size the launch) and as a
+ * device copy with the same values (cu_seqlens_q_dev / _k_dev, read by the
+ * kernels; _k_dev may be NULL only when cu_seqlens_k is).  An empty sequence
+ * is skipped, one with queries but no keys is invalid; one with keys but no
+ * queries gets zero dK and dV rows.  `base` supplies h_q, h_kv, d, causal,
  * p_drop, scale, seed, offset, dev_status, flags and wait_timeout_ms; its b,
- * s and s_kv are ignored and its timing_events must be NULL.  The kernels
- * run one sequence after another on `stream` (the same kernels as the
- * padded entry points, each over one sequence's rows). */
+ * s and s_kv are ignored and its timing_events must be NULL.  The whole
+ * batch is one launch per kernel (the same kernels as the padded entry
+ * points): they take the batch as n_seq elements of the longest sequence's
+ * length, skip the work past each sequence's end, and store the rows of a
+ * sequence's last, partial block one by one so that nothing lands in the next
+ * sequence.  Both tables must stay unchanged until the calls' kernels have
+ * run. */
 typedef struct {
     attn_core_params base;
     int32_t n_seq;
-    const int32_t* cu_seqlens_q;   /* host, n_seq + 1 */
-    const int32_t* cu_seqlens_k;   /* host, n_seq + 1, or NULL: as cu_seqlens_q */
+    const int32_t* cu_seqlens_q;       /* host, n_seq + 1 */
+    const int32_t* cu_seqlens_k;       /* host, n_seq + 1, or NULL: as cu_seqlens_q */
+    const int32_t* cu_seqlens_q_dev;   /* device copy of cu_seqlens_q */
+    const int32_t* cu_seqlens_k_dev;   /* device copy of cu_seqlens_k, or NULL with it */
 } attn_core_varlen_params;
 
 int attn_core_fwd_varlen(const attn_core_varlen_params* p, const void* q, const void* k, const void* v, void* o,
                          float* lse, void* stream);
 
-/* Workspace of attn_core_bwd_varlen: each sequence's share of
- * attn_core_bwd_workspace_bytes, rounded up to 256 bytes. */
+/* Workspace of attn_core_bwd_varlen, 0 if p is invalid: the two fp32 row
+ * statistics of every query row, each sequence's rows padded to whole
+ * 128-row blocks and aligned to 16 bytes:
+ * 8 * h_q * (round_up(total_q, 4) + 132 * n_seq) bytes, rounded up to 256.
+ * (The dropout mask is drawn twice in a packed batch; there are no keep bits.) */
 size_t attn_core_bwd_varlen_workspace_bytes(const attn_core_varlen_params* p);
 
 int attn_core_bwd_varlen(const attn_core_varlen_params* p, const void* q, const void* k, const void* v,

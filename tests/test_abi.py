@@ -209,18 +209,31 @@ def test_dal_workspace_and_validation(lib):
 ])
 def test_varlen_rejects_bad_tables(lib, cu_q, cu_k, causal):
     p = _p(causal=causal)
-    assert ac.attn_core_fwd_varlen(p, cu_q, cu_k, *([FAKE] * 5), 0) == ac.ERR_INVALID_ARG
-    assert ac.attn_core_bwd_varlen_workspace_bytes(p, cu_q, cu_k) == 0
+    dev = dict(cu_q_dev=FAKE, cu_k_dev=FAKE if cu_k is not None else 0)
+    assert ac.attn_core_fwd_varlen(p, cu_q, cu_k, *([FAKE] * 5), 0, **dev) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_bwd_varlen_workspace_bytes(p, cu_q, cu_k, **dev) == 0
 
 
-def test_varlen_workspace_is_the_sum_of_the_sequences(lib):
-    p = _p(p_drop=0.1)
+def test_varlen_needs_the_device_tables(lib):
+    """The kernels read the sequence tables' device copies: a call without them
+    (or with a key table but no device copy of it) is rejected before anything runs."""
+    p = _p()
+    assert ac.attn_core_fwd_varlen(p, [0, 5, 9], None, *([FAKE] * 5), 0) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_fwd_varlen(p, [0, 5, 9], [0, 5, 9], *([FAKE] * 5), 0, cu_q_dev=FAKE) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_bwd_varlen_workspace_bytes(p, [0, 5, 9], None) == 0
+
+
+def test_varlen_workspace_formula_of_the_header(lib):
+    """8 h_q (round_up(total_q, 4) + 132 n_seq) bytes of row statistics, rounded
+    up to 256: every sequence's rows padded to whole 128-row blocks and aligned
+    to 16 bytes, no keep bits."""
+    p = _p(p_drop=0.1, h_q=4, h_kv=2)
     cu = [0, 200, 200, 300]            # lengths 200, 0 (skipped), 100
-    per = [ac.attn_core_bwd_workspace_bytes(_p(s=n, p_drop=0.1)) for n in (200, 100)]
-    assert ac.attn_core_bwd_varlen_workspace_bytes(p, cu, None) == sum((x + 255) // 256 * 256 for x in per)
+    want = 8 * 4 * (300 + 132 * 3)
+    assert ac.attn_core_bwd_varlen_workspace_bytes(p, cu, None, cu_q_dev=FAKE) == (want + 255) // 256 * 256
     pt = _p(p_drop=0.1)
     pt.timing_events = FAKE           # per-kernel events are not offered for packed batches
-    assert ac.attn_core_fwd_varlen(pt, cu, None, *([FAKE] * 5), 0) == ac.ERR_INVALID_ARG
+    assert ac.attn_core_fwd_varlen(pt, cu, None, *([FAKE] * 5), 0, cu_q_dev=FAKE) == ac.ERR_INVALID_ARG
 
 
 def test_bwd_workspace_formula_of_the_header(lib):

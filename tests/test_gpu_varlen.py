@@ -48,6 +48,7 @@ CASES = [
     ([100, 300], [257, 40], 2, 1, 128, False, 0.2),
     ([90, 150], None, 2, 2, 160, True, 0.1),
     ([100, 300, 5], [257, 40, 5], 2, 1, 128, True, 0.1),    # causal, top-left per sequence
+    ([1, 600, 0, 129, 128, 77, 1000, 3], None, 2, 2, 96, True, 0.1),   # many lengths, one launch
 ]
 
 
@@ -136,11 +137,13 @@ def test_sequence_without_queries_gets_zero_key_gradients():
     dq = torch.empty_like(qd)
     dk = torch.full_like(kd, 1.0)
     dv = torch.full_like(vd, -2.0)
-    ws_bytes = ac.attn_core_bwd_varlen_workspace_bytes(pr_c, cq, ck)
+    tq, tk, pq, pk = ac._device_tables(cq, ck, dev)
+    ws_bytes = ac.attn_core_bwd_varlen_workspace_bytes(pr_c, cq, ck, cu_q_dev=pq, cu_k_dev=pk)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     rc = ac.attn_core_bwd_varlen(pr_c, cq, ck, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
                                  lse.data_ptr(), dod.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                 ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+                                 ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream,
+                                 cu_q_dev=pq, cu_k_dev=pk)
     assert rc == ac.OK, ac.attn_core_strerror(rc)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dk[:50]).item() == 0
