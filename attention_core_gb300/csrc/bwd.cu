@@ -87,7 +87,7 @@ struct DkdvBars {
 
 }  // namespace
 
-template <int D, bool DROP, bool MWS>
+template <int D, bool DROP, bool MWS, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -116,7 +116,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int bh0 = seq * a.h_q + kvh * group;         // the group's first flattened query head
     // The sequence's query and key counts and first rows (a packed batch), or the
     // padded layout's; a packed batch's key blocks past its sequence's end have no work.
-    const bool packed = a.cu_q != nullptr;
+    constexpr bool packed = PACKED;
     const int q_first = packed ? a.cu_q[seq] : 0, k_first = packed ? a.cu_k[seq] : 0;
     const int lq = packed ? a.cu_q[seq + 1] - q_first : a.s;
     const int lk = packed ? a.cu_k[seq + 1] - k_first : a.s_k;
@@ -550,7 +550,7 @@ static_assert(sizeof(DqBars) <= DqCfg<64>::BAR_BYTES, "barrier block");
 
 }  // namespace
 
-template <int D, bool DROP, bool MWS>
+template <int D, bool DROP, bool MWS, bool PACKED>
 __global__ void __launch_bounds__(kThreadsRng, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -634,7 +634,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             bool ok = true;
             int vt = 0;
             QTile w;
-            while (ok && next_qtile(sched, a, BN, vt, w)) {
+            while (ok && next_qtile<PACKED>(sched, a, BN, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % KST;
                     ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / KST) & 1) ^ 1, timeout_code(kSiteKEmpty));
@@ -656,7 +656,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // runs on into the next sequence.)
             QTile prev{}, w{}, wn{};
             int vt = 0;
-            bool have = next_qtile(sched, a, BN, vt, w);
+            bool have = next_qtile<PACKED>(sched, a, BN, vt, w);
             for (int u = 0;; ++u) {
                 if (have) {
                     if (!wait_bounded(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
@@ -679,7 +679,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 mbar_arrive_expect_tx(bar(bars->o_full), C::QT);
                 for (int ch = 0; ch < G::NCH; ++ch)
                     tma_load_3d(sb + C::OFF_O + ch * C::QCH, &tm_o, ch * G::CW, w.yq, w.zq, bar(bars->o_full));
-                const bool have_next = next_qtile(sched, a, BN, vt, wn);
+                const bool have_next = next_qtile<PACKED>(sched, a, BN, vt, wn);
                 if (have_next) {
                     for (int ch = 0; ch < G::NCH; ++ch) {
                         tma_prefetch_3d(&tm_q, ch * G::CW, wn.yq, wn.zq);
@@ -700,7 +700,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             bool ok = true;
             int vt = 0;
             QTile w;
-            while (ok && next_qtile(sched, a, BN, vt, w)) {
+            while (ok && next_qtile<PACKED>(sched, a, BN, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % VST;
                     ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / VST) & 1) ^ 1, timeout_code(kSiteVEmpty));
@@ -750,7 +750,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             bool ok = true;
             int vt = 0;
             QTile w;
-            for (int u = 0; ok && next_qtile(sched, a, BN, vt, w); ++u) {
+            for (int u = 0; ok && next_qtile<PACKED>(sched, a, BN, vt, w); ++u) {
                 const int g0 = g;
                 ok = wait_warp(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
                 if (ok) ok = issue_s(g0);
@@ -806,7 +806,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         bool ok = true;
         int vt = 0;
         QTile w;
-        while (ok && next_qtile(sched, a, BN, vt, w)) {
+        while (ok && next_qtile<PACKED>(sched, a, BN, vt, w)) {
             const uint32_t i = (uint32_t)(w.qb * 128 + r);
             const uint32_t bhc = (uint32_t)w.bh + a.bh0;
             for (int j = 0; j < w.nk; ++j, ++g) {
@@ -855,7 +855,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         };
         int vt = 0;
         QTile w, wn;
-        bool have = next_qtile(sched, a, BN, vt, w);
+        bool have = next_qtile<PACKED>(sched, a, BN, vt, w);
         float nl2_next = have ? row_nl2(w) : 0.f;
         int g = 0, nx = 0;
         bool ok = true;
@@ -864,7 +864,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int i = qb * 128 + r;              // query of the sequence
             const size_t srow = (size_t)w.ws0 + r;
             const float nl2 = nl2_next;
-            const bool have_next = next_qtile(sched, a, BN, vt, wn);
+            const bool have_next = next_qtile<PACKED>(sched, a, BN, vt, wn);
             nl2_next = have_next ? row_nl2(wn) : 0.f;
             if (h == 0) args.lse2_ws[srow] = nl2;
             const uint64_t nl22 = f2_pack(nl2, nl2);
@@ -1071,13 +1071,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 // ========================================================== launchers ====
 
-template <int D, bool DROP, bool MWS>
+template <int D, bool DROP, bool MWS, bool PACKED>
 static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
                          cudaStream_t stream)
 {
     constexpr uint32_t smem = DkdvCfg<D>::SMEM;
-    auto kern = attn_bwd_dkdv_kernel<D, DROP, MWS>;
+    auto kern = attn_bwd_dkdv_kernel<D, DROP, MWS, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
@@ -1091,12 +1091,12 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     return (int)cudaGetLastError();
 }
 
-template <int D, bool DROP, bool MWS>
+template <int D, bool DROP, bool MWS, bool PACKED>
 static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& to, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t stream)
 {
     constexpr uint32_t smem = DqCfg<D>::SMEM;
-    auto kern = attn_bwd_dq_kernel<D, DROP, MWS>;
+    auto kern = attn_bwd_dq_kernel<D, DROP, MWS, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     // the row warps' register raise waits until the others' shares are free:
@@ -1117,9 +1117,11 @@ int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMa
 {
 #define AC_DKDV_CASE(DD)                                                                            \
     case DD:                                                                                        \
-        return !dropout     ? launch_dkdv_t<DD, false, false>(tq, tk, tv, tdo, tdk, tdv, a, stream)   \
-               : a.mask_ws ? launch_dkdv_t<DD, true, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)    \
-                           : launch_dkdv_t<DD, true, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+        return a.c.cu_q ? (!dropout ? launch_dkdv_t<DD, false, false, true>(tq, tk, tv, tdo, tdk, tdv, a, stream) \
+                                    : launch_dkdv_t<DD, true, false, true>(tq, tk, tv, tdo, tdk, tdv, a, stream))  \
+               : !dropout  ? launch_dkdv_t<DD, false, false, false>(tq, tk, tv, tdo, tdk, tdv, a, stream)          \
+               : a.mask_ws ? launch_dkdv_t<DD, true, true, false>(tq, tk, tv, tdo, tdk, tdv, a, stream)            \
+                           : launch_dkdv_t<DD, true, false, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
     switch (d) {
         AC_DKDV_CASE(64)
         AC_DKDV_CASE(96)
@@ -1136,9 +1138,11 @@ int launch_bwd_dq(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap&
 {
 #define AC_DQ_CASE(DD)                                                                              \
     case DD:                                                                                        \
-        return !dropout     ? launch_dq_t<DD, false, false>(tq, tk, tv, tdo, to, tdq, a, stream)             \
-               : a.mask_ws ? launch_dq_t<DD, true, true>(tq, tk, tv, tdo, to, tdq, a, stream)              \
-                           : launch_dq_t<DD, true, false>(tq, tk, tv, tdo, to, tdq, a, stream);
+        return a.c.cu_q ? (!dropout ? launch_dq_t<DD, false, false, true>(tq, tk, tv, tdo, to, tdq, a, stream) \
+                                    : launch_dq_t<DD, true, false, true>(tq, tk, tv, tdo, to, tdq, a, stream))  \
+               : !dropout  ? launch_dq_t<DD, false, false, false>(tq, tk, tv, tdo, to, tdq, a, stream)          \
+               : a.mask_ws ? launch_dq_t<DD, true, true, false>(tq, tk, tv, tdo, to, tdq, a, stream)            \
+                           : launch_dq_t<DD, true, false, false>(tq, tk, tv, tdo, to, tdq, a, stream);
     switch (d) {
         AC_DQ_CASE(64)
         AC_DQ_CASE(96)

@@ -90,7 +90,7 @@ __device__ __forceinline__ int32_t timeout_code(int32_t site) { return 6 | (site
 
 }  // namespace
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -164,7 +164,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             int vt = 0;
             QTile w;
-            while (ok && next_qtile(sched, a, 128, vt, w)) {
+            while (ok && next_qtile<PACKED>(sched, a, 128, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteKEmpty));
@@ -179,7 +179,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ---- TMA producer: each tile's Q as soon as its buffer is free
             int vt = 0;
             QTile w;
-            for (int u = 0; next_qtile(sched, a, 128, vt, w); ++u) {
+            for (int u = 0; next_qtile<PACKED>(sched, a, 128, vt, w); ++u) {
                 const int qs = u % C::NQ;
                 if (!wait_bounded(wc, bar(bars->q_empty[qs]), ((u / C::NQ) & 1) ^ 1, timeout_code(kSiteQEmpty)))
                     break;
@@ -196,7 +196,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             int vt = 0;
             QTile w;
-            while (ok && next_qtile(sched, a, 128, vt, w)) {
+            while (ok && next_qtile<PACKED>(sched, a, 128, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteVEmpty));
@@ -244,7 +244,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             int vt = 0;
             QTile w;
-            for (int u = 0; ok && next_qtile(sched, a, 128, vt, w); ++u) {
+            for (int u = 0; ok && next_qtile<PACKED>(sched, a, 128, vt, w); ++u) {
                 // At a tile boundary the previous tile's last P.V goes first unless this
                 // tile's Q and first K block are already resident: it must never wait on
                 // this tile's loads.
@@ -291,7 +291,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool ok = true;
         int vt = 0;
         QTile w;
-        for (int u = 0; ok && next_qtile(sched, a, 128, vt, w); ++u) {
+        for (int u = 0; ok && next_qtile<PACKED>(sched, a, 128, vt, w); ++u) {
             const int qb = w.qb, bh = w.bh, nk = w.nk;
             const int i = qb * 128 + r;          // query of the sequence
             const bool live = i < w.lq;          // rows past the end are computed, not stored
@@ -499,12 +499,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool DROP>
+template <int D, bool DROP, bool PACKED>
 static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& to, const FwdArgs& a, cudaStream_t stream)
 {
     constexpr uint32_t smem = FwdCfg<D>::SMEM;
-    auto kern = attn_fwd_kernel<D, DROP>;
+    auto kern = attn_fwd_kernel<D, DROP, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
@@ -518,8 +518,10 @@ int launch_fwd(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk
 {
 #define AC_FWD_CASE(DD)                                                                             \
     case DD:                                                                                        \
-        return dropout ? launch_fwd_t<DD, true>(tq, tk, tv, to, a, stream)                          \
-                       : launch_fwd_t<DD, false>(tq, tk, tv, to, a, stream);
+        return a.c.cu_q ? (dropout ? launch_fwd_t<DD, true, true>(tq, tk, tv, to, a, stream)          \
+                                   : launch_fwd_t<DD, false, true>(tq, tk, tv, to, a, stream))        \
+                        : (dropout ? launch_fwd_t<DD, true, false>(tq, tk, tv, to, a, stream)         \
+                                   : launch_fwd_t<DD, false, false>(tq, tk, tv, to, a, stream));
     switch (d) {
         AC_FWD_CASE(64)
         AC_FWD_CASE(96)

@@ -80,7 +80,10 @@ __host__ __device__ inline int64_t packed_ws_row0(int q_first, int seq)
 // Where one work tile of the query-major kernels (the forward and dQ) lives:
 // the query block of one head of one sequence (or batch element), for both
 // layouts.  Tile t: query block n_blk - 1 - t / n_bh (longest first), and
-// flattened head bh = t % n_bh = sequence * h_q + head.
+// flattened head bh = t % n_bh = sequence * h_q + head.  The kernels are
+// compiled for one layout each (PACKED): in the padded one every field follows
+// from the launch parameters and `empty` and `tail` are constant false, so the
+// packed batch's bookkeeping costs the padded kernels nothing.
 struct QTile {
     int qb;          // query block within its sequence
     int bh;          // flattened query head (Philox counter word 2, minus bh0)
@@ -94,7 +97,8 @@ struct QTile {
     bool tail;       // a packed batch's tile that holds rows past its sequence's
                      // end (they are not stored: the next sequence follows)
 };
-__host__ __device__ inline QTile q_tile(const CommonArgs& a, int t, int bn)
+template <bool PACKED>
+__device__ __forceinline__ QTile q_tile(const CommonArgs& a, int t, int bn)
 {
     QTile w;
     w.qb = a.n_blk - 1 - t / a.n_bh;
@@ -102,7 +106,7 @@ __host__ __device__ inline QTile q_tile(const CommonArgs& a, int t, int bn)
     const int group = a.h_q / a.h_kv;
     const int seq = w.bh / a.h_q, head = w.bh % a.h_q;
     w.bkv = seq * a.h_kv + head / group;
-    if (a.cu_q == nullptr) {
+    if constexpr (!PACKED) {
         w.lq = a.s;
         w.lk = a.s_k;
         w.yq = w.qb * 128;

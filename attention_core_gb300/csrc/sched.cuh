@@ -28,12 +28,13 @@ struct TileSched {
 // scanning from position v (advanced past it): false when none is left.  A
 // packed batch's list holds tiles past the end of short sequences, which every
 // role of the kernel skips the same way.
+template <bool PACKED>
 __device__ __forceinline__ bool next_qtile(const TileSched& sched, const CommonArgs& a, int bn, int& v, QTile& w)
 {
     for (;; ++v) {
         const int t = sched.tile(v);
         if (t < 0) return false;
-        w = q_tile(a, t, bn);
+        w = q_tile<PACKED>(a, t, bn);
         if (!w.empty) {
             ++v;
             return true;

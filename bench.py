@@ -391,6 +391,11 @@ def run_ours(args, w):
     if not args.no_per_config and rank == 0:
         per_config = _per_config(dev, stream)
 
+    # a packed batch of mixed lengths, one launch per kernel
+    varlen = None
+    if not args.no_varlen and rank == 0:
+        varlen = _varlen_bench(dev, stream)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -428,6 +433,7 @@ def run_ours(args, w):
             "dropout_add_ln": dal,
             "layer_study": layer_study,
             "per_config": per_config,
+            "varlen": varlen,
             "bwd_workspace_bytes": ws_bytes,
             "gpu_launches": 3 * K,
             "kernel_ms_sampled": f"per-kernel events on every {EVERY}th timed step ({len(kt['fwd'])} samples)",
@@ -587,6 +593,83 @@ def _dal_measure(dev, stream, iters: int = 30):
             "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"], "bytes": nbytes,
             "traffic": _traffic("dal_" + name + "_kernel", "gpt175b_dal")}}
     return out
+
+
+VARLEN = {"n_seq": 64, "min_len": 64, "max_len": 4096, "h_q": 12, "h_kv": 12, "d": 128, "p_drop": 0.1,
+          "len_seed": 64}
+
+
+def _varlen_bench(dev, stream, steps: int = 20, warmup: int = 3):
+    """A packed batch of mixed lengths, one launch per kernel: 64 sequences of
+    lengths drawn uniformly from 64 .. 4096 (seeded), heads shaped as the 175B
+    shard (12 heads of 128, causal, p = 0.1).  Forward and backward are timed
+    with events around each call over `steps` steps; TFLOP/s are algorithmic
+    (fwd 4 d, bwd 10 d per visible pair, summed over the sequences)."""
+    import random
+
+    import torch
+
+    import attention_core_gb300 as ac
+    pk = _peaks()
+    c = VARLEN
+    rng = random.Random(c["len_seed"])
+    lens = [rng.randint(c["min_len"], c["max_len"]) for _ in range(c["n_seq"])]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    total, hq, hkv, d = cu[-1], c["h_q"], c["h_kv"], c["d"]
+    gen = torch.Generator(device="cpu").manual_seed(c["len_seed"])
+    q, g = (torch.randn((total, hq, d), generator=gen).to(torch.bfloat16).to(dev) for _ in range(2))
+    k, v = (torch.randn((total, hkv, d), generator=gen).to(torch.bfloat16).to(dev) for _ in range(2))
+    o, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((hq, total), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pr = ac.Params(b=1, h_q=hq, h_kv=hkv, s=1, d=d, causal=True, p_drop=c["p_drop"], seed=0x7A12,
+                   dev_status=status.data_ptr())
+    tq, _, cq_dev, _ = ac._device_tables(cu, None, dev)
+    ws_bytes = ac.attn_core_bwd_varlen_workspace_bytes(pr, cu, None, cu_q_dev=cq_dev)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    sh = stream.cuda_stream
+
+    def fwd():
+        rc = ac.attn_core_fwd_varlen(pr, cu, None, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), sh, cu_q_dev=cq_dev)
+        if rc:
+            raise ac.AttnCoreError(rc, "attn_core_fwd_varlen")
+
+    def bwd():
+        rc = ac.attn_core_bwd_varlen(pr, cu, None, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), g.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                     ws.data_ptr(), ws_bytes, sh, cu_q_dev=cq_dev)
+        if rc:
+            raise ac.AttnCoreError(rc, "attn_core_bwd_varlen")
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        evs[3 * i].record(stream)
+        fwd()
+        evs[3 * i + 1].record(stream)
+        bwd()
+        evs[3 * i + 2].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} in the packed batch")
+    fwd_ms = sum(evs[3 * i].elapsed_time(evs[3 * i + 1]) for i in range(steps)) / steps
+    bwd_ms = sum(evs[3 * i + 1].elapsed_time(evs[3 * i + 2]) for i in range(steps)) / steps
+    u = sum(n * (n + 1) // 2 for n in lens) * d * hq
+    tf = 14 * u / ((fwd_ms + bwd_ms) / 1e3) / 1e12
+    return {"n_seq": c["n_seq"], "lengths": f"uniform {c['min_len']}..{c['max_len']} (seed {c['len_seed']})",
+            "total_tokens": total, "max_len": max(lens), "h_q": hq, "h_kv": hkv, "d_head": d, "causal": True,
+            "p_drop": c["p_drop"], "ms_per_step": fwd_ms + bwd_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": 4 * u / (fwd_ms / 1e3) / 1e12, "bwd_tflops": 10 * u / (bwd_ms / 1e3) / 1e12,
+            "combined_tflops": tf, "pct_of_bf16_peak": 100.0 * tf / pk["bf16_tflops"],
+            "launches_per_step": 3, "bwd_workspace_bytes": ws_bytes, "steps": steps,
+            "l2": f"{(2 * total * (hq + hkv) * d * 2) / 2**20:.0f} MiB of inputs (> L2)"}
 
 
 def _layer_study(dev, stream, iters: int = 10):
@@ -790,6 +873,8 @@ def main():
                     help="skip the layer-level recompute-overhead measurement")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip timing the other workload configurations")
+    ap.add_argument("--no-varlen", action="store_true",
+                    help="skip the packed mixed-length batch")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the CPU-oracle baseline sample")
     args = ap.parse_args()
