@@ -16,10 +16,10 @@
  *     z = residual + dropout(x)                     (stored: next residual)
  *     y = gamma * (z - mean(z)) / sqrt(var(z) + eps) + beta   (next input)
  * per row (token) over the hidden dimension H, var the biased (1/H) variance.
- * Dropout uses the attention core's mask reading (Philox-4x32-10, 16-bit
- * draws, drop iff draw < round(p * 65536), kept values scaled by
- * 1 / (1 - p_eff)) with counter (col / 8, row, 0xFFFFFFFF, offset): word 2
- * is a value no attention head index takes.
+ * Dropout uses Philox-4x32-10 with 16-bit draws (eight per call; the
+ * attention core reads 8-bit ones), drop iff draw < round(p * 65536), kept
+ * values scaled by 1 / (1 - p_eff), with counter (col / 8, row, 0xFFFFFFFF,
+ * offset): word 2 is a value no attention head index takes.
  *
  * The backward takes dy (gradient of y) and, optionally, dz_next (the
  * gradient reaching z through the residual path) and returns
