@@ -77,13 +77,89 @@ struct DkdvCfg {
 };
 
 struct DkdvBars {
-    uint64_t kv_full;
+    uint64_t kv_full, kv_empty;        // a tile's K and V landed / free (its last S and dP done)
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full, dp_full, p_full, ds_full, acc_done;
-    uint64_t never;
+    uint64_t s_full, dp_full, p_full, ds_full;
+    uint64_t acc_done, acc_free;       // a tile's accumulators complete / read out
+    uint64_t out_staged;               // the tile's dK and dV staged (or stored row by row)
+    uint64_t out_read;                 // the store lane has finished a tile
+    uint64_t stage_free[2];            // the staged output in a query-ring slot has been read
+    uint64_t kv_stage_free;            // the staged output in the K/V buffers has been read
+    uint64_t drain, never;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
+static_assert(sizeof(DkdvBars) <= 256, "barrier block");
+
+// One work tile of the dK/dV kernel: a 128-key block of one KV head of one
+// sequence (or batch element).  Tile t: key block t / n_bkv (small key blocks
+// see the most queries under the causal mask: longest first) and flattened KV
+// head bkv = t % n_bkv = sequence * h_kv + head.
+struct KTile {
+    int kb, bkv, seq, kvh;
+    int bh0;              // the group's first flattened query head
+    int q_first, k_first; // the sequence's first query and key rows (packed batch), or 0
+    int lq, lk;           // its query and key counts
+    int qt0, per_head, n_it;   // first query tile, tiles per query head, iterations
+    int yk, zk;           // TMA coordinates of the key block
+    bool empty;           // a packed batch's key block past its sequence's keys
+    bool tail;            // a packed batch's key block holding rows past its end
+};
+template <bool PACKED>
+__device__ __forceinline__ KTile k_tile(const CommonArgs& a, int t, int bq)
+{
+    KTile w;
+    const int n_bkv = a.n_bh / a.h_q * a.h_kv;
+    const int group = a.h_q / a.h_kv;
+    w.kb = t / n_bkv;
+    w.bkv = t % n_bkv;
+    w.seq = w.bkv / a.h_kv;
+    w.kvh = w.bkv % a.h_kv;
+    w.bh0 = w.seq * a.h_q + w.kvh * group;
+    if constexpr (PACKED) {
+        w.q_first = a.cu_q[w.seq];
+        w.k_first = a.cu_k[w.seq];
+        w.lq = a.cu_q[w.seq + 1] - w.q_first;
+        w.lk = a.cu_k[w.seq + 1] - w.k_first;
+        w.zk = w.kvh;
+    } else {
+        w.q_first = w.k_first = 0;
+        w.lq = a.s;
+        w.lk = a.s_k;
+        w.zk = w.bkv;
+    }
+    w.empty = w.kb * 128 >= w.lk;
+    w.tail = PACKED && (w.kb + 1) * 128 > w.lk;
+    const int n_qt = ((w.lq + 127) / 128) * 128 / bq;
+    w.qt0 = a.causal ? (w.kb * 128) / bq : 0;
+    // under a top-left causal mask a key block past the last query is seen by none
+    w.per_head = n_qt > w.qt0 ? n_qt - w.qt0 : 0;
+    w.n_it = w.empty ? 0 : group * w.per_head;
+    w.yk = w.k_first + w.kb * 128;
+    return w;
+}
+// The key blocks the kernel walks: under a causal mask the padded layout's key
+// blocks past the last query block are seen by no query (the caller zeroes
+// their gradients); a packed batch's sequences differ, so there every key block
+// is a tile and such blocks store zeros.
+template <bool PACKED>
+__host__ __device__ inline int dkdv_key_blocks(const CommonArgs& a)
+{
+    return (!PACKED && a.causal && a.n_blk < a.n_blk_k) ? a.n_blk : a.n_blk_k;
+}
+template <bool PACKED>
+__device__ __forceinline__ bool next_ktile(const TileSched& sched, const CommonArgs& a, int bq, int& v, KTile& w)
+{
+    for (;; ++v) {
+        const int t = sched.tile(v);
+        if (t < 0) return false;
+        w = k_tile<PACKED>(a, t, bq);
+        if (!w.empty) {
+            ++v;
+            return true;
+        }
+    }
+}
 
 }  // namespace
 
@@ -108,47 +184,43 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     DkdvBars* bars = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
     auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
-    const int n_bkv = a.n_bh / a.h_q * a.h_kv;
-    const int kb = (int)(blockIdx.x / n_bkv);          // small key blocks carry the most work
-    const int bkv = (int)(blockIdx.x % n_bkv);         // flattened KV head: sequence * h_kv + head
     const int group = a.h_q / a.h_kv;
-    const int seq = bkv / a.h_kv, kvh = bkv % a.h_kv;
-    const int bh0 = seq * a.h_q + kvh * group;         // the group's first flattened query head
-    // The sequence's query and key counts and first rows (a packed batch), or the
-    // padded layout's; a packed batch's key blocks past its sequence's end have no work.
     constexpr bool packed = PACKED;
-    const int q_first = packed ? a.cu_q[seq] : 0, k_first = packed ? a.cu_k[seq] : 0;
-    const int lq = packed ? a.cu_q[seq + 1] - q_first : a.s;
-    const int lk = packed ? a.cu_k[seq + 1] - k_first : a.s_k;
-    if (kb * 128 >= lk) return;
-    const bool tail = packed && (kb + 1) * 128 > lk;   // rows past the end are not stored
-    const int n_qt = ((lq + 127) / 128) * 128 / BQ;
-    const int qt0 = a.causal ? (kb * 128) / BQ : 0;
-    // under a top-left causal mask a key block past the last query is seen by none:
-    // zero gradients
-    const int per_head = n_qt > qt0 ? n_qt - qt0 : 0;
-    const int n_it = group * per_head;
-    const int yk = k_first + kb * 128, zk = packed ? kvh : bkv;   // TMA coordinates of the key block
+    // Persistent: one CTA per SM walks its share of the key-block tiles, longest first.
+    const TileSched sched{dkdv_key_blocks<PACKED>(a) * (a.n_bh / a.h_q * a.h_kv), (int)gridDim.x, (int)blockIdx.x};
+    // Staging of dK and dV: where a query tile is 128 rows (d <= 128), a
+    // tile's dK and dV are staged in the query-ring slot of its last iteration
+    // (free once its last dK product is done), so the next tile's K and V can land
+    // during this tile's epilogue; otherwise (d = 160) they are staged in the K and
+    // V buffers and the next tile's K and V wait for their store.
+    constexpr bool RING_STAGE = (BQ == 128);
     // TMA row / head coordinates and workspace row of query tile qt of head `hq` of the group
-    auto q_coords = [&](int hq, int qt, int& yq, int& zq, size_t& srow) {
-        yq = q_first + qt * BQ;
-        zq = packed ? kvh * group + hq : bh0 + hq;
-        srow = packed ? (size_t)(kvh * group + hq) * a.ws_stride + packed_ws_row0(q_first, seq) + qt * BQ
-                      : (size_t)(bh0 + hq) * a.ws_stride + qt * BQ;
+    auto q_coords = [&](const KTile& w, int hq, int qt, int& yq, int& zq, size_t& srow) {
+        yq = w.q_first + qt * BQ;
+        zq = packed ? w.kvh * group + hq : w.bh0 + hq;
+        srow = packed ? (size_t)(w.kvh * group + hq) * a.ws_stride + packed_ws_row0(w.q_first, w.seq) + qt * BQ
+                      : (size_t)(w.bh0 + hq) * a.ws_stride + qt * BQ;
     };
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
         mbar_init(bar(bars->kv_full), 1);
+        mbar_init(bar(bars->kv_empty), 1);
         for (int st = 0; st < ST; ++st) {
             mbar_init(bar(bars->q_full[st]), 1);
             mbar_init(bar(bars->q_empty[st]), 1);
+            mbar_init(bar(bars->stage_free[st]), 1);
         }
         mbar_init(bar(bars->s_full), 1);
         mbar_init(bar(bars->dp_full), 1);
         mbar_init(bar(bars->p_full), kRowThreads);
         mbar_init(bar(bars->ds_full), kRowThreads);
         mbar_init(bar(bars->acc_done), 1);
+        mbar_init(bar(bars->acc_free), kRowThreads);
+        mbar_init(bar(bars->out_staged), kRowThreads);
+        mbar_init(bar(bars->out_read), 1);
+        mbar_init(bar(bars->kv_stage_free), 1);
+        mbar_init(bar(bars->drain), 1);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -174,34 +246,89 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     if (alive && warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer: K and V once, then (Q, dO, LSE2, D) per query tile
-            mbar_arrive_expect_tx(bar(bars->kv_full), 2 * C::KV_TILE);
-            for (int ch = 0; ch < G::NCH; ++ch) {
-                tma_load_3d(sb + C::OFF_K + ch * C::KV_CHUNK, &tm_k, ch * G::CW, yk, zk, bar(bars->kv_full));
-                tma_load_3d(sb + C::OFF_V + ch * C::KV_CHUNK, &tm_v, ch * G::CW, yk, zk, bar(bars->kv_full));
-            }
-            for (int it = 0; it < n_it; ++it) {
-                const int st = it % ST;
-                const int bh = bh0 + it / per_head;
-                const int qt = qt0 + it % per_head;
-                int yq, zq;
-                size_t srow;
-                q_coords(it / per_head, qt, yq, zq, srow);
-                if (!wait_bounded(wc, bar(bars->q_empty[st]), ((it / ST) & 1) ^ 1, timeout_code(kSiteQEmpty)))
-                    break;
-                const uint32_t fb = bar(bars->q_full[st]);
-                mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 2 * BQ * 4 + (MWS ? C::MSK_BYTES : 0u));
+            // ---- TMA producer: per tile K and V (once its predecessor's last S and dP
+            // products are done), then (Q, dO, LSE2, D and the keep bits) per query tile
+            // through one ring over all tiles.  A ring slot that holds a tile's staged
+            // output is refilled only after the store has read it.
+            int g = 0, u = 0, vt = 0;
+            bool ok = true;
+            uint32_t pending = 0u;     // bit st: slot st holds staged output not yet read
+            uint32_t sf_parity = 0u;   // bit st: phase parity of slot st's stage_free
+            KTile w;
+            while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
+                ok = wait_bounded(wc, bar(bars->kv_empty), (u & 1) ^ 1, timeout_code(kSiteKvFull));
+                if (ok && !RING_STAGE && u > 0)
+                    ok = wait_bounded(wc, bar(bars->kv_stage_free), (u - 1) & 1, timeout_code(kSiteStage));
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(bars->kv_full), 2 * C::KV_TILE);
                 for (int ch = 0; ch < G::NCH; ++ch) {
-                    tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, yq, zq, fb);
-                    tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, yq, zq, fb);
+                    tma_load_3d(sb + C::OFF_K + ch * C::KV_CHUNK, &tm_k, ch * G::CW, w.yk, w.zk, bar(bars->kv_full));
+                    tma_load_3d(sb + C::OFF_V + ch * C::KV_CHUNK, &tm_v, ch * G::CW, w.yk, w.zk, bar(bars->kv_full));
                 }
-                bulk_load_1d(sb + C::OFF_LSE + st * BQ * 4, args.lse2_ws + srow, BQ * 4, fb);
-                bulk_load_1d(sb + C::OFF_DEL + st * BQ * 4, args.delta_ws + srow, BQ * 4, fb);
-                if constexpr (MWS) {
-                    // this tile's rows of the (qb, kb) keep bits: both 64-row units, or one
-                    const size_t w0 = mask_pair_word(a, bh, (qt * BQ) >> 7, kb) + (size_t)(((qt * BQ) & 127) >> 6) * 256;
-                    bulk_load_1d(sb + C::OFF_MSK + st * C::MSK_BYTES, args.mask_ws + w0, C::MSK_BYTES, fb);
+                for (int it = 0; it < w.n_it && ok; ++it, ++g) {
+                    const int st = g % ST;
+                    const int bh = w.bh0 + it / w.per_head;
+                    const int qt = w.qt0 + it % w.per_head;
+                    int yq, zq;
+                    size_t srow;
+                    q_coords(w, it / w.per_head, qt, yq, zq, srow);
+                    ok = wait_bounded(wc, bar(bars->q_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteQEmpty));
+                    if (ok && RING_STAGE && ((pending >> st) & 1u)) {
+                        ok = wait_bounded(wc, bar(bars->stage_free[st]), (sf_parity >> st) & 1u, timeout_code(kSiteStage));
+                        sf_parity ^= 1u << st;
+                        pending &= ~(1u << st);
+                    }
+                    if (!ok) break;
+                    const uint32_t fb = bar(bars->q_full[st]);
+                    mbar_arrive_expect_tx(fb, 2 * C::Q_TILE + 2 * BQ * 4 + (MWS ? C::MSK_BYTES : 0u));
+                    for (int ch = 0; ch < G::NCH; ++ch) {
+                        tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, yq, zq, fb);
+                        tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, yq, zq,
+                                    fb);
+                    }
+                    bulk_load_1d(sb + C::OFF_LSE + st * BQ * 4, args.lse2_ws + srow, BQ * 4, fb);
+                    bulk_load_1d(sb + C::OFF_DEL + st * BQ * 4, args.delta_ws + srow, BQ * 4, fb);
+                    if constexpr (MWS) {
+                        // this tile's rows of the (qb, kb) keep bits: both 64-row units, or one
+                        const size_t w0 =
+                            mask_pair_word(a, bh, (qt * BQ) >> 7, w.kb) + (size_t)(((qt * BQ) & 127) >> 6) * 256;
+                        bulk_load_1d(sb + C::OFF_MSK + st * C::MSK_BYTES, args.mask_ws + w0, C::MSK_BYTES, fb);
+                    }
                 }
+                // the tile's last slot will hold its staged dK and dV
+                if (RING_STAGE && w.n_it > 0 && !w.tail) pending |= 1u << ((g - 1) % ST);
+                ++u;
+            }
+        } else if (lane == 1) {
+            // ---- dK and dV out: once the row threads have staged a tile's rows, one
+            // TMA store each, then the staging area is released (a tail tile's rows
+            // and a tile without queries were stored by the row threads)
+            int g = 0, u = 0, vt = 0;
+            bool ok = true;
+            KTile w;
+            while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
+                g += w.n_it;
+                ok = wait_bounded(wc, bar(bars->out_staged), u & 1, timeout_code(kSiteStage));
+                if (!ok) break;
+                const int slot = (g - 1 + 2 * ST) % ST;
+                const bool staged = !w.tail && (!RING_STAGE || w.n_it > 0);
+                if (staged) {
+                    const uint32_t ok_off = RING_STAGE ? C::OFF_Q + slot * C::Q_TILE : C::OFF_K;
+                    const uint32_t ov_off = RING_STAGE ? C::OFF_DO + slot * C::Q_TILE : C::OFF_V;
+                    for (int ch = 0; ch < G::NCH; ++ch) {
+                        tma_store_3d(&tm_dv, sb + ov_off + ch * C::KV_CHUNK, ch * G::CW, w.yk, w.zk);
+                        tma_store_3d(&tm_dk, sb + ok_off + ch * C::KV_CHUNK, ch * G::CW, w.yk, w.zk);
+                    }
+                    bulk_commit();
+                    bulk_wait_read0();
+                }
+                if (RING_STAGE) {
+                    if (staged) mbar_arrive(bar(bars->stage_free[slot]));
+                } else {
+                    mbar_arrive(bar(bars->kv_stage_free));
+                }
+                mbar_arrive(bar(bars->out_read));
+                ++u;
             }
         }
     } else if (alive && warp == 1) {
@@ -225,42 +352,62 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                            G::template desc_k<BQ>(dobase, kk), IDS, kk > 0 ? 1u : 0u);
                 mma_commit(bar(bars->dp_full));
             };
-            bool ok = wait_warp(wc, bar(bars->kv_full), 0, timeout_code(kSiteKvFull));
-            if (ok && n_it > 0) ok = wait_warp(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull));
-            if (ok && n_it > 0) {
-                tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-            }
-            for (int it = 0; it < n_it && ok; ++it) {
-                const int st = it % ST;
-                const uint32_t qbase = sb + C::OFF_Q + st * C::Q_TILE;
-                const uint32_t dobase = sb + C::OFF_DO + st * C::Q_TILE;
-                ok = wait_warp(wc, bar(bars->p_full), it & 1, timeout_code(kSitePFull));
+            int g = 0, u = 0, vt = 0;
+            bool ok = true;
+            KTile w;
+            while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
+                const int n_it = w.n_it;
+                ok = wait_warp(wc, bar(bars->kv_full), u & 1, timeout_code(kSiteKvFull));
+                if (ok && n_it > 0) ok = wait_warp(wc, bar(bars->q_full[g % ST]), (g / ST) & 1, timeout_code(kSiteQFull));
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::T_DV, tmem + C::T_S + split_a_col(kk, BQ), G::template desc_mn<BQ>(dobase, kk),
-                           IDG, (it > 0 || kk > 0) ? 1u : 0u);
-                if (it + 1 < n_it) {
-                    const int st1 = (it + 1) % ST;
-                    ok = wait_warp(wc, bar(bars->q_full[st1]), ((it + 1) / ST) & 1, timeout_code(kSiteQFull));
+                if (n_it > 0) {
+                    issue_s(g);
+                    issue_dp(g);
+                }
+                // K and V are free once the tile's last S and dP products are done
+                if (n_it <= 1) mma_commit(bar(bars->kv_empty));
+                for (int it = 0; it < n_it && ok; ++it, ++g) {
+                    const int st = g % ST;
+                    const uint32_t qbase = sb + C::OFF_Q + st * C::Q_TILE;
+                    const uint32_t dobase = sb + C::OFF_DO + st * C::Q_TILE;
+                    ok = wait_warp(wc, bar(bars->p_full), g & 1, timeout_code(kSitePFull));
+                    // the first dV product of a tile overwrites the accumulators: the
+                    // epilogue of the tile before must have read them
+                    if (ok && it == 0) ok = wait_warp(wc, bar(bars->acc_free), (u & 1) ^ 1, timeout_code(kSiteAcc));
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(it + 1);
-                }
-                ok = wait_warp(wc, bar(bars->ds_full), it & 1, timeout_code(kSiteDsFull));
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::T_DK, tmem + C::T_DP + split_a_col(kk, BQ), G::template desc_mn<BQ>(qbase, kk),
-                           IDG, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(bars->q_empty[st]));
-                if (it + 1 < n_it) issue_dp(it + 1);
+                    for (int kk = 0; kk < BQ / 16; ++kk)
+                        mma_ts(tmem + C::T_DV, tmem + C::T_S + split_a_col(kk, BQ), G::template desc_mn<BQ>(dobase, kk),
+                               IDG, (it > 0 || kk > 0) ? 1u : 0u);
+                    if (it + 1 < n_it) {
+                        const int st1 = (g + 1) % ST;
+                        ok = wait_warp(wc, bar(bars->q_full[st1]), ((g + 1) / ST) & 1, timeout_code(kSiteQFull));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(g + 1);
+                    }
+                    ok = wait_warp(wc, bar(bars->ds_full), g & 1, timeout_code(kSiteDsFull));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk)
+                        mma_ts(tmem + C::T_DK, tmem + C::T_DP + split_a_col(kk, BQ), G::template desc_mn<BQ>(qbase, kk),
+                               IDG, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(bars->q_empty[st]));
+                    if (it + 1 < n_it) {
+                        issue_dp(g + 1);
+                        if (it + 2 == n_it) mma_commit(bar(bars->kv_empty));
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar(bars->acc_done));
+                ++u;
             }
-            if (ok) mma_commit(bar(bars->acc_done));
+            // every MMA must be complete before the CTA releases TMEM
+            mma_commit(bar(bars->drain));
+            wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 4) {
         // ---- row threads: key = TMEM lane, half = which BQ/2 queries of a tile
@@ -268,8 +415,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const RowThread rt = row_thread();
         const int h = rt.half, r = rt.row;
         const uint32_t lane_off = rt.lane_off;
-        const int key = kb * 128 + r;
-        const uint32_t warp_key0 = (uint32_t)(kb * 128 + (int)(warp & 3u) * 32);
         const float* lse2_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
         const KeepSwar8 ks(a.thr);
         const uint64_t zs2 = f2_pack(a.keep_scale, a.keep_scale);
@@ -278,9 +423,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // of tile it + 1 are drawn right after tile it's dS, while the tensor core forms
         // S_{it+1}: the draw needs no score.
         uint32_t kw[HQ / 16][4];
-        auto draw_mask = [&](int it) {
-            const int bh = bh0 + it / per_head;
-            const int q0 = (qt0 + it % per_head) * BQ + HQ * h;
+        auto draw_mask = [&](const KTile& w, int it) {
+            const int bh = w.bh0 + it / w.per_head;
+            const int q0 = (w.qt0 + it % w.per_head) * BQ + HQ * h;
+            const uint32_t warp_key0 = (uint32_t)(w.kb * 128 + (int)(warp & 3u) * 32);
             const PhiloxKey pk{a.rk, (uint32_t)bh + a.bh0, a.offset};
             keep_bytes_col16<HQ>(pk, ks, warp_key0 / 16u + lane / 16u, (uint32_t)q0, kw);
         };
@@ -298,15 +444,20 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // after the transpose, lane p holds the queries of bit position p, so the lane
         // of key L reads it from lane keep_bit_position(L).
         const int src_lane = (int)keep_bit_position(lane);
-        if (DROP && !MWS && n_it > 0) draw_mask(0);
+        int g = 0, u = 0, vt = 0;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int st = it % ST;
-            const int q0 = (qt0 + it % per_head) * BQ + HQ * h;     // this half's first query
+        KTile w;
+        while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
+        const int n_it = w.n_it, kb = w.kb;
+        const int key = kb * 128 + r;
+        if (DROP && !MWS && n_it > 0) draw_mask(w, 0);
+        for (int it = 0; it < n_it; ++it, ++g) {
+            const int st = g % ST;
+            const int q0 = (w.qt0 + it % w.per_head) * BQ + HQ * h;     // this half's first query
             ok = __all_sync(0xffffffffu,
-                            wait_bounded(wc, bar(bars->q_full[st]), (it / ST) & 1, timeout_code(kSiteQFull)));
+                            wait_bounded(wc, bar(bars->q_full[st]), (g / ST) & 1, timeout_code(kSiteQFull)));
             if (ok)
-                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), it & 1, timeout_code(kSiteSFull)));
+                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
             if constexpr (DROP && MWS) {
@@ -376,7 +527,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_before();
             mbar_arrive(bar(bars->p_full));
 
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), it & 1, timeout_code(kSiteDpFull)));
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -405,18 +556,24 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(bars->ds_full));
-            if (DROP && !MWS && it + 1 < n_it) draw_mask(it + 1);
+            if (DROP && !MWS && it + 1 < n_it) draw_mask(w, it + 1);
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), 0, timeout_code(kSiteAcc)));
-        // dV and dK of this key row: staged for one TMA store of the block, or (a
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), u & 1, timeout_code(kSiteAcc)));
+        if (!ok) break;
+        // dV and dK of this key row: staged for the TMA store of the tile (in the
+        // query-ring slot of its last iteration, or the K and V buffers), or -- a
         // packed batch's tail block, whose tensor map runs on into the next
-        // sequence) stored row by row; zero when no query sees the block
+        // sequence, and a ring-staged tile without queries -- stored row by row;
+        // zero when no query sees the block
+        const int slot = (g - 1 + 2 * ST) % ST;
+        const bool direct = w.tail || (RING_STAGE && n_it == 0);
         auto put_row = [&](uint16_t* base, uint32_t stage_off, int c32, uint32_t (&rr)[32], float mul) {
-            if (!tail) {
+            if (!direct) {
                 stage_row32<D, 128>(sb + stage_off, r, c32 * 32, rr, mul);
-            } else if (kb * 128 + r < lk) {
-                uint4* row = reinterpret_cast<uint4*>(base + (size_t)zk * args.kv_head_stride +
-                                                      (size_t)(yk + r) * args.kv_row_stride) + c32 * 4;
+            } else if (kb * 128 + r < w.lk) {
+                uint4* row = reinterpret_cast<uint4*>(base + (size_t)w.zk * args.kv_head_stride +
+                                                      (size_t)(w.yk + r) * args.kv_row_stride) + c32 * 4;
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
                     uint32_t wv[4];
@@ -428,34 +585,34 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 }
             }
         };
-        if (ok) {
-            tc_fence_after();
+        const uint32_t stage_k = RING_STAGE ? C::OFF_Q + slot * C::Q_TILE : C::OFF_K;
+        const uint32_t stage_v = RING_STAGE ? C::OFF_DO + slot * C::Q_TILE : C::OFF_V;
+        tc_fence_after();
 #pragma unroll 1
-            for (int c32 = h; c32 < D / 32; c32 += 2) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
-                if (n_it == 0) {
+        for (int c32 = h; c32 < D / 32; c32 += 2) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + C::T_DV + lane_off + c32 * 32, rr);
+            if (n_it == 0) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
-                }
-                put_row(args.dv, C::OFF_V, c32, rr, DROP ? a.keep_scale : 1.0f);
-                tmem_ld32(tmem + C::T_DK + lane_off + c32 * 32, rr);
-                if (n_it == 0) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
-                }
-                put_row(args.dk, C::OFF_K, c32, rr, a.scale);
+                for (int e = 0; e < 32; ++e) rr[e] = 0u;
             }
+            put_row(args.dv, stage_v, c32, rr, DROP ? a.keep_scale : 1.0f);
+            tmem_ld32(tmem + C::T_DK + lane_off + c32 * 32, rr);
+            if (n_it == 0) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) rr[e] = 0u;
+            }
+            put_row(args.dk, stage_k, c32, rr, a.scale);
         }
+        tc_fence_before();
+        mbar_arrive(bar(bars->acc_free));   // the next tile's products may overwrite them
         fence_proxy_async_smem();
-        named_barrier_sync(1, kRowThreads);
-        if (!tail && h == 0 && r == 0 && !bars->abort_flag) {
-            for (int ch = 0; ch < G::NCH; ++ch) {
-                tma_store_3d(&tm_dv, sb + C::OFF_V + ch * C::KV_CHUNK, ch * G::CW, yk, zk);
-                tma_store_3d(&tm_dk, sb + C::OFF_K + ch * C::KV_CHUNK, ch * G::CW, yk, zk);
-            }
-            bulk_commit();
-            bulk_wait_read0();
+        // the store lane takes one tile at a time: a tile is handed over only after
+        // the previous one is done (tiles without queries can follow one another fast)
+        if (u > 0) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->out_read), (u - 1) & 1, timeout_code(kSiteStage)));
+        if (!ok) break;
+        mbar_arrive(bar(bars->out_staged));
+        ++u;
         }
     }
 
@@ -1081,12 +1238,8 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
-    // under a causal mask the key blocks past the last query block are seen by
-    // no query (the caller zeroes their gradients); a packed batch's sequences
-    // differ, so there every key block runs and such blocks store zeros
-    const unsigned n_kb =
-        (unsigned)(a.c.causal && a.c.n_blk < a.c.n_blk_k && a.c.cu_q == nullptr ? a.c.n_blk : a.c.n_blk_k);
-    const unsigned grid = n_kb * n_bkv;
+    const unsigned tiles = (unsigned)dkdv_key_blocks<PACKED>(a.c) * n_bkv;
+    const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;   // persistent
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return (int)cudaGetLastError();
 }
