@@ -19,11 +19,17 @@
 //           TMEM score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM
 //   warps 4-11  two warpgroups on the same 128 query rows (TMEM lanes), one
 //           per half of the 128 keys of a block: online softmax in the log2
-//           domain (the halves swap their row maxima and sums through spare
-//           TMEM columns), dropout from Philox, P_d written back to TMEM as
-//           bf16 inside the half's own score columns; epilogue O / l -> bf16
+//           domain, dropout from Philox, P_d written back to TMEM as bf16
+//           inside the half's own score columns; epilogue O / l -> bf16
 //           staged in shared memory and written by one TMA store per tile
 //           (d <= 128; d = 160 stores rows from registers)
+// For d <= 128 the two halves of a row are independent online softmaxes: each
+// keeps its own running maximum and sum, and its own O accumulator in TMEM
+// (O_h += P_h V_h, V_h the half's 64 rows of the block), so neither waits on
+// the other inside a tile; the epilogue merges them,
+//     m = max(m_0, m_1),  l = sum_h l_h 2^(m_h - m),  O = sum_h O_h 2^(m_h - m) / l.
+// For d = 160 TMEM has no room for a second accumulator: the halves share one
+// O and swap their block maxima (and the final sums) through TMEM columns.
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks skip the rescale; O / l is exact either way.
 #include "kernels.h"
@@ -55,21 +61,32 @@ struct FwdCfg {
     static constexpr uint32_t OFF_OST = OFF_V + ST * TILE;
     static constexpr uint32_t OFF_BAR = OFF_OST + (STAGE_O ? TILE : 0);
     static constexpr uint32_t BAR_BYTES = 512;
-    static constexpr uint32_t SMEM = OFF_BAR + BAR_BYTES + 1024;
+    // SPLIT (d <= 128): each column half of a row keeps its own running maximum,
+    // sum and O accumulator, so the halves never wait on each other inside a
+    // tile; the tile's epilogue merges the two (row statistics swapped through
+    // XCH_BYTES of shared memory).  d = 160 has no TMEM for a second
+    // accumulator: its halves share one O and swap their block maxima.
+    static constexpr bool SPLIT = (D <= 128);
+    static constexpr uint32_t OFF_XCH = OFF_BAR + BAR_BYTES;
+    static constexpr uint32_t XCH_BYTES = SPLIT ? 128 * 8 : 0;
+    static constexpr uint32_t SMEM = OFF_XCH + XCH_BYTES + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    // TMEM columns: two score buffers, the O accumulator, then six exchange
+    // TMEM columns: two score buffers, then the O accumulator of half 0 (T_O)
+    // and of half 1 (T_O1) when SPLIT, else the shared O and six exchange
     // columns through which the two halves of a row swap their block maxima
     // (2 buffers x 2 halves) and row sums (2 halves).
-    static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_X = 256 + D;
-    static_assert(T_X + 6 <= 512, "TMEM budget");
+    static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O = 256, T_O1 = 256 + D, T_X = 256 + D;
+    static_assert(SPLIT ? (T_O1 + D <= 512) : (T_X + 6 <= 512), "TMEM budget");
 };
 
 struct FwdBars {
     uint64_t q_full[2], q_empty[2];
     uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
     uint64_t s_full[2], p_full[2];
+    uint64_t p_half[2][2];  // SPLIT: [score buffer][half] P_d of the half is in TMEM
+    uint64_t o_half[2];     // SPLIT: the half's P.V of the block is done
     uint64_t xmax[2];       // row-max exchange between the two column halves
-    uint64_t lsum;          // row-sum exchange at the end of a tile
+    uint64_t lsum, lsum2;   // row-statistics exchange at the end of a tile
     uint64_t o_done, o_free;
     uint64_t o_tile;        // a tile's last P.V product is done (its O is final)
     uint64_t drain;         // every MMA of this CTA is done (before TMEM is released)
@@ -120,6 +137,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(bars->s_full[b]), 1);
             mbar_init(bar(bars->p_full[b]), kRowThreads);
             mbar_init(bar(bars->xmax[b]), kRowThreads);
+            mbar_init(bar(bars->p_half[b][0]), kRowThreads / 2);
+            mbar_init(bar(bars->p_half[b][1]), kRowThreads / 2);
+            mbar_init(bar(bars->o_half[b]), 1);
         }
         mbar_init(bar(bars->o_done), 1);
         mbar_init(bar(bars->o_free), kRowThreads);
@@ -134,6 +154,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(bar(bars->v_empty[st]), 1);
         }
         mbar_init(bar(bars->lsum), kRowThreads);
+        mbar_init(bar(bars->lsum2), kRowThreads);
         mbar_init(bar(bars->never), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -222,20 +243,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             auto issue_pv = [&](const Blk& k) -> bool {
                 if (k.j == 0 && !wait_warp(wc, bar(bars->o_free), (k.u & 1) ^ 1, timeout_code(kSiteOFree)))
                     return false;
-                if (!wait_warp(wc, bar(bars->p_full[k.g & 1]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
-                    return false;
                 const int st = k.g % ST;
-                if (!wait_warp(wc, bar(bars->v_full[st]), (k.g / ST) & 1, timeout_code(kSiteVFull)))
-                    return false;
-                tc_fence_after();
                 const uint32_t vbase = sb + C::OFF_V + st * C::TILE;
                 const uint32_t tP = tmem + ((k.g & 1) ? C::T_S1 : C::T_S0);
+                if constexpr (C::SPLIT) {
+                    // O_h += P_h V_h for each half h of the block's keys (P_h in the
+                    // half's first 32 score columns, V_h the half's 64 rows of V)
+                    if (!wait_warp(wc, bar(bars->v_full[st]), (k.g / ST) & 1, timeout_code(kSiteVFull)))
+                        return false;
+                    for (int h = 0; h < 2; ++h) {
+                        if (!wait_warp(wc, bar(bars->p_half[k.g & 1][h]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
+                            return false;
+                        tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + C::T_O, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk), IDO,
-                           (k.j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts(tmem + (h ? C::T_O1 : C::T_O), tP + 64 * h + 8 * kk,
+                                   G::template desc_mn<128>(vbase, 4 * h + kk), IDO, (k.j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar(bars->o_half[h]));
+                    }
+                } else {
+                    if (!wait_warp(wc, bar(bars->p_full[k.g & 1]), (k.g >> 1) & 1, timeout_code(kSitePFull)))
+                        return false;
+                    if (!wait_warp(wc, bar(bars->v_full[st]), (k.g / ST) & 1, timeout_code(kSiteVFull)))
+                        return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + C::T_O, tP + split_a_col(kk, 128), G::template desc_mn<128>(vbase, kk), IDO,
+                               (k.j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(bars->o_done));
+                }
                 mma_commit(bar(bars->v_empty[st]));
-                mma_commit(bar(bars->o_done));
                 if (k.j == k.nk - 1) mma_commit(bar(bars->o_tile));
                 return true;
             };
@@ -285,7 +323,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const RowThread rt = row_thread();
         const int h = rt.half, r = rt.row;
         const uint32_t lane_off = rt.lane_off;
-        const uint32_t tX = tmem + C::T_X + lane_off;   // exchange columns of this warp's rows
+        const uint32_t tX = tmem + C::T_X + lane_off;   // exchange columns of this warp's rows (d = 160)
+        float2* xch = reinterpret_cast<float2*>(smem_raw + pad + C::OFF_XCH);   // row statistics (SPLIT)
         int pv_done = 0;            // P.V products completed into O by earlier tiles
         int g0 = 0;
         bool ok = true;
@@ -296,6 +335,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int i = qb * 128 + r;          // query of the sequence
             const bool live = i < w.lq;          // rows past the end are computed, not stored
             const uint32_t tO = tmem + C::T_O + lane_off;
+            const uint32_t tO1 = tmem + C::T_O1 + lane_off;
+            // this half's accumulator (SPLIT), else the shared one
+            const uint32_t tOh = (C::SPLIT && h) ? tO1 : tO;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nk; ++j) {
                 const int g = g0 + j;
@@ -326,29 +368,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int c = 3; c < 63; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
                 mx = fmaxf(mx, x[63]);
-                // swap block maxima with the other half of the row through TMEM
-                tmem_st1(tX + (g & 1) * 2 + h, __float_as_uint(mx));
-                tmem_st_wait();
-                tc_fence_before();
-                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xmax[g & 1]), (g >> 1) & 1,
-                                                         timeout_code(kSiteXmax)));
-                if (!ok) break;
-                tc_fence_after();
-                mx = fmaxf(mx, __uint_as_float(tmem_ld1(tX + (g & 1) * 2 + (h ^ 1))));
+                if constexpr (!C::SPLIT) {
+                    // swap block maxima with the other half of the row through TMEM
+                    tmem_st1(tX + (g & 1) * 2 + h, __float_as_uint(mx));
+                    tmem_st_wait();
+                    tc_fence_before();
+                    ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xmax[g & 1]), (g >> 1) & 1,
+                                                             timeout_code(kSiteXmax)));
+                    if (!ok) break;
+                    tc_fence_after();
+                    mx = fmaxf(mx, __uint_as_float(tmem_ld1(tX + (g & 1) * 2 + (h ^ 1))));
+                }
                 const float m_new = fmaxf(m_run, mx * a.scale_log2);
                 if (__any_sync(0xffffffffu, m_new > m_run + 8.0f)) {
                     if (j > 0) {
-                        ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_done), (pv_done + j - 1) & 1,
-                                                                  timeout_code(kSiteODone)));
+                        // the accumulator's last P.V (block j - 1) must be done
+                        ok = __all_sync(0xffffffffu,
+                                        wait_bounded(wc, bar(C::SPLIT ? bars->o_half[h] : bars->o_done),
+                                                     (pv_done + j - 1) & 1, timeout_code(kSiteODone)));
                         if (!ok) break;
                         tc_fence_after();
                         const float f = ex2_approx(m_run - m_new);
                         l_run *= f;
                         const uint64_t f2 = f2_pack(f, f);
+                        // SPLIT: all of this half's accumulator; else this half's share
+                        // of the columns of the shared one
+                        constexpr int c_step = C::SPLIT ? 1 : 2;
 #pragma unroll 1
-                        for (int c32 = h; c32 < D / 32; c32 += 2) {
+                        for (int c32 = C::SPLIT ? 0 : h; c32 < D / 32; c32 += c_step) {
                             uint32_t rr[32];
-                            tmem_ld32(tO + c32 * 32, rr);
+                            tmem_ld32(tOh + c32 * 32, rr);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const uint64_t o2 =
@@ -358,12 +407,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                 rr[2 * e] = __float_as_uint(lo);
                                 rr[2 * e + 1] = __float_as_uint(hi);
                             }
-                            tmem_st32(tO + c32 * 32, rr);
+                            tmem_st32(tOh + c32 * 32, rr);
                         }
                         tmem_st_wait();
                     }
                     m_run = m_new;
                 }
+                // A SPLIT half whose keys have all been masked so far has m_run = -inf:
+                // its exponent reference is then 0 (every p of the half is 0).
+                const float m_ref = (C::SPLIT && m_run == -INFINITY) ? 0.f : m_run;
                 // p = 2^(x * scale_log2 - m), two at a time, and the dropout mask, in four
                 // independent units of 16 keys (one Philox call each) so that the exp2
                 // (MUFU) and Philox (integer multiply) work of different units overlap;
@@ -371,7 +423,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // of one SWAR test per output word (four keys) as byte sign bits, which
                 // mask the packed bf16 pairs directly.
                 const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-                const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
                 const KeepSwar8 ks(a.thr);
                 uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
                 uint32_t pw[32];
@@ -407,24 +459,76 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_st32(tS, pw);   // P_d of these 64 keys over the first 32 of the half's columns
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(bars->p_full[g & 1]));
+                mbar_arrive(bar(C::SPLIT ? bars->p_half[g & 1][h] : bars->p_full[g & 1]));
             }
             if (!ok) break;
-            // row sum over both halves, through TMEM
-            tmem_st1(tX + 4 + h, __float_as_uint(l_run));
-            tmem_st_wait();
-            tc_fence_before();
-            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->lsum), u & 1, timeout_code(kSiteLsum)));
-            if (!ok) break;
-            tc_fence_after();
-            const float l_tot = l_run + __uint_as_float(tmem_ld1(tX + 4 + (h ^ 1)));
+            // Final row statistics, and the factors that turn the accumulator(s) into
+            // O: O = a0 * O_0 + a1 * O_1 (SPLIT), O = a0 * O (else).
+            float a0 = 0.f, a1 = 0.f, lse_i = 0.f;
+            if constexpr (C::SPLIT) {
+                // half 1 hands its (m, l) to half 0, which merges them and hands back
+                // the two factors
+                if (h == 1) xch[r] = make_float2(m_run, l_run);
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->lsum), u & 1, timeout_code(kSiteLsum)));
+                if (!ok) break;
+                if (h == 0) {
+                    const float2 o1 = xch[r];
+                    const float m = fmaxf(m_run, o1.x);
+                    const float m_ref = (m == -INFINITY) ? 0.f : m;
+                    const float f0 = ex2_approx(m_run - m_ref), f1 = ex2_approx(o1.x - m_ref);
+                    const float l_tot = l_run * f0 + o1.y * f1;
+                    const float inv = a.keep_scale / l_tot;
+                    a0 = f0 * inv;
+                    a1 = f1 * inv;
+                    lse_i = (m_ref + log2f(l_tot)) * 0.693147180559945309f;
+                    xch[r] = make_float2(a0, a1);
+                }
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->lsum2), u & 1, timeout_code(kSiteLsum)));
+                if (!ok) break;
+                if (h == 1) {
+                    const float2 f = xch[r];
+                    a0 = f.x;
+                    a1 = f.y;
+                }
+            } else {
+                // row sum over both halves, through TMEM
+                tmem_st1(tX + 4 + h, __float_as_uint(l_run));
+                tmem_st_wait();
+                tc_fence_before();
+                ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->lsum), u & 1, timeout_code(kSiteLsum)));
+                if (!ok) break;
+                tc_fence_after();
+                const float l_tot = l_run + __uint_as_float(tmem_ld1(tX + 4 + (h ^ 1)));
+                a0 = a.keep_scale / l_tot;
+                lse_i = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+            }
             // the tile's final P.V: a barrier of its own, completing once per tile (the
-            // shared o_done may still be two phases behind here)
+            // per-block barriers may still be two phases behind here)
             ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_tile), u & 1, timeout_code(kSiteOTile)));
             if (!ok) break;
             tc_fence_after();
-            const float inv = a.keep_scale / l_tot;
-            const float lse_i = (m_run + log2f(l_tot)) * 0.693147180559945309f;
+            // 32 columns [32 c32, 32 c32 + 32) of this row of O, as fp32 bits
+            auto o_chunk = [&](int c32, uint32_t (&rr)[32]) {
+                tmem_ld32(tO + c32 * 32, rr);
+                if constexpr (C::SPLIT) {
+                    uint32_t r1[32];
+                    tmem_ld32(tO1 + c32 * 32, r1);
+                    const uint64_t a02 = f2_pack(a0, a0), a12 = f2_pack(a1, a1);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t o2 =
+                            f2_fma(f2_pack(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1])), a02,
+                                   f2_mul(f2_pack(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])), a12));
+                        float lo, hi;
+                        f2_unpack(o2, lo, hi);
+                        rr[2 * e] = __float_as_uint(lo);
+                        rr[2 * e + 1] = __float_as_uint(hi);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * a0);
+                }
+            };
             // O row i straight to global memory: 16-byte stores of this half's
             // 32-column chunks.  The TMEM loads are warp-collective, so every lane
             // takes them; only the stores are guarded (rows past the sequence's end).
@@ -434,14 +538,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll 1
                 for (int c32 = h; c32 < D / 32; c32 += 2) {
                     uint32_t rr[32];
-                    tmem_ld32(tO + c32 * 32, rr);
+                    o_chunk(c32, rr);
 #pragma unroll
                     for (int u4 = 0; u4 < 4; ++u4) {
                         uint32_t wv[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            wv[e] = pack_bf16x2(__uint_as_float(rr[8 * u4 + 2 * e]) * inv,
-                                                __uint_as_float(rr[8 * u4 + 2 * e + 1]) * inv);
+                            wv[e] = pack_bf16x2(__uint_as_float(rr[8 * u4 + 2 * e]),
+                                                __uint_as_float(rr[8 * u4 + 2 * e + 1]));
                         if (live) orow[c32 * 4 + u4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                     }
                 }
@@ -460,8 +564,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll 1
                     for (int c32 = h; c32 < D / 32; c32 += 2) {
                         uint32_t rr[32];
-                        tmem_ld32(tO + c32 * 32, rr);
-                        stage_row32<D, 128>(sb + C::OFF_OST, r, c32 * 32, rr, inv);
+                        o_chunk(c32, rr);
+                        stage_row32<D, 128>(sb + C::OFF_OST, r, c32 * 32, rr, 1.0f);
                     }
                 } else {
                     store_rows();
