@@ -240,11 +240,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
-    // Launched behind the dQ kernel, which released its dependents only after
-    // its own inputs were complete: Q, K, V and dO may be loaded at once, the
-    // row statistics and keep bits that kernel writes only after griddep_wait
-    // (the producer's, before its first workspace load).
-    griddep_launch_dependents();
 
     bool alive = true;
     if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
@@ -259,7 +254,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bool ok = true;
             uint32_t pending = 0u;     // bit st: slot st holds staged output not yet read
             uint32_t sf_parity = 0u;   // bit st: phase parity of slot st's stage_free
-            bool dep_done = false;     // the dQ kernel's outputs are visible
             KTile w;
             while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
                 ok = wait_bounded(wc, bar(bars->kv_empty), (u & 1) ^ 1, timeout_code(kSiteKvFull));
@@ -291,10 +285,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                         tma_load_3d(sb + C::OFF_Q + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_q, ch * G::CW, yq, zq, fb);
                         tma_load_3d(sb + C::OFF_DO + st * C::Q_TILE + ch * C::Q_CHUNK, &tm_do, ch * G::CW, yq, zq,
                                     fb);
-                    }
-                    if (!dep_done) {
-                        griddep_wait();
-                        dep_done = true;
                     }
                     bulk_load_1d(sb + C::OFF_LSE + st * BQ * 4, args.lse2_ws + srow, BQ * 4, fb);
                     bulk_load_1d(sb + C::OFF_DEL + st * BQ * 4, args.delta_ws + srow, BQ * 4, fb);
@@ -786,11 +776,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
-    // everything above overlaps the kernel before; the rest reads its outputs.
-    // Dependents are released only after that wait: the dK/dV kernel loads this
-    // kernel's inputs (Q, K, V, dO) before its own wait.
-    griddep_wait();
-    griddep_launch_dependents();
 
     bool alive = true;
     if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
@@ -1255,7 +1240,8 @@ static int launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     const unsigned n_bkv = (unsigned)(a.c.n_bh / a.c.h_q * a.c.h_kv);
     const unsigned tiles = (unsigned)dkdv_key_blocks<PACKED>(a.c) * n_bkv;
     const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;   // persistent
-    return (int)launch_pdl(kern, grid, kThreads, smem, stream, tq, tk, tv, tdo, tdk, tdv, a);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, a);
+    return (int)cudaGetLastError();
 }
 
 template <int D, bool DROP, bool MWS, bool PACKED>
@@ -1274,7 +1260,8 @@ static int launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
         return (int)cudaErrorInvalidConfiguration;
     const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
     const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;
-    return (int)launch_pdl(kern, grid, kThreadsRng, smem, stream, tq, tk, tv, tdo, to, tdq, a);
+    kern<<<grid, kThreadsRng, smem, stream>>>(tq, tk, tv, tdo, to, tdq, a);
+    return (int)cudaGetLastError();
 }
 
 int launch_bwd_dkdv(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -174,9 +174,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
-    // everything above overlaps the kernel before; the rest reads its outputs
-    griddep_wait();
-    griddep_launch_dependents();
 
     bool alive = true;
     if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
@@ -616,7 +613,8 @@ static int launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (e != cudaSuccess) return (int)e;
     const unsigned tiles = (unsigned)a.c.n_blk * (unsigned)a.c.n_bh;
     const unsigned grid = tiles < (unsigned)a.num_sms ? tiles : (unsigned)a.num_sms;
-    return (int)launch_pdl(kern, grid, kThreads, smem, stream, tq, tk, tv, to, a);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, a);
+    return (int)cudaGetLastError();
 }
 
 int launch_fwd(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

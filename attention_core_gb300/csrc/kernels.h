@@ -179,27 +179,6 @@ __host__ __device__ inline size_t mask_pair_word(const CommonArgs& a, int bh, in
 }
 inline size_t mask_ws_words(const CommonArgs& a) { return mask_pair_word(a, a.n_bh, 0, 0); }
 
-// Launch of the tensor-core kernels with programmatic stream serialization:
-// each may start (prologue, TMEM allocation, barrier set-up) while the kernel
-// before it in the stream finishes, and waits for it (griddep_wait) before it
-// touches memory that kernel may write.
-template <class... KArgs, class... Args>
-inline cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, unsigned smem,
-                              cudaStream_t stream, const Args&... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 // Host launchers; return a cudaError_t value.
 int launch_fwd(int d, bool dropout, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& to, const FwdArgs& a, cudaStream_t stream);

@@ -214,18 +214,6 @@ __device__ __forceinline__ void regs_lower()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// Programmatic dependent launch.  A kernel launched with programmatic stream
-// serialization may start while the kernel before it in the stream is still
-// running, once every CTA of that kernel has released its dependents (or
-// exited).  griddep_wait returns when the kernel before has completed and its
-// memory writes are visible (at once when there is no such dependency), so
-// every access to memory that kernel may write must follow it.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ------------------------------------------------------------ tcgen05 ---
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
