@@ -189,6 +189,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteKEmpty));
+                    // At the start every CTA loads at once and HBM is the bottleneck:
+                    // the ring's later stages wait until the block before has landed,
+                    // so the first scores' operands are not queued behind them.
+                    if (ok && g > 0 && g < ST)
+                        ok = wait_bounded(wc, bar(bars->k_full[g - 1]), 0, timeout_code(kSiteKFull));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->k_full[st]), C::TILE);
                     for (int ch = 0; ch < G::NCH; ++ch)
@@ -203,6 +208,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int u = 0; next_qtile<PACKED>(sched, a, 128, vt, w); ++u) {
                 const int qs = u % C::NQ;
                 if (!wait_bounded(wc, bar(bars->q_empty[qs]), ((u / C::NQ) & 1) ^ 1, timeout_code(kSiteQEmpty)))
+                    break;
+                // the second tile's Q only once the first has landed (see the K ring)
+                if (u == 1 && C::NQ == 2 && !wait_bounded(wc, bar(bars->q_full[0]), 0, timeout_code(kSiteQFull)))
                     break;
                 mbar_arrive_expect_tx(bar(bars->q_full[qs]), C::TILE);
                 for (int ch = 0; ch < G::NCH; ++ch)
@@ -221,6 +229,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % ST;
                     ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteVEmpty));
+                    // the first V block after the first K block, the ring's later
+                    // stages after the block before (see the K ring)
+                    if (ok && g < ST)
+                        ok = wait_bounded(wc, bar(g == 0 ? bars->k_full[0] : bars->v_full[g - 1]), 0,
+                                          timeout_code(g == 0 ? kSiteKFull : kSiteVFull));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->v_full[st]), C::TILE);
                     for (int ch = 0; ch < G::NCH; ++ch)
