@@ -456,10 +456,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const int q0 = (w.qt0 + it % w.per_head) * BQ + HQ * h;     // this half's first query
             ok = __all_sync(0xffffffffu,
                             wait_bounded(wc, bar(bars->q_full[st]), (g / ST) & 1, timeout_code(kSiteQFull)));
-            if (ok)
-                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
-            tc_fence_after();
+            // The keep bits came with this query tile's stage: their transpose needs no
+            // score, so it runs while the tensor core forms S^T.
             if constexpr (DROP && MWS) {
                 const uint32_t* msk = reinterpret_cast<const uint32_t*>(smem + C::OFF_MSK + st * C::MSK_BYTES);
 #pragma unroll
@@ -471,6 +470,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     for (int n = 0; n < 8; ++n) kbyte[8 * c + n] = keep_nibble_bytes((col >> (4 * n)) & 0xFu);
                 }
             }
+            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
+            if (!ok) break;
+            tc_fence_after();
             // per-query row statistics of this half (-LSE log2(e) and -D), four at a time
             const float4* nl4 = reinterpret_cast<const float4*>(lse2_s + st * BQ + HQ * h);
             const float4* dl4 = reinterpret_cast<const float4*>(del_s + st * BQ + HQ * h);
