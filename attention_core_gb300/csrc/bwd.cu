@@ -1035,6 +1035,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint64_t dt2 = 0, ndt2 = 0;
             uint64_t dacc2 = f2_pack(0.f, 0.f);
             for (int j = 0; j < nk && ok; ++j, ++g) {
+                // this block's keep bits from the RNG warps' ring: they need no score, so
+                // they are taken (and the slot freed) while the tensor core forms S
+                uint32_t kbits[HK / 32];
+                if (DROP) {
+                    const int rs = g % C::RNG_ST;
+                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->rng_full[rs]), (g / C::RNG_ST) & 1,
+                                                              timeout_code(kSiteRng)));
+                    if (!ok) break;
+                    const uint32_t* ring =
+                        reinterpret_cast<const uint32_t*>(smem_raw + pad + C::OFF_RNG + rs * C::RNG_BYTES);
+#pragma unroll
+                    for (int c32 = 0; c32 < HK / 32; ++c32) kbits[c32] = ring[(h * (HK / 32) + c32) * 128 + r];
+                    mbar_arrive(bar(bars->rng_empty[rs]));
+                }
                 ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
                 if (!ok) break;
                 tc_fence_after();
@@ -1119,19 +1133,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 // and one mask per word, the inverse of keep_bits32).
                 uint32_t keep[HK / 4];
                 if (DROP) {
-                    const int rs = g % C::RNG_ST;
-                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->rng_full[rs]), (g / C::RNG_ST) & 1,
-                                                              timeout_code(kSiteRng)));
-                    if (!ok) break;
-                    const uint32_t* ring =
-                        reinterpret_cast<const uint32_t*>(smem_raw + pad + C::OFF_RNG + rs * C::RNG_BYTES);
 #pragma unroll
                     for (int c32 = 0; c32 < HK / 32; ++c32) {
-                        const uint32_t bits = ring[(h * (HK / 32) + c32) * 128 + r];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) keep[8 * c32 + k] = (bits << k) & 0x80808080u;
+                        for (int k = 0; k < 8; ++k) keep[8 * c32 + k] = (kbits[c32] << k) & 0x80808080u;
                     }
-                    mbar_arrive(bar(bars->rng_empty[rs]));
                 }
                 ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
                 if (!ok) break;
