@@ -49,6 +49,27 @@ def random_inputs(b: int, h_q: int, h_kv: int, s: int, d: int, seed: int, s_kv: 
     return Tensors(q, k, v, dout)
 
 
+def growing_scores_inputs(b: int, h_q: int, h_kv: int, s: int, d: int, seed: int) -> Tensors:
+    """bf16 inputs whose first two 128-key blocks score far below the rest, on the CPU.
+
+    Q entries are 0.75 + 0.75 N(0,1); K rows have N(0,1) entries plus a common
+    mean that puts the scaled scores of keys 0..127 about 20 and of keys
+    128..255 about 10 below the others (mean offset / (0.75 sqrt(d)) per entry).
+    A query that sees key block 2 then finds its running row maximum rising by
+    about 10 at block 1 and again at block 2, while the early keys keep
+    probabilities near zero (no large common component of K is left for the
+    gradients to cancel).  V and dO are N(0,1)."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = (0.75 + 0.75 * torch.randn((b, h_q, s, d), generator=g, dtype=torch.float32)).to(torch.bfloat16)
+    blk = torch.arange(s) // 128
+    offset = torch.where(blk == 0, -20.0, torch.where(blk == 1, -10.0, 0.0)).to(torch.float32)
+    mean_k = (offset / (0.75 * float(d) ** 0.5)).view(1, 1, s, 1)
+    k = (torch.randn((b, h_kv, s, d), generator=g, dtype=torch.float32) + mean_k).to(torch.bfloat16)
+    v = torch.randn((b, h_kv, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dout = torch.randn((b, h_q, s, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return Tensors(q, k, v, dout)
+
+
 def fwd_mask_probe(b: int, h_q: int, h_kv: int, s: int, d: int, w0: int) -> Tensors:
     """Inputs that expose the forward dropout mask on a window of keys.
 

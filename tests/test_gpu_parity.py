@@ -10,7 +10,7 @@ import torch
 import attention_core_gb300 as ac
 import oracle
 from attention_core_gb300.inputs import (dq_mask_probe, dv_mask_probe, fwd_mask_probe,
-                                         random_inputs)
+                                         growing_scores_inputs, random_inputs)
 from tests.gpu_util import LSE_TOL, TOL, row_rel_err, run_gpu, to_np
 
 pytestmark = pytest.mark.gpu
@@ -59,6 +59,48 @@ def test_fwd_bwd_match_oracle(case):
     lse_err = float(np.abs(to_np(out["lse"]) - rlse).max())
     assert lse_err <= LSE_TOL, lse_err
     assert all(e <= TOL for e in errs.values()), errs
+
+
+# Key blocks 0 and 1 score far below the rest, so that for every query that sees key
+# block 2 the forward's running row maximum rises by more than its lazy-rescale
+# threshold (2^8) at blocks 1 and 2 and the O accumulator(s) are rescaled: each column
+# half's own accumulator for d <= 128, the shared one (with the block-maximum
+# exchange) for d = 160.  O and the LSE are compared in every case.  The gradients are
+# compared where every query sees the unshifted keys (not causal): under a causal
+# mask the first 256 queries attend only among the shifted keys, which share a large
+# common component, and their dQ = sum_j dS_ij K_j is then a residue of sum_j dS_ij = 0
+# that magnifies the bf16 rounding of dS beyond the 1e-2 bar, whatever the kernel.
+RESCALE = [
+    (1, 2, 2, 640, 128, True, 0.1),
+    (1, 4, 2, 400, 96, True, 0.2),
+    (1, 2, 2, 500, 160, True, 0.1),
+    (1, 2, 2, 520, 64, False, 0.0),
+    (1, 2, 2, 450, 96, False, 0.1),
+    (1, 2, 1, 384, 160, False, 0.2),
+]
+
+
+@pytest.mark.parametrize("case", RESCALE, ids=_ids)
+def test_growing_scores_rescale(case):
+    b, hq, hkv, s, d, causal, p = case
+    seed = 4242 + s + d
+    t = growing_scores_inputs(b, hq, hkv, s, d, seed=s * d)
+    # the test's premise: along the last query row (which sees every key), the largest
+    # score of key blocks 1 and 2 exceeds that of the block before by more than the
+    # lazy-rescale threshold, 2^8, i.e. 8 / log2(e) in the natural domain
+    sc = (t.q[0, 0].double() @ t.k[0, 0].double().T).numpy() / np.sqrt(d)
+    bmax = [sc[s - 1, j:j + 128].max() for j in (0, 128, 256)]
+    assert all(bmax[j + 1] - bmax[j] > 8.0 / np.log2(np.e) for j in range(2)), bmax
+    out = run_gpu(t, causal, p, seed)
+    pr = oracle.Problem(b=b, h_q=hq, h_kv=hkv, s=s, d=d, causal=causal, p_drop=p, seed=seed)
+    ro, rlse = oracle.fwd(pr, t.q, t.k, t.v)
+    assert float(np.abs(to_np(out["lse"]) - rlse).max()) <= LSE_TOL
+    assert row_rel_err(to_np(out["o"]), ro) <= TOL
+    if not causal:
+        rdq, rdk, rdv = oracle.bwd(pr, t.q, t.k, t.v, t.dout)
+        errs = {"dq": row_rel_err(to_np(out["dq"]), rdq), "dk": row_rel_err(to_np(out["dk"]), rdk),
+                "dv": row_rel_err(to_np(out["dv"]), rdv)}
+        assert all(e <= TOL for e in errs.values()), errs
 
 
 def test_custom_scale_and_offset():
