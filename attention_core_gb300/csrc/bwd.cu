@@ -34,6 +34,13 @@
 #include "tile.cuh"
 
 namespace ac {
+// The backward kernels' waits do not suspend (they retry after the hardware's
+// short try-wait limit): their row threads' dependency chains resume sooner, which
+// outweighs the issue slots a retrying warp takes (mbar_try_wait).
+constexpr bool kBwdSuspend = false;
+}  // namespace ac
+
+namespace ac {
 
 namespace {
 
@@ -242,7 +249,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
 
     bool alive = true;
-    if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
+    if (a.inject_timeout) alive = wait_bounded<kBwdSuspend>(wc, bar(bars->never), 0, timeout_code(kSiteInject));
 
     if (alive && warp == 0) {
         if (lane == 0) {
@@ -256,9 +263,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             uint32_t sf_parity = 0u;   // bit st: phase parity of slot st's stage_free
             KTile w;
             while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
-                ok = wait_bounded(wc, bar(bars->kv_empty), (u & 1) ^ 1, timeout_code(kSiteKvFull));
+                ok = wait_bounded<kBwdSuspend>(wc, bar(bars->kv_empty), (u & 1) ^ 1, timeout_code(kSiteKvFull));
                 if (ok && !RING_STAGE && u > 0)
-                    ok = wait_bounded(wc, bar(bars->kv_stage_free), (u - 1) & 1, timeout_code(kSiteStage));
+                    ok = wait_bounded<kBwdSuspend>(wc, bar(bars->kv_stage_free), (u - 1) & 1, timeout_code(kSiteStage));
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(bars->kv_full), 2 * C::KV_TILE);
                 for (int ch = 0; ch < G::NCH; ++ch) {
@@ -272,9 +279,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     int yq, zq;
                     size_t srow;
                     q_coords(w, it / w.per_head, qt, yq, zq, srow);
-                    ok = wait_bounded(wc, bar(bars->q_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteQEmpty));
+                    ok = wait_bounded<kBwdSuspend>(wc, bar(bars->q_empty[st]), ((g / ST) & 1) ^ 1, timeout_code(kSiteQEmpty));
                     if (ok && RING_STAGE && ((pending >> st) & 1u)) {
-                        ok = wait_bounded(wc, bar(bars->stage_free[st]), (sf_parity >> st) & 1u, timeout_code(kSiteStage));
+                        ok = wait_bounded<kBwdSuspend>(wc, bar(bars->stage_free[st]), (sf_parity >> st) & 1u, timeout_code(kSiteStage));
                         sf_parity ^= 1u << st;
                         pending &= ~(1u << st);
                     }
@@ -308,7 +315,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             KTile w;
             while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
                 g += w.n_it;
-                ok = wait_bounded(wc, bar(bars->out_staged), u & 1, timeout_code(kSiteStage));
+                ok = wait_bounded<kBwdSuspend>(wc, bar(bars->out_staged), u & 1, timeout_code(kSiteStage));
                 if (!ok) break;
                 const int slot = (g - 1 + 2 * ST) % ST;
                 const bool staged = !w.tail && (!RING_STAGE || w.n_it > 0);
@@ -357,8 +364,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             KTile w;
             while (ok && next_ktile<PACKED>(sched, a, BQ, vt, w)) {
                 const int n_it = w.n_it;
-                ok = wait_warp(wc, bar(bars->kv_full), u & 1, timeout_code(kSiteKvFull));
-                if (ok && n_it > 0) ok = wait_warp(wc, bar(bars->q_full[g % ST]), (g / ST) & 1, timeout_code(kSiteQFull));
+                ok = wait_warp<kBwdSuspend>(wc, bar(bars->kv_full), u & 1, timeout_code(kSiteKvFull));
+                if (ok && n_it > 0) ok = wait_warp<kBwdSuspend>(wc, bar(bars->q_full[g % ST]), (g / ST) & 1, timeout_code(kSiteQFull));
                 if (!ok) break;
                 tc_fence_after();
                 if (n_it > 0) {
@@ -371,10 +378,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     const int st = g % ST;
                     const uint32_t qbase = sb + C::OFF_Q + st * C::Q_TILE;
                     const uint32_t dobase = sb + C::OFF_DO + st * C::Q_TILE;
-                    ok = wait_warp(wc, bar(bars->p_full), g & 1, timeout_code(kSitePFull));
+                    ok = wait_warp<kBwdSuspend>(wc, bar(bars->p_full), g & 1, timeout_code(kSitePFull));
                     // the first dV product of a tile overwrites the accumulators: the
                     // epilogue of the tile before must have read them
-                    if (ok && it == 0) ok = wait_warp(wc, bar(bars->acc_free), (u & 1) ^ 1, timeout_code(kSiteAcc));
+                    if (ok && it == 0) ok = wait_warp<kBwdSuspend>(wc, bar(bars->acc_free), (u & 1) ^ 1, timeout_code(kSiteAcc));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -383,12 +390,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                                IDG, (it > 0 || kk > 0) ? 1u : 0u);
                     if (it + 1 < n_it) {
                         const int st1 = (g + 1) % ST;
-                        ok = wait_warp(wc, bar(bars->q_full[st1]), ((g + 1) / ST) & 1, timeout_code(kSiteQFull));
+                        ok = wait_warp<kBwdSuspend>(wc, bar(bars->q_full[st1]), ((g + 1) / ST) & 1, timeout_code(kSiteQFull));
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(g + 1);
                     }
-                    ok = wait_warp(wc, bar(bars->ds_full), g & 1, timeout_code(kSiteDsFull));
+                    ok = wait_warp<kBwdSuspend>(wc, bar(bars->ds_full), g & 1, timeout_code(kSiteDsFull));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -407,7 +414,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             // every MMA must be complete before the CTA releases TMEM
             mma_commit(bar(bars->drain));
-            wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
+            wait_warp<kBwdSuspend>(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 4) {
         // ---- row threads: key = TMEM lane, half = which BQ/2 queries of a tile
@@ -455,7 +462,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const int st = g % ST;
             const int q0 = (w.qt0 + it % w.per_head) * BQ + HQ * h;     // this half's first query
             ok = __all_sync(0xffffffffu,
-                            wait_bounded(wc, bar(bars->q_full[st]), (g / ST) & 1, timeout_code(kSiteQFull)));
+                            wait_bounded<kBwdSuspend>(wc, bar(bars->q_full[st]), (g / ST) & 1, timeout_code(kSiteQFull)));
             if (!ok) break;
             // The keep bits came with this query tile's stage: their transpose needs no
             // score, so it runs while the tensor core forms S^T.
@@ -470,7 +477,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     for (int n = 0; n < 8; ++n) kbyte[8 * c + n] = keep_nibble_bytes((col >> (4 * n)) & 0xFu);
                 }
             }
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
+            ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
             if (!ok) break;
             tc_fence_after();
             // per-query row statistics of this half (-LSE log2(e) and -D), four at a time
@@ -529,7 +536,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_before();
             mbar_arrive(bar(bars->p_full));
 
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
+            ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -561,7 +568,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (DROP && !MWS && it + 1 < n_it) draw_mask(w, it + 1);
         }
         if (!ok) break;
-        ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), u & 1, timeout_code(kSiteAcc)));
+        ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->acc_done), u & 1, timeout_code(kSiteAcc)));
         if (!ok) break;
         // dV and dK of this key row: staged for the TMA store of the tile (in the
         // query-ring slot of its last iteration, or the K and V buffers), or -- a
@@ -611,7 +618,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         fence_proxy_async_smem();
         // the store lane takes one tile at a time: a tile is handed over only after
         // the previous one is done (tiles without queries can follow one another fast)
-        if (u > 0) ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->out_read), (u - 1) & 1, timeout_code(kSiteStage)));
+        if (u > 0) ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->out_read), (u - 1) & 1, timeout_code(kSiteStage)));
         if (!ok) break;
         mbar_arrive(bar(bars->out_staged));
         ++u;
@@ -780,7 +787,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const WaitCtx wc{&bars->abort_flag, a.status, a.timeout_ns};
 
     bool alive = true;
-    if (a.inject_timeout) alive = wait_bounded(wc, bar(bars->never), 0, timeout_code(kSiteInject));
+    if (a.inject_timeout) alive = wait_bounded<kBwdSuspend>(wc, bar(bars->never), 0, timeout_code(kSiteInject));
 
     // Registers: the row warps raise their share to kDqRowRegs (176), every
     // other warp lowers its own to kDqOtherRegs (80); kernels.h checks the sum
@@ -796,7 +803,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             while (ok && next_qtile<PACKED>(sched, a, BN, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % KST;
-                    ok = wait_bounded(wc, bar(bars->k_empty[st]), ((g / KST) & 1) ^ 1, timeout_code(kSiteKEmpty));
+                    ok = wait_bounded<kBwdSuspend>(wc, bar(bars->k_empty[st]), ((g / KST) & 1) ^ 1, timeout_code(kSiteKEmpty));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->k_full[st]), C::KT);
                     for (int ch = 0; ch < G::NCH; ++ch)
@@ -818,7 +825,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             bool have = next_qtile<PACKED>(sched, a, BN, vt, w);
             for (int u = 0;; ++u) {
                 if (have) {
-                    if (!wait_bounded(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
+                    if (!wait_bounded<kBwdSuspend>(wc, bar(bars->q_empty), (u & 1) ^ 1, timeout_code(kSiteQEmpty))) break;
                     mbar_arrive_expect_tx(bar(bars->q_full), 2 * C::QT);
                     for (int ch = 0; ch < G::NCH; ++ch) {
                         tma_load_3d(sb + C::OFF_Q + ch * C::QCH, &tm_q, ch * G::CW, w.yq, w.zq, bar(bars->q_full));
@@ -826,7 +833,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                 }
                 if (u > 0) {
-                    if (!wait_bounded(wc, bar(bars->dq_staged), (u - 1) & 1, timeout_code(kSiteStage))) break;
+                    if (!wait_bounded<kBwdSuspend>(wc, bar(bars->dq_staged), (u - 1) & 1, timeout_code(kSiteStage))) break;
                     if (!prev.tail) {
                         for (int ch = 0; ch < G::NCH; ++ch)
                             tma_store_3d(&tm_dq, sb + C::OFF_O + ch * C::QCH, ch * G::CW, prev.yq, prev.zq);
@@ -862,7 +869,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             while (ok && next_qtile<PACKED>(sched, a, BN, vt, w)) {
                 for (int j = 0; j < w.nk; ++j, ++g) {
                     const int st = g % VST;
-                    ok = wait_bounded(wc, bar(bars->v_empty[st]), ((g / VST) & 1) ^ 1, timeout_code(kSiteVEmpty));
+                    ok = wait_bounded<kBwdSuspend>(wc, bar(bars->v_empty[st]), ((g / VST) & 1) ^ 1, timeout_code(kSiteVEmpty));
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(bars->v_full[st]), C::KT);
                     for (int ch = 0; ch < G::NCH; ++ch)
@@ -882,7 +889,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             constexpr uint32_t IDQ = idesc_bf16(128, D, false, true);    // dQ~ += dS~ K, PK += P K
             auto issue_s = [&](int g) -> bool {
                 const int st = g % KST;
-                if (!wait_warp(wc, bar(bars->k_full[st]), (g / KST) & 1, timeout_code(kSiteKFull))) return false;
+                if (!wait_warp<kBwdSuspend>(wc, bar(bars->k_full[st]), (g / KST) & 1, timeout_code(kSiteKFull))) return false;
                 tc_fence_after();
                 const uint32_t kbase = sb + C::OFF_K + st * C::KT;
 #pragma unroll
@@ -894,7 +901,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             };
             auto issue_dp = [&](int g) -> bool {
                 const int st = g % VST;
-                if (!wait_warp(wc, bar(bars->v_full[st]), (g / VST) & 1, timeout_code(kSiteVFull))) return false;
+                if (!wait_warp<kBwdSuspend>(wc, bar(bars->v_full[st]), (g / VST) & 1, timeout_code(kSiteVFull))) return false;
                 tc_fence_after();
                 const uint32_t vbase = sb + C::OFF_V + st * C::KT;
 #pragma unroll
@@ -911,7 +918,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             QTile w;
             for (int u = 0; ok && next_qtile<PACKED>(sched, a, BN, vt, w); ++u) {
                 const int g0 = g;
-                ok = wait_warp(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
+                ok = wait_warp<kBwdSuspend>(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull));
                 if (ok) ok = issue_s(g0);
                 if (ok) ok = issue_dp(g0);
                 // Q and dO are free once the tile's last S and dP products are done
@@ -919,11 +926,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int j = 0; j < w.nk && ok; ++j, ++g) {
                     const int st = g % KST;
                     const uint32_t kbase = sb + C::OFF_K + st * C::KT;
-                    ok = wait_warp(wc, bar(bars->p_full), g & 1, timeout_code(kSitePRead));
+                    ok = wait_warp<kBwdSuspend>(wc, bar(bars->p_full), g & 1, timeout_code(kSitePRead));
                     // the first P K of a tile overwrites PK: the epilogue of the tile
                     // before must have read the accumulators
                     if (ok && j == 0)
-                        ok = wait_warp(wc, bar(bars->acc_free), (u & 1) ^ 1, timeout_code(kSiteAcc));
+                        ok = wait_warp<kBwdSuspend>(wc, bar(bars->acc_free), (u & 1) ^ 1, timeout_code(kSiteAcc));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -934,7 +941,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         ok = issue_s(g + 1);      // overwrites P_j: after PK_j in the tensor pipe
                         if (!ok) break;
                     }
-                    ok = wait_warp(wc, bar(bars->ds_full), g & 1, timeout_code(kSiteDsFull));
+                    ok = wait_warp<kBwdSuspend>(wc, bar(bars->ds_full), g & 1, timeout_code(kSiteDsFull));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -951,7 +958,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             // every MMA must be complete before the CTA releases TMEM
             mma_commit(bar(bars->drain));
-            wait_warp(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
+            wait_warp<kBwdSuspend>(wc, bar(bars->drain), 0, timeout_code(kSiteDrain));
         }
     } else if (alive && warp >= 12 && DROP) {
         regs_lower<kDqOtherRegs>();
@@ -970,7 +977,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint32_t bhc = (uint32_t)w.bh + a.bh0;
             for (int j = 0; j < w.nk; ++j, ++g) {
                 const int rs = g % C::RNG_ST;
-                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->rng_empty[rs]), ((g / C::RNG_ST) & 1) ^ 1,
+                ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->rng_empty[rs]), ((g / C::RNG_ST) & 1) ^ 1,
                                                           timeout_code(kSiteRng)));
                 if (!ok) break;
                 uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw + pad + C::OFF_RNG + rs * C::RNG_BYTES);
@@ -1040,7 +1047,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 uint32_t kbits[HK / 32];
                 if (DROP) {
                     const int rs = g % C::RNG_ST;
-                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->rng_full[rs]), (g / C::RNG_ST) & 1,
+                    ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->rng_full[rs]), (g / C::RNG_ST) & 1,
                                                               timeout_code(kSiteRng)));
                     if (!ok) break;
                     const uint32_t* ring =
@@ -1049,7 +1056,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int c32 = 0; c32 < HK / 32; ++c32) kbits[c32] = ring[(h * (HK / 32) + c32) * 128 + r];
                     mbar_arrive(bar(bars->rng_empty[rs]));
                 }
-                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
+                ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->s_full), g & 1, timeout_code(kSiteSFull)));
                 if (!ok) break;
                 tc_fence_after();
                 uint64_t pp[HK / 2];
@@ -1102,10 +1109,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tc_fence_before();
                 mbar_arrive(bar(bars->p_full));
                 if (j == 0) {
-                    ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->o_full), u & 1, timeout_code(kSiteOFull)));
+                    ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->o_full), u & 1, timeout_code(kSiteOFull)));
                     if (ok)
                         ok = __all_sync(0xffffffffu,
-                                        wait_bounded(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull)));
+                                        wait_bounded<kBwdSuspend>(wc, bar(bars->q_full), u & 1, timeout_code(kSiteQFull)));
                     if (!ok) break;
                     uint64_t acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
@@ -1139,7 +1146,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         for (int k = 0; k < 8; ++k) keep[8 * c32 + k] = (kbits[c32] << k) & 0x80808080u;
                     }
                 }
-                ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
+                ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->dp_full), g & 1, timeout_code(kSiteDpFull)));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -1177,13 +1184,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 d_exact = DROP ? (lo + hi) * a.keep_scale : lo + hi;   // dP = Z dP_d, Z = keep / (1 - p)
             }
             dred[h * 128 + r] = d_exact;
-            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xbar), nx++ & 1, timeout_code(kSiteX)));
+            ok = __all_sync(0xffffffffu, row_barrier<kBwdSuspend>(wc, bar(bars->xbar), nx++ & 1, timeout_code(kSiteX)));
             if (!ok) break;
             d_exact += dred[(h ^ 1) * 128 + r];
             // every row thread has read the region before anyone writes it again
-            ok = __all_sync(0xffffffffu, row_barrier(wc, bar(bars->xbar), nx++ & 1, timeout_code(kSiteX)));
+            ok = __all_sync(0xffffffffu, row_barrier<kBwdSuspend>(wc, bar(bars->xbar), nx++ & 1, timeout_code(kSiteX)));
             if (!ok) break;
-            ok = __all_sync(0xffffffffu, wait_bounded(wc, bar(bars->acc_done), u & 1, timeout_code(kSiteAcc)));
+            ok = __all_sync(0xffffffffu, wait_bounded<kBwdSuspend>(wc, bar(bars->acc_done), u & 1, timeout_code(kSiteAcc)));
             if (!ok) break;
             tc_fence_after();
             const float eps = d_exact - d_tilde;
